@@ -1,0 +1,272 @@
+/*
+ * pa_oracle.c -- plain, slow, obviously correct CPU oracle for exact paged
+ * attention, in fp64.  TEST INFRASTRUCTURE ONLY: nothing on the product path
+ * links, loads or calls this file.  It shares no code with the CUDA library.
+ *
+ * The method, as the pages define it, and the function below that follows it:
+ *
+ *   gather_one()  -- "Week 3 Day 5: Paged FlashAttention", Task 1: every
+ *                    logical key position s is translated through the block
+ *                    table (logical_page = s / page_size, slot = s % page_size,
+ *                    physical_page = block_table[batch, logical_page]) and the
+ *                    row pages[physical_page, kv_head, slot, :] is read.  The
+ *                    whole history is first gathered into a contiguous buffer,
+ *                    as the reference of "Day 22: the fused paged-attention
+ *                    kernel" (What I added today) does.
+ *   kv_head_of()  -- "Week 2 Day 5: Fused Decode Attention", Task 1:
+ *                    kv_head = query_head / (H_q / H_kv).
+ *   attend_row()  -- scaled scores, softmax, weighted sum of values, written
+ *                    out explicitly ("Week 2 Day 5", Task 1: the readable
+ *                    equation kept as the oracle), restricted to the visible
+ *                    keys s <= l + context_len - L under the causal rule of
+ *                    "Week 3 Day 5", Task 2.  Natural exp in double; the max
+ *                    is subtracted before exponentiating (stable softmax).
+ *
+ * No tiling, no online rescaling, no reordering beyond the definition.
+ * Parallelism: independent (batch, kv_head) items run on OpenMP threads; each
+ * row is computed by one thread in the definition's order.
+ *
+ * ORACLE_MUTANT (compile-time, default 0) plants one deliberate mistake.  It
+ * exists only so that the CPU test suite can show that its pins catch such
+ * mistakes; the normal build never defines it.
+ */
+#include "pa_oracle.h"
+
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#ifndef ORACLE_MUTANT
+#define ORACLE_MUTANT 0
+#endif
+
+/* Exact widening of one stored element to double. */
+static double widen(const void* base, int dtype, int64_t idx) {
+    if (dtype == 0) {
+        uint32_t u = (uint32_t)((const uint16_t*)base)[idx] << 16;
+        float f;
+        memcpy(&f, &u, sizeof f);
+        return (double)f;
+    }
+    return (double)((const float*)base)[idx];
+}
+
+static int check_shape(const oracle_shape* sh) {
+    if (!sh) return ORACLE_ERR_INVALID_ARG;
+    if (sh->B < 1 || sh->H_q < 1 || sh->H_kv < 1 || sh->L < 1 || sh->D < 1 ||
+        sh->num_pages < 1 || sh->page_size < 1 || sh->max_pages_per_seq < 1)
+        return ORACLE_ERR_INVALID_ARG;
+    if (sh->H_q % sh->H_kv != 0) return ORACLE_ERR_INVALID_ARG;
+    if (sh->dtype != 0 && sh->dtype != 1) return ORACLE_ERR_INVALID_ARG;
+    return ORACLE_OK;
+}
+
+/* Validates what the method will read for sequence b: its context length and
+ * the block-table entries of its ceil(S / page_size) logical pages. */
+static int check_sequence(const oracle_shape* sh, const int32_t* block_table,
+                          const int32_t* context_lens, int b, int causal) {
+    const int S = context_lens[b];
+    if (S < 1 || (int64_t)S > (int64_t)sh->max_pages_per_seq * sh->page_size)
+        return ORACLE_ERR_INVALID_ARG;
+    if (causal && sh->L > S) return ORACLE_ERR_INVALID_ARG;
+    const int npg = (S + sh->page_size - 1) / sh->page_size;
+    for (int lp = 0; lp < npg; ++lp) {
+        const int32_t pp = block_table[(int64_t)b * sh->max_pages_per_seq + lp];
+        if (pp < 0 || pp >= sh->num_pages) return ORACLE_ERR_BAD_BLOCK_TABLE;
+    }
+    return ORACLE_OK;
+}
+
+static int kv_head_of(const oracle_shape* sh, int h) {
+#if ORACLE_MUTANT == 2
+    return h % sh->H_kv; /* planted: wrong GQA head map */
+#else
+    return h / (sh->H_q / sh->H_kv);
+#endif
+}
+
+/* Gathers the S logical rows of (b, kvh) into K[S][D], V[S][D]. */
+static void gather_one(const oracle_shape* sh, const void* key_pages, const void* value_pages,
+                       const int32_t* block_table, int b, int kvh, int S, double* K,
+                       double* V) {
+    const int ps = sh->page_size, D = sh->D;
+    for (int s = 0; s < S; ++s) {
+        const int logical_page = s / ps;
+        const int slot = s % ps;
+#if ORACLE_MUTANT == 3
+        const int64_t physical_page = logical_page; /* planted: block table ignored */
+#else
+        const int64_t physical_page =
+            block_table[(int64_t)b * sh->max_pages_per_seq + logical_page];
+#endif
+        const int64_t row = ((physical_page * sh->H_kv + kvh) * ps + slot) * (int64_t)D;
+        for (int d = 0; d < D; ++d) {
+#if ORACLE_MUTANT == 5
+            K[(int64_t)s * D + d] = widen(value_pages, sh->dtype, row + d); /* planted: K/V swapped */
+            V[(int64_t)s * D + d] = widen(key_pages, sh->dtype, row + d);
+#else
+            K[(int64_t)s * D + d] = widen(key_pages, sh->dtype, row + d);
+            V[(int64_t)s * D + d] = widen(value_pages, sh->dtype, row + d);
+#endif
+        }
+    }
+}
+
+/* One output row (b, h, l) from the gathered K/V of its kv head.
+ * x is scratch for S scores, o receives D outputs. */
+static void attend_row(const oracle_shape* sh, const void* query, int b, int h, int l, int S,
+                       const double* K, const double* V, double scale, int causal, double* x,
+                       double* o) {
+    const int D = sh->D, L = sh->L;
+    const int64_t qbase = (((int64_t)b * sh->H_q + h) * L + l) * D;
+    /* last visible key: s <= l + S - L under causal, s <= S - 1 otherwise */
+#if ORACLE_MUTANT == 1
+    int last = causal ? l + S - L - 1 : S - 1; /* planted: causal off by one */
+#elif ORACLE_MUTANT == 7
+    int last = causal ? l - S + L : S - 1; /* planted: causal offset sign flipped */
+#else
+    int last = causal ? l + S - L : S - 1;
+#endif
+    if (last > S - 1) last = S - 1;
+
+    double M = -INFINITY;
+    for (int s = 0; s <= last; ++s) {
+        double acc = 0.0;
+        for (int d = 0; d < D; ++d) acc += widen(query, sh->dtype, qbase + d) * K[(int64_t)s * D + d];
+#if ORACLE_MUTANT == 4
+        x[s] = acc; /* planted: scale dropped */
+#else
+        x[s] = scale * acc;
+#endif
+        if (x[s] > M) M = x[s];
+    }
+    double den = 0.0;
+    for (int d = 0; d < D; ++d) o[d] = 0.0;
+    for (int s = 0; s <= last; ++s) {
+        const double w = exp(x[s] - M);
+#if ORACLE_MUTANT == 6
+        if (s > 0) den += w; /* planted: a dropped term in the normaliser */
+#else
+        den += w;
+#endif
+        for (int d = 0; d < D; ++d) o[d] += w * V[(int64_t)s * D + d];
+    }
+    for (int d = 0; d < D; ++d) o[d] /= den;
+}
+
+static int validate_all(const oracle_shape* sh, const int32_t* block_table,
+                        const int32_t* context_lens, int causal) {
+    int st = check_shape(sh);
+    if (st) return st;
+    for (int b = 0; b < sh->B; ++b) {
+        st = check_sequence(sh, block_table, context_lens, b, causal);
+        if (st) return st;
+    }
+    return ORACLE_OK;
+}
+
+int oracle_gather(const oracle_shape* sh, const void* key_pages, const void* value_pages,
+                  const int32_t* block_table, const int32_t* context_lens, int max_S,
+                  double* k_dense, double* v_dense) {
+    if (!key_pages || !value_pages || !block_table || !context_lens || !k_dense || !v_dense)
+        return ORACLE_ERR_INVALID_ARG;
+    int st = validate_all(sh, block_table, context_lens, 0);
+    if (st) return st;
+    const int D = sh->D;
+    for (int b = 0; b < sh->B; ++b)
+        if (context_lens[b] > max_S) return ORACLE_ERR_INVALID_ARG;
+    for (int b = 0; b < sh->B; ++b) {
+        for (int kvh = 0; kvh < sh->H_kv; ++kvh) {
+            const int64_t base = ((int64_t)b * sh->H_kv + kvh) * max_S * D;
+            memset(k_dense + base, 0, sizeof(double) * (size_t)max_S * D);
+            memset(v_dense + base, 0, sizeof(double) * (size_t)max_S * D);
+            gather_one(sh, key_pages, value_pages, block_table, b, kvh, context_lens[b],
+                       k_dense + base, v_dense + base);
+        }
+    }
+    return ORACLE_OK;
+}
+
+int oracle_paged_attention(const oracle_shape* sh, const void* query, const void* key_pages,
+                           const void* value_pages, const int32_t* block_table,
+                           const int32_t* context_lens, double scale, int causal,
+                           double* out, int num_threads) {
+    if (!query || !key_pages || !value_pages || !block_table || !context_lens || !out)
+        return ORACLE_ERR_INVALID_ARG;
+    int st = validate_all(sh, block_table, context_lens, causal);
+    if (st) return st;
+    const int G = sh->H_q / sh->H_kv, D = sh->D;
+    const int n_items = sh->B * sh->H_kv;
+    int failed = 0;
+#ifdef _OPENMP
+    if (num_threads <= 0) num_threads = omp_get_max_threads();
+#pragma omp parallel for schedule(dynamic, 1) num_threads(num_threads)
+#endif
+    for (int item = 0; item < n_items; ++item) {
+        const int b = item / sh->H_kv, kvh = item % sh->H_kv;
+        const int S = context_lens[b];
+        double* K = (double*)malloc(sizeof(double) * (size_t)S * D);
+        double* V = (double*)malloc(sizeof(double) * (size_t)S * D);
+        double* x = (double*)malloc(sizeof(double) * (size_t)S);
+        if (!K || !V || !x) {
+            failed = 1;
+        } else {
+            gather_one(sh, key_pages, value_pages, block_table, b, kvh, S, K, V);
+            for (int h = 0; h < sh->H_q; ++h) {
+                if (kv_head_of(sh, h) != kvh) continue;
+                for (int l = 0; l < sh->L; ++l)
+                    attend_row(sh, query, b, h, l, S, K, V, scale, causal, x,
+                               out + (((int64_t)b * sh->H_q + h) * sh->L + l) * D);
+            }
+        }
+        free(K);
+        free(V);
+        free(x);
+    }
+    (void)G;
+    return failed ? ORACLE_ERR_NOMEM : ORACLE_OK;
+}
+
+int oracle_paged_attention_rows(const oracle_shape* sh, const void* query,
+                                const void* key_pages, const void* value_pages,
+                                const int32_t* block_table, const int32_t* context_lens,
+                                double scale, int causal, const int32_t* rows, int n_rows,
+                                double* out, int num_threads) {
+    if (!query || !key_pages || !value_pages || !block_table || !context_lens || !out ||
+        (!rows && n_rows > 0) || n_rows < 0)
+        return ORACLE_ERR_INVALID_ARG;
+    int st = validate_all(sh, block_table, context_lens, causal);
+    if (st) return st;
+    for (int i = 0; i < n_rows; ++i) {
+        const int b = rows[3 * i], h = rows[3 * i + 1], l = rows[3 * i + 2];
+        if (b < 0 || b >= sh->B || h < 0 || h >= sh->H_q || l < 0 || l >= sh->L)
+            return ORACLE_ERR_INVALID_ARG;
+    }
+    const int D = sh->D;
+    int failed = 0;
+#ifdef _OPENMP
+    if (num_threads <= 0) num_threads = omp_get_max_threads();
+#pragma omp parallel for schedule(dynamic, 1) num_threads(num_threads)
+#endif
+    for (int i = 0; i < n_rows; ++i) {
+        const int b = rows[3 * i], h = rows[3 * i + 1], l = rows[3 * i + 2];
+        const int S = context_lens[b];
+        const int kvh = kv_head_of(sh, h);
+        double* K = (double*)malloc(sizeof(double) * (size_t)S * D);
+        double* V = (double*)malloc(sizeof(double) * (size_t)S * D);
+        double* x = (double*)malloc(sizeof(double) * (size_t)S);
+        if (!K || !V || !x) {
+            failed = 1;
+        } else {
+            gather_one(sh, key_pages, value_pages, block_table, b, kvh, S, K, V);
+            attend_row(sh, query, b, h, l, S, K, V, scale, causal, x, out + (int64_t)i * D);
+        }
+        free(K);
+        free(V);
+        free(x);
+    }
+    return failed ? ORACLE_ERR_NOMEM : ORACLE_OK;
+}

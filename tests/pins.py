@@ -1,0 +1,349 @@
+"""Pins for the fp64 oracle: checks against facts fixed by the pages and by
+mathematics, not against the oracle itself.
+
+Each ``pin_*`` function takes an ``oracle.OracleLib`` and raises
+``AssertionError`` (or ``oracle.OracleError``) when the oracle disagrees.
+They are used twice: by test_oracle_pins.py on the real oracle, and by
+test_oracle_mutants.py on builds with one planted mistake, to show that every
+planted mistake trips at least one pin.
+
+The facts:
+  * brute force: a separately written dense attention on the *logical* K/V
+    (never paged), with the visibility mask materialised as an L x S matrix
+    ("Week 2 Day 5: Fused Decode Attention", Task 1 normalises masks to
+    [B*H_q, L, S]) and scipy's softmax;
+  * a library routine: torch's scaled_dot_product_attention in float64 where
+    its causal convention coincides with the pages' (non-causal, or L == S);
+  * invariants: physical page permutation ("Week 3 Day 5: Paged
+    FlashAttention", Task 1: physical ids need not be consecutive), block-table
+    entries past the last page are never read, GQA equals explicit head
+    repetition ("Week 2 Day 5", Task 1: broadcasting pairs heads without
+    repeating K/V);
+  * tile-size independence of a streaming online-softmax fold ("Day 22: the
+    fused paged-attention kernel", What I learned 1 and 3);
+  * closed forms: a dominant key gives exactly its value row; identical keys
+    give the mean of exactly the visible value rows, which fixes the causal
+    boundary s <= l + context_len - L ("Week 3 Day 5", Task 2) to the key.
+"""
+from __future__ import annotations
+
+import json
+import math
+import os
+
+import numpy as np
+import scipy.special
+
+import oracle as oracle_mod
+from paged_kv_cache_03_gb300.synth import bf16_bits, bf16_to_f32
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+TOL = 1e-12
+
+
+def golden(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+# --------------------------------------------------------------------------
+# Paged case built from logical tensors (test side, independent of synth's
+# pool generator): logical K/V are drawn first, then scattered into a pool.
+# --------------------------------------------------------------------------
+class Case:
+    pass
+
+
+def make_case(seed, B, H_q, H_kv, L, D, ps, ctx, *, num_pages=None, dtype="bf16",
+              perm=None, k_mult=1.0, q=None, K=None, V=None, causal=True, scale=None):
+    rng = np.random.default_rng(seed)
+    ctx = np.asarray(ctx, dtype=np.int32)
+    Smax = int(ctx.max())
+
+    def draw(shape, mult=1.0):
+        v = rng.standard_normal(shape).astype(np.float32) * np.float32(mult)
+        if dtype == "bf16":
+            bits = bf16_bits(v)
+            return bits, bf16_to_f32(bits).astype(np.float64)
+        return v, v.astype(np.float64)
+
+    c = Case()
+    if q is None:
+        c.q_store, c.q = draw((B, H_q, L, D))
+    else:
+        c.q_store, c.q = q
+    if K is None:
+        c.K_store, c.K = draw((B, H_kv, Smax, D), k_mult)
+    else:
+        c.K_store, c.K = K
+    if V is None:
+        c.V_store, c.V = draw((B, H_kv, Smax, D))
+    else:
+        c.V_store, c.V = V
+    npg = [(int(s) + ps - 1) // ps for s in ctx]
+    need = sum(npg)
+    P = num_pages if num_pages is not None else need + 3
+    if perm is None:
+        perm = rng.permutation(P)
+    perm = np.asarray(perm)
+    maxnpg = max(npg) + 1
+    bt = np.full((B, maxnpg), -1, dtype=np.int32)
+    sdt = np.uint16 if dtype == "bf16" else np.float32
+    # every pool slot starts as noise, so a stray read would show
+    kp, _ = draw((P, H_kv, ps, D))
+    vp, _ = draw((P, H_kv, ps, D))
+    kp = np.ascontiguousarray(kp.astype(sdt))
+    vp = np.ascontiguousarray(vp.astype(sdt))
+    off = 0
+    for b in range(B):
+        for lp in range(npg[b]):
+            page = int(perm[off])
+            off += 1
+            bt[b, lp] = page
+            for slot in range(ps):
+                s = lp * ps + slot
+                if s < ctx[b]:
+                    kp[page, :, slot, :] = c.K_store[b, :, s, :]
+                    vp[page, :, slot, :] = c.V_store[b, :, s, :]
+    c.kp, c.vp, c.bt, c.ctx = kp, vp, bt, ctx
+    c.q_store = np.ascontiguousarray(c.q_store)
+    c.B, c.H_q, c.H_kv, c.L, c.D, c.ps = B, H_q, H_kv, L, D, ps
+    c.causal = causal
+    c.scale = float(np.float32(1.0 / math.sqrt(D) if scale is None else scale))
+    return c
+
+
+def run_oracle(lib, c, bt=None):
+    return lib.paged_attention(c.q_store, c.kp, c.vp, c.bt if bt is None else bt, c.ctx,
+                               c.scale, c.causal)
+
+
+def visible_mask(L, S, causal):
+    s = np.arange(S)[None, :]
+    l = np.arange(L)[:, None]
+    return (s <= l + S - L) if causal else np.ones((L, S), dtype=bool)
+
+
+def dense_bruteforce(c):
+    """Dense attention on the logical tensors with a materialised mask."""
+    G = c.H_q // c.H_kv
+    out = np.zeros((c.B, c.H_q, c.L, c.D))
+    for b in range(c.B):
+        S = int(c.ctx[b])
+        Kr = np.repeat(c.K[b, :, :S], G, axis=0)  # [H_q, S, D]
+        Vr = np.repeat(c.V[b, :, :S], G, axis=0)
+        scores = np.einsum("hld,hsd->hls", c.q[b], Kr) * c.scale
+        scores = np.where(visible_mask(c.L, S, c.causal)[None], scores, -np.inf)
+        P = scipy.special.softmax(scores, axis=-1)
+        out[b] = np.einsum("hls,hsd->hld", P, Vr)
+    return out
+
+
+def assert_close(a, b, tol=TOL, what=""):
+    err = np.max(np.abs(np.asarray(a) - np.asarray(b)))
+    assert np.all(np.isfinite(a)), f"{what}: non-finite output"
+    assert err <= tol, f"{what}: max abs err {err:.3e} > {tol:.1e}"
+
+
+# --------------------------------------------------------------------------
+# Pins
+# --------------------------------------------------------------------------
+BRUTE_CASES = [
+    # (seed, B, H_q, H_kv, L, D, ps, ctx, causal, dtype)
+    (11, 2, 4, 2, 5, 128, 16, [13, 40], True, "bf16"),   # the tiny workload's shape
+    (12, 2, 4, 2, 3, 8, 3, [7, 20], True, "bf16"),
+    (13, 1, 2, 1, 4, 16, 1, [9], True, "bf16"),
+    (14, 2, 4, 4, 6, 8, 5, [6, 33], True, "f32"),
+    (15, 2, 6, 2, 2, 8, 4, [17, 2], False, "bf16"),
+    (16, 1, 4, 2, 1, 32, 16, [40], True, "f32"),
+]
+
+
+def pin_bruteforce(lib):
+    for seed, B, Hq, Hkv, L, D, ps, ctx, causal, dt in BRUTE_CASES:
+        c = make_case(seed, B, Hq, Hkv, L, D, ps, ctx, dtype=dt, causal=causal)
+        assert_close(run_oracle(lib, c), dense_bruteforce(c), what=f"bruteforce seed {seed}")
+
+
+def pin_torch_sdpa(lib):
+    import torch
+    import torch.nn.functional as F
+    for seed, B, Hq, Hkv, L, D, ps, S, causal in [
+        (21, 1, 4, 2, 24, 16, 5, 24, True),    # L == S: torch's causal convention agrees
+        (22, 2, 2, 1, 3, 32, 4, 19, False),
+        (23, 1, 8, 2, 9, 128, 16, 9, True),
+    ]:
+        c = make_case(seed, B, Hq, Hkv, L, D, ps, [S] * B, causal=causal)
+        G = Hq // Hkv
+        q = torch.from_numpy(c.q)
+        K = torch.from_numpy(np.repeat(c.K[:, :, :S], G, axis=1))
+        V = torch.from_numpy(np.repeat(c.V[:, :, :S], G, axis=1))
+        ref = F.scaled_dot_product_attention(q, K, V, is_causal=causal, scale=c.scale)
+        assert_close(run_oracle(lib, c), ref.numpy(), what=f"sdpa seed {seed}")
+
+
+def pin_page_permutation(lib):
+    base = dict(B=2, H_q=4, H_kv=2, L=3, D=16, ps=4, ctx=[15, 9])
+    outs = []
+    need = 4 + 3
+    for perm in (np.arange(need), np.random.default_rng(5).permutation(need),
+                 np.random.default_rng(6).permutation(need)[::-1].copy()):
+        c = make_case(31, num_pages=need, perm=perm, **base)
+        outs.append(run_oracle(lib, c))
+    for o in outs[1:]:
+        assert np.array_equal(o, outs[0]), "output depends on physical page placement"
+    assert_close(outs[0], dense_bruteforce(c), what="permutation case")
+
+
+def pin_unused_table_entries(lib):
+    c = make_case(41, 2, 2, 1, 2, 16, 8, [17, 8])
+    ref = run_oracle(lib, c)
+    for fill in (-1, 0, 2 ** 31 - 1, c.kp.shape[0]):
+        bt = c.bt.copy()
+        for b in range(c.B):
+            npg = (int(c.ctx[b]) + c.ps - 1) // c.ps
+            bt[b, npg:] = fill
+        assert np.array_equal(run_oracle(lib, c, bt), ref), f"unused entry {fill} was read"
+
+
+def _online_fold(q, K, V, last, scale, tile):
+    """Streaming fold of the keys 0..last in tiles, keeping a running max,
+    running denominator and running weighted-V sum; the old state is
+    rescaled by exp(m_old - m_new) whenever the max moves up."""
+    D = q.shape[0]
+    m, den, acc = -np.inf, 0.0, np.zeros(D)
+    S = K.shape[0]
+    for t0 in range(0, S, tile):
+        idx = np.arange(t0, min(t0 + tile, S))
+        valid = idx <= last
+        x = np.where(valid, scale * (K[idx] @ q), -np.inf)
+        m_new = max(m, float(x.max()))
+        if m_new == -np.inf:
+            continue
+        corr = math.exp(m - m_new) if m > -np.inf else 0.0
+        p = np.where(valid, np.exp(x - m_new), 0.0)
+        den = den * corr + p.sum()
+        acc = acc * corr + p @ V[idx]
+        m = m_new
+    return acc / den
+
+
+def pin_tile_size_invariance(lib):
+    g = golden("tile_size_invariance.json")
+    S = g["history"]
+    d = golden("fused_kernel_diagram.json")
+    for seed, S_, L, tiles in ((51, S, 3, g["block_sizes"]), (52, d["history"], 1, [d["tile"]])):
+        c = make_case(seed, 1, 2, 1, L, 16, 4, [S_])
+        ref = run_oracle(lib, c)
+        for tile in tiles:
+            for h in range(c.H_q):
+                for l in range(L):
+                    last = l + S_ - L
+                    got = _online_fold(c.q[0, h, l], c.K[0, 0, :S_], c.V[0, 0, :S_],
+                                       last, c.scale, tile)
+                    assert_close(ref[0, h, l], got, what=f"tile {tile}")
+
+
+def pin_single_page(lib):
+    # context inside one page: the result is plain attention over that page's
+    # first S slots, read straight from the pool array
+    rng = np.random.default_rng(61)
+    ps, S, D = 16, 11, 32
+    c = make_case(61, 1, 2, 2, 1, D, ps, [S], num_pages=5, causal=False)
+    page = int(c.bt[0, 0])
+    got = run_oracle(lib, c)
+    for h in range(2):
+        Kp = bf16_to_f32(c.kp[page, h, :S]).astype(np.float64)
+        Vp = bf16_to_f32(c.vp[page, h, :S]).astype(np.float64)
+        w = scipy.special.softmax(c.scale * (Kp @ c.q[0, h, 0]))
+        assert_close(got[0, h, 0], w @ Vp, what="single page")
+    del rng
+
+
+def pin_one_hot(lib):
+    # one key's score exceeds all others by > 745, so every other weight is
+    # below exp(-745) ~ 5e-324: the output is exactly that key's value row
+    D, S, j = 128, 37, 23
+    rng = np.random.default_rng(71)
+    qf = rng.standard_normal((1, 1, 1, D)).astype(np.float32)
+    qb = bf16_bits(qf)
+    qv = bf16_to_f32(qb).astype(np.float64)
+    Kf = rng.standard_normal((1, 1, S, D)).astype(np.float32) * np.float32(0.01)
+    Kf[0, 0, j] = bf16_to_f32(qb[0, 0, 0]) * np.float32(120.0)
+    Kb = bf16_bits(Kf)
+    c = make_case(71, 1, 1, 1, 1, D, 8, [S], q=(qb, qv),
+                  K=(Kb, bf16_to_f32(Kb).astype(np.float64)), causal=False)
+    x = c.scale * (c.K[0, 0, :S] @ c.q[0, 0, 0])
+    assert x[j] - np.delete(x, j).max() > 745.0
+    got = run_oracle(lib, c)
+    assert np.array_equal(got[0, 0, 0], c.V[0, 0, j]), "dominant key must return its value row"
+
+
+def pin_uniform_visible_mean(lib):
+    # identical keys -> equal scores -> each row averages exactly its visible
+    # value rows; with causal, row l sees keys 0 .. l + S - L
+    for seed, L, S, ps, causal in ((81, 5, 13, 4, True), (82, 7, 40, 16, True),
+                                   (83, 3, 9, 2, False), (84, 9, 9, 3, True)):
+        D = 16
+        rng = np.random.default_rng(seed)
+        row = bf16_bits(rng.standard_normal(D).astype(np.float32))
+        Kb = np.broadcast_to(row, (1, 1, S, D)).copy()
+        c = make_case(seed, 1, 1, 1, L, D, ps, [S],
+                      K=(Kb, bf16_to_f32(Kb).astype(np.float64)), causal=causal)
+        got = run_oracle(lib, c)
+        for l in range(L):
+            n = (l + S - L + 1) if causal else S
+            assert_close(got[0, 0, l], c.V[0, 0, :n].mean(axis=0), what=f"uniform row {l}")
+
+
+def pin_gqa_equals_repeat(lib):
+    B, Hq, Hkv, L, D, ps, ctx = 2, 6, 2, 3, 16, 4, [14, 7]
+    c = make_case(91, B, Hq, Hkv, L, D, ps, ctx)
+    G = Hq // Hkv
+    rep = make_case(91, B, Hq, Hq, L, D, ps, ctx, q=(c.q_store, c.q),
+                    K=(np.repeat(c.K_store, G, axis=1), np.repeat(c.K, G, axis=1)),
+                    V=(np.repeat(c.V_store, G, axis=1), np.repeat(c.V, G, axis=1)))
+    assert np.array_equal(run_oracle(lib, c), run_oracle(lib, rep)), "GQA map differs from repetition"
+
+
+def pin_gather(lib):
+    c = make_case(101, 2, 2, 2, 1, 16, 3, [10, 4])
+    k, v = lib.gather(c.kp, c.vp, c.bt, c.ctx, 12)
+    for b in range(c.B):
+        S = int(c.ctx[b])
+        assert np.array_equal(k[b, :, :S], c.K[b, :, :S])
+        assert np.array_equal(v[b, :, :S], c.V[b, :, :S])
+        assert not k[b, :, S:].any() and not v[b, :, S:].any()
+
+
+def pin_errors(lib):
+    c = make_case(111, 1, 2, 1, 2, 16, 4, [6])
+    bt = c.bt.copy()
+    bt[0, 0] = c.kp.shape[0]
+    for args, code in (
+        (dict(bt=bt), oracle_mod.oracle.ORACLE_ERR_BAD_BLOCK_TABLE),
+        (dict(ctx=np.array([1], np.int32)), oracle_mod.oracle.ORACLE_ERR_INVALID_ARG),
+        (dict(ctx=np.array([0], np.int32)), oracle_mod.oracle.ORACLE_ERR_INVALID_ARG),
+        (dict(ctx=np.array([10 ** 6], np.int32)), oracle_mod.oracle.ORACLE_ERR_INVALID_ARG),
+    ):
+        try:
+            lib.paged_attention(c.q_store, c.kp, c.vp, args.get("bt", c.bt),
+                                args.get("ctx", c.ctx), c.scale, True)
+        except oracle_mod.OracleError as e:
+            assert e.code == code, (args, e.code)
+        else:
+            raise AssertionError(f"expected error {code} for {list(args)}")
+
+
+def pin_rows_api(lib):
+    c = make_case(121, 2, 4, 2, 3, 16, 4, [9, 12])
+    full = run_oracle(lib, c)
+    rows = [(0, 3, 2), (1, 0, 0), (1, 2, 1)]
+    got = lib.paged_attention_rows(c.q_store, c.kp, c.vp, c.bt, c.ctx, c.scale, True, rows)
+    for i, (b, h, l) in enumerate(rows):
+        assert np.array_equal(got[i], full[b, h, l])
+
+
+ALL_PINS = [pin_bruteforce, pin_torch_sdpa, pin_page_permutation, pin_unused_table_entries,
+            pin_tile_size_invariance, pin_single_page, pin_one_hot, pin_uniform_visible_mean,
+            pin_gqa_equals_repeat, pin_gather, pin_errors, pin_rows_api]

@@ -1,0 +1,25 @@
+"""Every planted mistake in the oracle must trip at least one pin (CPU only).
+
+The mistakes are compiled into separate builds of the oracle source with
+ORACLE_MUTANT=n: (1) causal bound off by one, (2) wrong GQA head map, (3)
+block table ignored, (4) scale dropped, (5) K and V swapped, (6) a term
+dropped from the softmax denominator, (7) causal offset with its sign flipped.
+"""
+import pytest
+
+import oracle
+import pins
+
+MUTANTS = [1, 2, 3, 4, 5, 6, 7]
+
+
+@pytest.mark.parametrize("mutant", MUTANTS)
+def test_planted_mistake_is_caught(mutant):
+    lib = oracle.load(mutant)
+    caught = []
+    for pin in pins.ALL_PINS:
+        try:
+            pin(lib)
+        except (AssertionError, oracle.OracleError, FloatingPointError):
+            caught.append(pin.__name__)
+    assert caught, f"mutant {mutant} passed every pin"

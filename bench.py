@@ -1,0 +1,527 @@
+#!/usr/bin/env python3
+"""Benchmark of the paged-attention hot path on GB300.
+
+One step = one call of the C-ABI entry point over one batch of the workload
+(for the decode workload: the split page-walk kernel and the combine kernel).
+Prints ONE JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload decode|prefill|tails|long_decode|tiny]
+
+Default workload: batched decode, B=64, L=1, H_q=32, H_kv=8, D=128,
+page_size=128, context lengths U{128..4096}, scattered pages (seeded).
+Metric: achieved HBM GB/s = algorithmic bytes / device time (bf16).
+
+--impl reference times the fp64 CPU oracle on the host cores over a bounded
+sample of the same workload (the method has no other reference program).
+Under torchrun each rank runs its own replica (the path has no exchange
+step); rank 0 prints.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from paged_kv_cache_03_gb300 import synth  # noqa: E402
+
+METRIC = "paged-attn decode HBM GB/s & prefill TFLOP/s vs GB300 roofline (bf16, d128)"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_FLUSH_BYTES = 256 << 20
+
+# Which quantity each workload is measured in.
+WORKLOAD_BOUND = {"decode": "hbm", "long_decode": "hbm", "tiny": "hbm", "prefill": "tensor",
+                  "tails": "tensor"}
+
+
+# ---------------------------------------------------------------------------
+# algorithmic work (per call)
+# ---------------------------------------------------------------------------
+def algorithmic_bytes(inp) -> int:
+    """Minimum bytes one call moves: every visible K and V row of each
+    (sequence, kv head) once (2 * H_kv * D * elt per context token), query in
+    and output out once, the block-table entries of the used pages and the
+    context lengths."""
+    es = 2 if inp.dtype == "bf16" else 4
+    tokens = int(inp.context_lens.astype(np.int64).sum())
+    kv = 2 * inp.H_kv * inp.D * es * tokens
+    qo = 2 * inp.query.size * es
+    pages = sum((int(s) + inp.page_size - 1) // inp.page_size for s in inp.context_lens)
+    return kv + qo + 4 * pages + 4 * inp.B
+
+
+def visible_pairs(inp) -> int:
+    """(query row, key) pairs with the key visible, per query head."""
+    L = inp.L
+    tot = 0
+    for s in inp.context_lens.astype(np.int64):
+        s = int(s)
+        tot += (L * (s - L) + L * (L + 1) // 2) if inp.causal else L * s
+    return tot
+
+
+def algorithmic_flops(inp) -> int:
+    """4 * H_q * D * visible pairs: a multiply-add per element of Q.K^T and
+    of P.V."""
+    return 4 * inp.H_q * inp.D * visible_pairs(inp)
+
+
+def workload_desc(name, inp) -> str:
+    kw = synth.WORKLOADS[name]
+    ctx = (f"ctx~U[{kw['ctx_range'][0]},{kw['ctx_range'][1]}]" if "ctx_range" in kw
+           else f"ctx={sorted(set(int(x) for x in inp.context_lens))}")
+    ks = f" K*{kw['k_scale']}" if kw.get("k_scale", 1.0) != 1.0 else ""
+    return (f"{name}: B={inp.B} L={inp.L} H_q={inp.H_q} H_kv={inp.H_kv} D={inp.D} "
+            f"page_size={inp.page_size} pool={inp.num_pages} pages {ctx} "
+            f"{'causal' if inp.causal else 'full'}{ks} seed={kw['seed']}")
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_digest() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "paged_kv_cache_03_gb300", "csrc")
+    for fn in sorted(os.listdir(csrc)):
+        if fn.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, fn), "rb") as f:
+                h.update(fn.encode() + b"\0" + f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, or None when the
+    kernel sources changed since the counters were taken."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        e = d[f"{kernel}@{workload}"]
+        if e.get("source_digest") != kernel_source_digest():
+            return None
+        return int(e["dram_bytes_per_launch"])
+    except Exception:
+        return None
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+REASON_BITS = {0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap",
+               0x8: "hw_slowdown", 0x10: "sync_boost", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown",
+               0x100: "display_clock_setting"}
+
+
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active")
+
+    def __init__(self, device_index: int):
+        self.idx = device_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        import tempfile
+        try:
+            fd, self.path = tempfile.mkstemp(prefix="pa_clocks_", suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
+                    "note": "nvidia-smi unavailable"}
+        time.sleep(0.1)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, mx, reasons, pw = [], [], set(), []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 5:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    mx.append(float(parts[2]))
+                    pw.append(float(parts[3]))
+                    bits = int(parts[4], 16)
+                except ValueError:
+                    continue
+                for b, name in REASON_BITS.items():
+                    if bits & b and name != "gpu_idle":
+                        reasons.add(name)
+        os.unlink(self.path)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm),
+                "power_w_max": max(pw) if pw else None}
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (replicas: no data-path collective)
+# ---------------------------------------------------------------------------
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def dist_init(backend: str):
+    import torch.distributed as dist
+    if not dist.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group(backend=backend)
+    return dist
+
+
+def reduce_max(value: float, device) -> float:
+    """Max of a float over all ranks (identity without a process group)."""
+    import torch
+    import torch.distributed as dist
+    if not dist.is_available() or not dist.is_initialized():
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(device):
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        if dist.get_backend() == "nccl":
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+def aggregate(bytes_per_step: float, steps: int, local_ms_total: float, world: int, device):
+    """Whole-job throughput: every rank's units over the slowest rank's time."""
+    t = reduce_max(local_ms_total, device)
+    return bytes_per_step * steps * world / (t * 1e-3), t
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (cpu_baseline leg and --impl reference)
+# ---------------------------------------------------------------------------
+def sub_batch(inp, n):
+    """The first n sequences of a workload (same pool)."""
+    return synth.PagedInputs(np.ascontiguousarray(inp.query[:n]), inp.key_pages,
+                             inp.value_pages, np.ascontiguousarray(inp.block_table[:n]),
+                             np.ascontiguousarray(inp.context_lens[:n]), inp.page_size,
+                             inp.scale, inp.causal, inp.dtype, inp.name)
+
+
+def time_oracle(inp, target_s: float, unit_fn):
+    """Runs the oracle on growing leading sub-batches until one run takes
+    about target_s; returns (units/s, seconds, description, threads)."""
+    import oracle
+    lib = oracle.load()
+    cores = oracle.host_cores()
+    n = 1
+    while True:
+        sub = sub_batch(inp, n)
+        t0 = time.perf_counter()
+        lib.paged_attention(sub.query, sub.key_pages, sub.value_pages, sub.block_table,
+                            sub.context_lens, sub.scale, sub.causal, num_threads=cores)
+        dt = time.perf_counter() - t0
+        if dt >= target_s or n >= inp.B:
+            break
+        grow = max(2, int(math.ceil(target_s / max(dt, 1e-3) * 0.9)))
+        n = min(inp.B, n * grow)
+    return unit_fn(sub) / dt, dt, f"first {n} of {inp.B} sequences, one full oracle call", cores
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+def run_ours(args):
+    import torch
+    from paged_kv_cache_03_gb300 import binding as B
+    world, rank, local = dist_env()
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist_init("nccl")
+    device = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(device)
+    B.load()
+
+    inp = synth.workload(args.workload)
+    bound = WORKLOAD_BOUND[args.workload]
+    bytes_step = algorithmic_bytes(inp)
+    flops_step = algorithmic_flops(inp)
+    es = 2 if inp.dtype == "bf16" else 4
+    tdt = torch.bfloat16 if inp.dtype == "bf16" else torch.float32
+
+    def dev_tensor(a, dt=None):
+        t = torch.from_numpy(np.ascontiguousarray(a))
+        if dt is not None:
+            t = t.view(dt)
+        return t.to(device)
+
+    q = dev_tensor(inp.query, tdt)
+    kp = dev_tensor(inp.key_pages, tdt)
+    vp = dev_tensor(inp.value_pages, tdt)
+    bt = dev_tensor(inp.block_table)
+    ctx = dev_tensor(inp.context_lens)
+    out = torch.empty_like(q)
+    shape = B.shape_of(q, kp, bt)
+    sched = B.pa_choose_schedule(shape)
+    launches = B.pa_launch_count(shape, sched)
+    ws = B.new_workspace(shape, device)
+    stream = torch.cuda.current_stream(device)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+    dominant = {B.PA_SCHED_DECODE: "decode_split_kernel",
+                B.PA_SCHED_PREFILL: "prefill_tile_kernel"}[sched]
+
+    def call(ev0=None, ev1=None):
+        st = B.pa_paged_attention_profiled(shape, q, kp, vp, bt, ctx, inp.scale, inp.causal, out,
+                                           ws, ws.numel(), stream, sched, ev0, ev1)
+        if st != B.PA_OK:
+            raise RuntimeError(f"pa_paged_attention: {B.status_str(st)}")
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        call()
+    torch.cuda.synchronize(device)
+    st, flag = B.pa_check_device_flag(ws, stream=stream)
+    if flag:
+        raise RuntimeError(f"device flag {flag:#x} after warm-up")
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    for e in ev:  # create the CUDA events up front (torch makes them on first record)
+        for x in e:
+            x.record(stream)
+    torch.cuda.synchronize(device)
+
+    sampler = ClockSampler(device.index)
+    if rank == 0:
+        sampler.start()
+    barrier(device)
+    torch.cuda.synchronize(device)
+    wall0 = time.perf_counter()
+    for k in range(K):
+        flush.zero_()  # L2 flush between timed steps (outside the step's events)
+        e = ev[k]
+        e[0].record(stream)
+        call(e[1].cuda_event, e[2].cuda_event)
+        e[3].record(stream)
+    torch.cuda.synchronize(device)
+    barrier(device)
+    wall = time.perf_counter() - wall0
+    clocks = sampler.stop() if rank == 0 else None
+    step_ms = np.array([e[0].elapsed_time(e[3]) for e in ev])
+    kern_ms = np.array([e[1].elapsed_time(e[2]) for e in ev])
+    st, flag = B.pa_check_device_flag(ws, stream=stream)
+    if flag:
+        raise RuntimeError(f"device flag {flag:#x} after timed steps")
+
+    value, t_max = aggregate(bytes_step, K, float(step_ms.sum()), world, device)
+    ms_per_step = t_max / K
+    if bound == "tensor":
+        value_unit, value = "TFLOP/s", flops_step * K * world / (t_max * 1e-3) / 1e12
+    else:
+        value_unit, value = "GB/s", value / 1e9
+
+    peaks, peaks_src = load_peaks()
+    kern_avg_s = float(kern_ms.mean()) * 1e-3
+    if bound == "tensor":
+        achieved = flops_step / kern_avg_s / 1e12
+        peak = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
+        runit = "TFLOP/s"
+    else:
+        achieved = bytes_step / kern_avg_s / 1e9
+        peak = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
+        runit = "GB/s"
+    roofline = {"bound": bound, "achieved": round(achieved, 2), "peak": peak, "unit": runit,
+                "frac": round(achieved / peak, 4), "traffic": recorded_traffic(
+                    dominant, args.workload),
+                "kernel": dominant, "kernel_ms_avg": round(float(kern_ms.mean()), 5),
+                "kernel_ms_median": round(float(np.median(kern_ms)), 5),
+                "peak_source": f"{peaks_src} (MEASURED_PEAKS.json)" if peaks_src == "measured"
+                else "fallback", "algorithmic_bytes": bytes_step,
+                "algorithmic_flops": flops_step}
+
+    # ---- end to end through the public call with host buffers ----------------
+    e2e = None
+    if not args.no_e2e:
+        host = {n: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
+                for n, a in (("query", inp.query), ("key_pages", inp.key_pages),
+                             ("value_pages", inp.value_pages), ("block_table", inp.block_table),
+                             ("context_lens", inp.context_lens))}
+        out_host = torch.empty(out.shape, dtype=tdt).pin_memory()
+        dst = {"query": q, "key_pages": kp, "value_pages": vp, "block_table": bt,
+               "context_lens": ctx}
+        h2d = sum(t.numel() * t.element_size() for t in host.values())
+        d2h = out.numel() * out.element_size()
+        Ke = max(3, min(args.e2e_steps, K))
+
+        def e2e_step():
+            for n, t in host.items():
+                d = dst[n]
+                d.view(torch.uint8).view(-1).copy_(t.view(torch.uint8).view(-1),
+                                                   non_blocking=True)
+            st = B.pa_paged_attention(shape, q, kp, vp, bt, ctx, inp.scale, inp.causal, out, ws,
+                                      ws.numel(), stream)
+            if st != B.PA_OK:
+                raise RuntimeError(B.status_str(st))
+            out_host.copy_(out, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize(device)
+        barrier(device)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(Ke):
+            e2e_step()
+        b.record(stream)
+        torch.cuda.synchronize(device)
+        e2e_ms = a.elapsed_time(b)
+        e2e_ms = reduce_max(e2e_ms, device)
+        if bound == "tensor":
+            ev_ = flops_step * Ke * world / (e2e_ms * 1e-3) / 1e12
+        else:
+            ev_ = bytes_step * Ke * world / (e2e_ms * 1e-3) / 1e9
+        e2e = {"value": round(ev_, 3), "unit": value_unit, "h2d_bytes_per_step": int(h2d),
+               "d2h_bytes_per_step": int(d2h), "steps": Ke,
+               "ms_per_step": round(e2e_ms / Ke, 4),
+               "note": "pinned host inputs (query, both page pools, block table, context "
+                       "lengths) copied to HBM, one call, output copied back, every step"}
+
+    line = {
+        "metric": METRIC, "value": round(value, 3), "unit": value_unit, "n_gpus": world,
+        "steps": K, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": inp.dtype,
+        "data": "synthetic (seeded N(0,1) bf16, scattered pages)",
+        "config": {"workload": workload_desc(args.workload, inp), "schedule":
+                   {1: "decode", 2: "prefill"}[sched],
+                   "l2": "flushed: 256 MiB write between timed steps (outside step events)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
+                   "algorithmic_bytes_per_step": bytes_step,
+                   "algorithmic_flops_per_step": flops_step},
+        "clocks": clocks, "e2e": e2e, "gpu_launches": K * launches, "roofline": roofline,
+        "step_ms_median": round(float(np.median(step_ms)), 5),
+        "wall_s_timed_region": round(wall, 3),
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        unit_fn = (lambda s: algorithmic_flops(s) / 1e12) if bound == "tensor" else (
+            lambda s: algorithmic_bytes(s) / 1e9)
+        v, secs, desc, cores = time_oracle(inp, args.cpu_seconds, unit_fn)
+        line["cpu_baseline"] = {"value": round(v, 6), "unit": value_unit, "cores": cores,
+                                "kind": "oracle", "sample": desc, "seconds": round(secs, 3)}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    return line
+
+
+# ---------------------------------------------------------------------------
+# reference arm: the fp64 oracle on the host cores
+# ---------------------------------------------------------------------------
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if world > 1 and rank != 0:
+        return None
+    import oracle
+    lib = oracle.load()
+    cores = oracle.host_cores()
+    inp = synth.workload(args.workload)
+    bound = WORKLOAD_BOUND[args.workload]
+    unit_fn = (lambda s: algorithmic_flops(s) / 1e12) if bound == "tensor" else (
+        lambda s: algorithmic_bytes(s) / 1e9)
+    unit = "TFLOP/s" if bound == "tensor" else "GB/s"
+    # size each step so the whole run takes about args.ref_budget seconds
+    per_step = max(0.05, min(3.0, args.ref_budget / max(1, args.steps + args.warmup)))
+    _, _, _, _ = time_oracle(inp, min(per_step, 0.5), unit_fn)  # warm the library
+    n = 1
+    while n < inp.B:
+        sub = sub_batch(inp, n)
+        t0 = time.perf_counter()
+        lib.paged_attention(sub.query, sub.key_pages, sub.value_pages, sub.block_table,
+                            sub.context_lens, sub.scale, sub.causal, num_threads=cores)
+        dt = time.perf_counter() - t0
+        if dt >= per_step:
+            break
+        n = min(inp.B, max(n + 1, int(n * per_step / max(dt, 1e-4) * 0.9)))
+    sub = sub_batch(inp, n)
+
+    def step():
+        lib.paged_attention(sub.query, sub.key_pages, sub.value_pages, sub.block_table,
+                            sub.context_lens, sub.scale, sub.causal, num_threads=cores)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = time.perf_counter() - t0
+    v = unit_fn(sub) * args.steps / dt
+    desc = f"first {n} of {inp.B} sequences per step, one full oracle call"
+    line = {"impl": "reference", "metric": METRIC, "value": round(v, 6), "unit": unit,
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(dt / args.steps * 1e3, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded N(0,1) bf16, scattered pages)",
+            "config": {"workload": workload_desc(args.workload, inp), "sample": desc},
+            "cpu_baseline": {"value": round(v, 6), "unit": unit, "cores": cores,
+                             "kind": "oracle", "sample": desc},
+            "e2e": {"value": round(v, 6), "unit": unit, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+    print(json.dumps(line), flush=True)
+    return line
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(synth.WORKLOADS), default="decode")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--ref-budget", type=float, default=90.0,
+                    help="seconds the reference arm's timed steps should take in total")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,153 @@
+/*
+ * paged_attn.h -- C ABI of the GB300 (sm_103a) paged-attention library.
+ *
+ * One operation: exact scaled-dot-product attention of a batch of queries
+ * over a paged K/V pool, as defined in "Week 3 Day 5: Paged FlashAttention"
+ * (tiny-llm):
+ *   - Keep the Day 4 Interface: the single model-facing call is
+ *     paged_attention(query, key_pages, value_pages, block_table,
+ *     context_lens, page_size, scale, mask="causal"); here mask="causal"
+ *     becomes causal=1 and mask=None becomes causal=0.
+ *   - Task 1: logical key position s of sequence b lives at
+ *     pages[block_table[b, s / page_size], kv_head, s % page_size, :].
+ *   - Task 2: key s is visible to query row l iff s <= l + context_len - L
+ *     (causal), every s < context_len otherwise; the output is the softmax
+ *     over the visible scores (scaled by `scale`) applied to the value rows.
+ *   - GQA ("Week 2 Day 5: Fused Decode Attention", Task 1):
+ *     kv_head = q_head / (H_q / H_kv).
+ *
+ * Layouts (row-major, contiguous, device memory unless stated):
+ *   query        [B, H_q, L, D]                 bf16 or fp32
+ *   key_pages    [num_pages, H_kv, page_size, D] same dtype as query
+ *   value_pages  [num_pages, H_kv, page_size, D] same dtype
+ *   block_table  [B, max_pages_per_seq]          int32 physical page ids
+ *   context_lens [B]                             int32 keys per sequence,
+ *                                                including the L new queries
+ *   out          [B, H_q, L, D]                  same dtype as query
+ * D must be 128.  All device pointers must be 16-byte aligned.
+ * Entries block_table[b, i] with i >= ceil(context_lens[b] / page_size) are
+ * never read and may hold anything.
+ *
+ * Ownership: the caller allocates and owns every buffer, including the
+ * workspace.  The library allocates no device memory in any call.  Calls are
+ * asynchronous on the given stream (cudaStream_t passed as void*, NULL = the
+ * legacy default stream).
+ *
+ * Errors: arguments are checked on the host before anything is enqueued; a
+ * failed check returns an error status and launches nothing.  The device
+ * arrays block_table and context_lens are not read on the host (that would
+ * need a synchronisation); instead the kernels record problems they meet in a
+ * sticky 32-bit flag word at the start of the workspace (PA_FLAG_* bits) and
+ * carry on without faulting.  pa_check_device_flag() reads it.
+ */
+#ifndef PAGED_ATTN_H
+#define PAGED_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    PA_OK = 0,
+    PA_ERR_INVALID_ARG = 1,     /* bad shape, null or misaligned pointer, bad context length */
+    PA_ERR_UNSUPPORTED = 2,     /* valid but not implemented here (D != 128, ...) */
+    PA_ERR_BAD_BLOCK_TABLE = 3, /* a block-table entry that is read is out of range */
+    PA_ERR_WORKSPACE = 4,       /* workspace missing or smaller than pa_workspace_bytes() */
+    PA_ERR_CUDA = 5,            /* a CUDA runtime call or launch failed */
+    PA_ERR_DEVICE_FLAG = 6      /* the kernels recorded an error in the flag word */
+} pa_status;
+
+typedef enum { PA_BF16 = 0, PA_F32 = 1 } pa_dtype;
+
+/* Which hand-written schedule runs.  AUTO applies the library's shape rule. */
+typedef enum {
+    PA_SCHED_AUTO = 0,
+    PA_SCHED_DECODE = 1,  /* split-S CUDA-core page walk + combine: any L, bf16 or fp32 */
+    PA_SCHED_PREFILL = 2  /* tcgen05 tensor-core tiles: bf16 only */
+} pa_schedule;
+
+/* Bits of the device flag word (workspace offset 0). */
+#define PA_FLAG_BAD_PAGE 0x1u    /* a block-table entry read was outside [0, num_pages) */
+#define PA_FLAG_BAD_CONTEXT 0x2u /* context_lens[b] < 1, > max_pages_per_seq*page_size,
+                                    or < L under causal: that sequence's rows are 0 */
+#define PA_FLAG_TIMEOUT 0x4u     /* an on-chip pipeline wait gave up (bounded spin) */
+
+typedef struct {
+    int B, H_q, H_kv, L, D, num_pages, page_size, max_pages_per_seq;
+    pa_dtype dtype;
+} pa_shape;
+
+/* Bytes of workspace a call with this shape needs on the current device (the
+ * largest over the schedules).  The first 4 bytes are the flag word; the
+ * caller must zero the workspace once before its first use (the flag is then
+ * sticky across calls until cleared).  The rest holds the decode schedule's
+ * per-split partial states (m, l, o[D] in fp32) and needs no initialisation.
+ * Returns 0 for an invalid shape. */
+size_t pa_workspace_bytes(const pa_shape* shape);
+
+/* out = attention(query, paged K/V) for every (b, q_head, l).  `scale`
+ * multiplies q.k before the softmax (1/sqrt(D) for standard attention).
+ * The shape rule picks the decode schedule when the rows sharing one kv head
+ * (H_q/H_kv * L) are few, or for fp32; the tensor-core prefill otherwise. */
+pa_status pa_paged_attention(const pa_shape* shape, const void* query, const void* key_pages,
+                             const void* value_pages, const int32_t* block_table,
+                             const int32_t* context_lens, float scale, int causal, void* out,
+                             void* workspace, size_t workspace_bytes, void* cuda_stream);
+
+/* Same operation with the schedule chosen by the caller (pa_schedule);
+ * PA_ERR_UNSUPPORTED if that schedule cannot run this shape or dtype. */
+pa_status pa_paged_attention_sched(const pa_shape* shape, const void* query,
+                                   const void* key_pages, const void* value_pages,
+                                   const int32_t* block_table, const int32_t* context_lens,
+                                   float scale, int causal, void* out, void* workspace,
+                                   size_t workspace_bytes, void* cuda_stream, int schedule);
+
+/* pa_paged_attention_sched, plus two caller-created CUDA events
+ * (cudaEvent_t passed as void*; either may be NULL) recorded on the stream
+ * immediately before and after the launch of the schedule's dominant kernel:
+ * the split page-walk kernel of the decode schedule, the tile kernel of the
+ * prefill schedule.  cudaEventElapsedTime(before, after) then times that
+ * kernel alone.  The events are only recorded, never created or destroyed. */
+pa_status pa_paged_attention_profiled(const pa_shape* shape, const void* query,
+                                      const void* key_pages, const void* value_pages,
+                                      const int32_t* block_table, const int32_t* context_lens,
+                                      float scale, int causal, void* out, void* workspace,
+                                      size_t workspace_bytes, void* cuda_stream, int schedule,
+                                      void* event_before, void* event_after);
+
+/* Debug gather of "Week 3 Day 5", Task 1: writes the dense history of every
+ * (b, kv_head) through the block table, k_dense/v_dense [B, H_kv, max_S, D]
+ * in the pool's dtype, zeros at s >= context_lens[b].  Page translation is
+ * bit-exact, so this is compared bitwise with the oracle's gather. */
+pa_status pa_gather_debug(const pa_shape* shape, const void* key_pages, const void* value_pages,
+                          const int32_t* block_table, const int32_t* context_lens, int max_S,
+                          void* k_dense, void* v_dense, void* workspace, void* cuda_stream);
+
+/* Synchronises the stream, copies the flag word to *flag_out and, if clear is
+ * non-zero, resets it to 0.  Returns PA_ERR_DEVICE_FLAG when any bit was set. */
+pa_status pa_check_device_flag(void* workspace, uint32_t* flag_out, int clear, void* cuda_stream);
+
+/* Host-side check of the device metadata (copies block_table and
+ * context_lens to the host, synchronising the stream): PA_ERR_INVALID_ARG for
+ * a context length outside [max(1, causal ? L : 1), max_pages_per_seq *
+ * page_size], PA_ERR_BAD_BLOCK_TABLE for a read entry outside
+ * [0, num_pages).  Meant for debugging; the fast path never calls it. */
+pa_status pa_validate_metadata(const pa_shape* shape, const int32_t* block_table,
+                               const int32_t* context_lens, int causal, void* cuda_stream);
+
+/* The schedule pa_paged_attention would pick for this shape (PA_SCHED_*),
+ * or -1 for an invalid shape. */
+int pa_choose_schedule(const pa_shape* shape);
+
+/* Kernel launches one call of this shape and schedule enqueues. */
+int pa_launch_count(const pa_shape* shape, int schedule);
+
+const char* pa_status_str(pa_status status);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* PAGED_ATTN_H */

@@ -1,0 +1,247 @@
+// api.cu -- the extern "C" entry points of paged_attn.h: argument checks on
+// the host, schedule choice (the shape dispatch that "Week 3 Day 5: Paged
+// FlashAttention" puts inside the extension), and the launches.
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "internal.h"
+
+namespace pa {
+
+pa_status current_device_info(DeviceInfo* out) {
+    static std::mutex mu;
+    static DeviceInfo cache[64];
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) {
+        cudaGetLastError();
+        return PA_ERR_CUDA;
+    }
+    if (dev >= 64) return PA_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(mu);
+    DeviceInfo& d = cache[dev];
+    if (d.device != dev) {
+        DeviceInfo n;
+        n.device = dev;
+        if (cudaDeviceGetAttribute(&n.sm_count, cudaDevAttrMultiProcessorCount, dev) !=
+                cudaSuccess ||
+            cudaDeviceGetAttribute(&n.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
+                cudaSuccess ||
+            cudaDeviceGetAttribute(&n.cc_major, cudaDevAttrComputeCapabilityMajor, dev) !=
+                cudaSuccess ||
+            cudaDeviceGetAttribute(&n.cc_minor, cudaDevAttrComputeCapabilityMinor, dev) !=
+                cudaSuccess) {
+            cudaGetLastError();
+            return PA_ERR_CUDA;
+        }
+        d = n;
+    }
+    *out = d;
+    return PA_OK;
+}
+
+namespace {
+
+pa_status check_shape(const pa_shape* s) {
+    if (!s) return PA_ERR_INVALID_ARG;
+    if (s->B < 1 || s->H_q < 1 || s->H_kv < 1 || s->L < 1 || s->D < 1 || s->num_pages < 1 ||
+        s->page_size < 1 || s->max_pages_per_seq < 1)
+        return PA_ERR_INVALID_ARG;
+    if (s->H_q % s->H_kv != 0) return PA_ERR_INVALID_ARG;
+    if (s->dtype != PA_BF16 && s->dtype != PA_F32) return PA_ERR_INVALID_ARG;
+    if (s->D != kHeadDim) return PA_ERR_UNSUPPORTED;
+    // row indices of the pool and key positions stay inside int32
+    if (static_cast<long long>(s->num_pages) * s->H_kv * s->page_size >= (1ll << 31))
+        return PA_ERR_UNSUPPORTED;
+    if (static_cast<long long>(s->max_pages_per_seq) * s->page_size >= (1ll << 30))
+        return PA_ERR_UNSUPPORTED;
+    if (static_cast<long long>(s->H_q) * s->L >= (1ll << 30)) return PA_ERR_UNSUPPORTED;
+    return PA_OK;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int choose(const pa_shape& s) {
+    if (s.dtype != PA_BF16) return PA_SCHED_DECODE;
+    const long long rows = static_cast<long long>(s.H_q / s.H_kv) * s.L;
+    // A one-token query has no query-tile reuse: the page walk on CUDA cores
+    // is memory-bound and needs no tensor cores.  Enough rows per kv head to
+    // fill a 128-row tensor-core tile go to the tiled prefill.
+    if (rows <= 16 || !prefill_supported(s)) return PA_SCHED_DECODE;
+    return PA_SCHED_PREFILL;
+}
+
+pa_status run(const pa_shape* shape, const void* query, const void* key_pages,
+              const void* value_pages, const int32_t* block_table, const int32_t* context_lens,
+              float scale, int causal, void* out, void* workspace, size_t workspace_bytes,
+              void* cuda_stream, int schedule, void* ev_before = nullptr,
+              void* ev_after = nullptr) {
+    pa_status st = check_shape(shape);
+    if (st != PA_OK) return st;
+    if (!query || !key_pages || !value_pages || !block_table || !context_lens || !out)
+        return PA_ERR_INVALID_ARG;
+    if (!aligned(query, 16) || !aligned(key_pages, 16) || !aligned(value_pages, 16) ||
+        !aligned(out, 16) || !aligned(block_table, 4) || !aligned(context_lens, 4))
+        return PA_ERR_INVALID_ARG;
+    if (!(scale == scale)) return PA_ERR_INVALID_ARG;  // NaN scale
+    if (!workspace || !aligned(workspace, 256)) return PA_ERR_WORKSPACE;
+    if (schedule == PA_SCHED_AUTO) schedule = choose(*shape);
+    if (schedule != PA_SCHED_DECODE && schedule != PA_SCHED_PREFILL) return PA_ERR_INVALID_ARG;
+    if (schedule == PA_SCHED_PREFILL && !prefill_supported(*shape)) return PA_ERR_UNSUPPORTED;
+
+    Call c;
+    c.sh = *shape;
+    c.q = query;
+    c.kp = key_pages;
+    c.vp = value_pages;
+    c.bt = block_table;
+    c.ctx = context_lens;
+    c.scale = scale;
+    c.causal = causal ? 1 : 0;
+    c.out = out;
+    c.ws = workspace;
+    c.ws_bytes = workspace_bytes;
+    c.stream = static_cast<cudaStream_t>(cuda_stream);
+    c.ev_before = static_cast<cudaEvent_t>(ev_before);
+    c.ev_after = static_cast<cudaEvent_t>(ev_after);
+    st = current_device_info(&c.dev);
+    if (st != PA_OK) return st;
+    if (c.dev.cc_major != 10 || c.dev.cc_minor != 3) return PA_ERR_UNSUPPORTED;
+    if (workspace_bytes < kFlagBytes) return PA_ERR_WORKSPACE;
+    return schedule == PA_SCHED_DECODE ? decode_launch(c) : prefill_launch(c);
+}
+
+}  // namespace
+}  // namespace pa
+
+using namespace pa;
+
+extern "C" {
+
+size_t pa_workspace_bytes(const pa_shape* shape) {
+    if (check_shape(shape) != PA_OK) return 0;
+    DeviceInfo dev;
+    if (current_device_info(&dev) != PA_OK) return 0;
+    size_t need = decode_workspace_bytes(*shape, dev.sm_count);
+    return need > kFlagBytes ? need : kFlagBytes;
+}
+
+pa_status pa_paged_attention(const pa_shape* shape, const void* query, const void* key_pages,
+                             const void* value_pages, const int32_t* block_table,
+                             const int32_t* context_lens, float scale, int causal, void* out,
+                             void* workspace, size_t workspace_bytes, void* cuda_stream) {
+    return run(shape, query, key_pages, value_pages, block_table, context_lens, scale, causal,
+               out, workspace, workspace_bytes, cuda_stream, PA_SCHED_AUTO);
+}
+
+pa_status pa_paged_attention_sched(const pa_shape* shape, const void* query,
+                                   const void* key_pages, const void* value_pages,
+                                   const int32_t* block_table, const int32_t* context_lens,
+                                   float scale, int causal, void* out, void* workspace,
+                                   size_t workspace_bytes, void* cuda_stream, int schedule) {
+    return run(shape, query, key_pages, value_pages, block_table, context_lens, scale, causal,
+               out, workspace, workspace_bytes, cuda_stream, schedule);
+}
+
+pa_status pa_paged_attention_profiled(const pa_shape* shape, const void* query,
+                                      const void* key_pages, const void* value_pages,
+                                      const int32_t* block_table, const int32_t* context_lens,
+                                      float scale, int causal, void* out, void* workspace,
+                                      size_t workspace_bytes, void* cuda_stream, int schedule,
+                                      void* event_before, void* event_after) {
+    return run(shape, query, key_pages, value_pages, block_table, context_lens, scale, causal,
+               out, workspace, workspace_bytes, cuda_stream, schedule, event_before, event_after);
+}
+
+pa_status pa_gather_debug(const pa_shape* shape, const void* key_pages, const void* value_pages,
+                          const int32_t* block_table, const int32_t* context_lens, int max_S,
+                          void* k_dense, void* v_dense, void* workspace, void* cuda_stream) {
+    pa_status st = check_shape(shape);
+    if (st != PA_OK) return st;
+    if (!key_pages || !value_pages || !block_table || !context_lens || !k_dense || !v_dense ||
+        max_S < 1)
+        return PA_ERR_INVALID_ARG;
+    if (!aligned(key_pages, 16) || !aligned(value_pages, 16) || !aligned(k_dense, 16) ||
+        !aligned(v_dense, 16))
+        return PA_ERR_INVALID_ARG;
+    if (!workspace || !aligned(workspace, 4)) return PA_ERR_WORKSPACE;
+    return gather_launch(*shape, key_pages, value_pages, block_table, context_lens, max_S,
+                         k_dense, v_dense, static_cast<uint32_t*>(workspace),
+                         static_cast<cudaStream_t>(cuda_stream));
+}
+
+pa_status pa_check_device_flag(void* workspace, uint32_t* flag_out, int clear, void* cuda_stream) {
+    if (!workspace) return PA_ERR_WORKSPACE;
+    cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
+    uint32_t f = 0;
+    if (cudaMemcpyAsync(&f, workspace, sizeof f, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess) {
+        cudaGetLastError();
+        return PA_ERR_CUDA;
+    }
+    if (clear && f) {
+        if (cudaMemsetAsync(workspace, 0, sizeof f, s) != cudaSuccess ||
+            cudaStreamSynchronize(s) != cudaSuccess) {
+            cudaGetLastError();
+            return PA_ERR_CUDA;
+        }
+    }
+    if (flag_out) *flag_out = f;
+    return f ? PA_ERR_DEVICE_FLAG : PA_OK;
+}
+
+pa_status pa_validate_metadata(const pa_shape* shape, const int32_t* block_table,
+                               const int32_t* context_lens, int causal, void* cuda_stream) {
+    pa_status st = check_shape(shape);
+    if (st != PA_OK) return st;
+    if (!block_table || !context_lens) return PA_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
+    std::vector<int32_t> ctx(shape->B);
+    std::vector<int32_t> bt(static_cast<size_t>(shape->B) * shape->max_pages_per_seq);
+    if (cudaMemcpyAsync(ctx.data(), context_lens, ctx.size() * 4, cudaMemcpyDeviceToHost, s) !=
+            cudaSuccess ||
+        cudaMemcpyAsync(bt.data(), block_table, bt.size() * 4, cudaMemcpyDeviceToHost, s) !=
+            cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess) {
+        cudaGetLastError();
+        return PA_ERR_CUDA;
+    }
+    const long long cap = static_cast<long long>(shape->max_pages_per_seq) * shape->page_size;
+    for (int b = 0; b < shape->B; ++b) {
+        const int S = ctx[b];
+        if (S < 1 || S > cap || (causal && S < shape->L)) return PA_ERR_INVALID_ARG;
+        const int npg = (S + shape->page_size - 1) / shape->page_size;
+        for (int i = 0; i < npg; ++i) {
+            const int32_t pp = bt[static_cast<size_t>(b) * shape->max_pages_per_seq + i];
+            if (pp < 0 || pp >= shape->num_pages) return PA_ERR_BAD_BLOCK_TABLE;
+        }
+    }
+    return PA_OK;
+}
+
+int pa_choose_schedule(const pa_shape* shape) {
+    if (check_shape(shape) != PA_OK) return -1;
+    return choose(*shape);
+}
+
+int pa_launch_count(const pa_shape* shape, int schedule) {
+    if (check_shape(shape) != PA_OK) return -1;
+    if (schedule == PA_SCHED_AUTO) schedule = choose(*shape);
+    return schedule == PA_SCHED_DECODE ? 2 : 1;
+}
+
+const char* pa_status_str(pa_status status) {
+    switch (status) {
+        case PA_OK: return "ok";
+        case PA_ERR_INVALID_ARG: return "invalid argument";
+        case PA_ERR_UNSUPPORTED: return "unsupported shape or dtype";
+        case PA_ERR_BAD_BLOCK_TABLE: return "block table entry out of range";
+        case PA_ERR_WORKSPACE: return "workspace missing or too small";
+        case PA_ERR_CUDA: return "CUDA error";
+        case PA_ERR_DEVICE_FLAG: return "kernel recorded an error in the device flag";
+    }
+    return "unknown status";
+}
+
+}  // extern "C"

@@ -1,0 +1,63 @@
+// internal.h -- declarations shared by the host dispatcher and the kernel
+// translation units (not part of the public ABI).
+#pragma once
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+#include "paged_attn.h"
+
+namespace pa {
+
+constexpr int kHeadDim = 128;
+// Workspace: [0, kFlagBytes) holds the sticky flag word.
+constexpr size_t kFlagBytes = 256;
+
+struct DeviceInfo {
+    int device = -1;
+    int sm_count = 0;
+    int smem_optin = 0;
+    int cc_major = 0, cc_minor = 0;
+};
+
+// Properties of the current device (cached per device).
+pa_status current_device_info(DeviceInfo* out);
+
+struct Call {
+    pa_shape sh;
+    const void* q;
+    const void* kp;
+    const void* vp;
+    const int32_t* bt;
+    const int32_t* ctx;
+    float scale;
+    int causal;
+    void* out;
+    void* ws;
+    size_t ws_bytes;
+    cudaStream_t stream;
+    cudaEvent_t ev_before = nullptr;  // recorded around the dominant kernel
+    cudaEvent_t ev_after = nullptr;
+    DeviceInfo dev;
+};
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// ---- decode schedule (split-S page walk on CUDA cores + combine) ----------
+// Rows of one (b, kv_head) handled together by one pass over its keys.
+int decode_rows_per_chunk(const pa_shape& sh);
+size_t decode_workspace_bytes(const pa_shape& sh, int sm_count);
+int decode_grid(const pa_shape& sh, int sm_count);
+pa_status decode_launch(const Call& c);
+
+// ---- prefill schedule (tcgen05 tensor cores) ------------------------------
+bool prefill_supported(const pa_shape& sh);
+pa_status prefill_launch(const Call& c);
+
+// ---- debug gather ---------------------------------------------------------
+pa_status gather_launch(const pa_shape& sh, const void* kp, const void* vp, const int32_t* bt,
+                        const int32_t* ctx, int max_S, void* kd, void* vd, uint32_t* flag,
+                        cudaStream_t stream);
+
+}  // namespace pa

@@ -1,0 +1,110 @@
+"""The C-ABI library loads, exports every declared entry point, and rejects
+bad arguments on the host before any CUDA call (CPU only)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from paged_kv_cache_03_gb300 import binding as B
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    names = []
+    for fn in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if fn.endswith(".h"):
+            with open(os.path.join(ROOT, "include", fn)) as f:
+                text = f.read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names += re.findall(r"^\s*[A-Za-z_][\w\s\*]*?\b(pa_\w+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for n in ("pa_paged_attention", "pa_paged_attention_sched", "pa_workspace_bytes",
+              "pa_gather_debug", "pa_check_device_flag", "pa_validate_metadata",
+              "pa_status_str"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol():
+    B.load()
+    lib = ctypes.CDLL(B.library_path())
+    for n in declared_functions():
+        assert hasattr(lib, n), f"{n} declared in include/ but not exported"
+
+
+def good_shape(**kw):
+    d = dict(B=2, H_q=4, H_kv=2, L=5, D=128, num_pages=16, page_size=16, max_pages_per_seq=3,
+             dtype=B.PA_BF16)
+    d.update(kw)
+    return B.make_shape(**d)
+
+
+FAKE = 1 << 20  # 16-byte aligned non-null addresses: never dereferenced on a failed check
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(H_q=3, H_kv=2), B.PA_ERR_INVALID_ARG),
+    (dict(B=0), B.PA_ERR_INVALID_ARG),
+    (dict(L=0), B.PA_ERR_INVALID_ARG),
+    (dict(page_size=0), B.PA_ERR_INVALID_ARG),
+    (dict(num_pages=0), B.PA_ERR_INVALID_ARG),
+    (dict(dtype=7), B.PA_ERR_INVALID_ARG),
+    (dict(D=64), B.PA_ERR_UNSUPPORTED),
+    (dict(num_pages=1 << 20, page_size=1 << 12), B.PA_ERR_UNSUPPORTED),
+])
+def test_bad_shapes_are_rejected_on_host(kw, status):
+    sh = good_shape(**kw)
+    st = B.pa_paged_attention_sched(sh, FAKE, FAKE, FAKE, FAKE, FAKE, 0.1, 1, FAKE, FAKE,
+                                    1 << 20, 0, B.PA_SCHED_DECODE)
+    assert st == status
+    assert B.pa_workspace_bytes(sh) == 0
+
+
+@pytest.mark.parametrize("which", ["query", "key", "value", "bt", "ctx", "out"])
+def test_null_pointers_are_rejected(which):
+    ptrs = dict(query=FAKE, key=FAKE, value=FAKE, bt=FAKE, ctx=FAKE, out=FAKE)
+    ptrs[which] = 0
+    st = B.pa_paged_attention(good_shape(), ptrs["query"], ptrs["key"], ptrs["value"],
+                              ptrs["bt"], ptrs["ctx"], 0.1, 1, ptrs["out"], FAKE, 1 << 20, 0)
+    assert st == B.PA_ERR_INVALID_ARG
+
+
+def test_misaligned_pointers_are_rejected():
+    st = B.pa_paged_attention(good_shape(), FAKE + 8, FAKE, FAKE, FAKE, FAKE, 0.1, 1, FAKE,
+                              FAKE, 1 << 20, 0)
+    assert st == B.PA_ERR_INVALID_ARG
+
+
+def test_missing_workspace_is_rejected():
+    st = B.pa_paged_attention(good_shape(), FAKE, FAKE, FAKE, FAKE, FAKE, 0.1, 1, FAKE, 0, 0, 0)
+    assert st == B.PA_ERR_WORKSPACE
+
+
+def test_nan_scale_is_rejected():
+    st = B.pa_paged_attention(good_shape(), FAKE, FAKE, FAKE, FAKE, FAKE, float("nan"), 1, FAKE,
+                              FAKE, 1 << 20, 0)
+    assert st == B.PA_ERR_INVALID_ARG
+
+
+def test_unknown_schedule_is_rejected():
+    st = B.pa_paged_attention_sched(good_shape(), FAKE, FAKE, FAKE, FAKE, FAKE, 0.1, 1, FAKE,
+                                    FAKE, 1 << 20, 0, 9)
+    assert st == B.PA_ERR_INVALID_ARG
+
+
+def test_schedule_rule():
+    # single-token decode and the fp32 control run on the page walk
+    assert B.pa_choose_schedule(good_shape(L=1)) == B.PA_SCHED_DECODE
+    assert B.pa_choose_schedule(good_shape(L=2048, dtype=B.PA_F32)) == B.PA_SCHED_DECODE
+    assert B.pa_choose_schedule(good_shape(D=64)) == -1
+    assert B.pa_launch_count(good_shape(L=1), B.PA_SCHED_DECODE) == 2
+
+
+def test_status_strings():
+    for st in range(7):
+        assert B.status_str(st) not in ("", "unknown status")

@@ -1,0 +1,330 @@
+"""CUDA path vs the fp64 oracle, element by element, through the C ABI.
+
+Bars: bf16 max-abs <= 1e-2 and mean-abs <= 1e-3; fp32 control max-abs
+<= 1e-5; page translation (debug gather) bit-exact; outputs bitwise equal
+under physical page permutation and under junk in unused block-table entries.
+"""
+import functools
+
+import numpy as np
+import pytest
+
+import gpu_util as gu
+import pins
+from paged_kv_cache_03_gb300 import binding as B
+from paged_kv_cache_03_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+SCHEDULES = {"decode": B.PA_SCHED_DECODE, "prefill": B.PA_SCHED_PREFILL}
+
+
+@functools.lru_cache(maxsize=None)
+def workload(name, dtype="bf16"):
+    return synth.workload(name, dtype=dtype)
+
+
+def check(oracle_lib, inp, schedule=B.PA_SCHED_AUTO, rows=None, what="", skip=True):
+    try:
+        out, _ = gu.run(inp, schedule)
+    except gu.Unsupported:
+        if skip:
+            pytest.skip("schedule not available for this shape")
+        return None
+    got = gu.out_to_f64(out)
+    if rows is None:
+        ref = gu.oracle_full(oracle_lib, inp)
+    else:
+        ref = gu.oracle_rows(oracle_lib, inp, rows)
+        got = got[rows[:, 0], rows[:, 1], rows[:, 2]]
+    return gu.assert_parity(got, ref, inp.dtype, what or inp.name)
+
+
+# ---- the five named workloads ------------------------------------------------
+@pytest.mark.parametrize("name", ["tiny", "decode", "tails", "long_decode"])
+def test_workload_auto_schedule(oracle_lib, name):
+    check(oracle_lib, workload(name))
+
+
+def test_prefill_workload_auto_schedule(oracle_lib):
+    inp = workload("prefill")
+    check(oracle_lib, inp, rows=gu.sample_rows(inp, 768, seed=3))
+
+
+@pytest.mark.parametrize("name", ["tiny", "tails"])
+@pytest.mark.parametrize("sched", ["decode", "prefill"])
+def test_workload_forced_schedule(oracle_lib, name, sched):
+    check(oracle_lib, workload(name), SCHEDULES[sched], what=f"{name}/{sched}")
+
+
+@pytest.mark.parametrize("sched", ["decode", "prefill"])
+def test_prefill_workload_forced_schedule(oracle_lib, sched):
+    inp = workload("prefill")
+    check(oracle_lib, inp, SCHEDULES[sched], rows=gu.sample_rows(inp, 384, seed=7),
+          what=f"prefill/{sched}")
+
+
+# ---- the page's required fixtures ("Week 3 Day 5", Task 3) --------------------
+FIXTURES = pins.golden("paged_fixtures.json")["fixtures"]
+
+
+def fixture_inputs(fx, dtype="bf16"):
+    kw = {k: fx[k] for k in ("B", "H_q", "H_kv", "L", "page_size", "context_lens", "causal")}
+    if "num_pages" in fx:
+        kw["num_pages"] = fx["num_pages"]
+    seed = sum(ord(c) for c in fx["name"])
+    return synth.generate(D=128, seed=seed, dtype=dtype, name=fx["name"], **kw)
+
+
+@pytest.mark.parametrize("fx", FIXTURES, ids=[f["name"] for f in FIXTURES])
+@pytest.mark.parametrize("sched", ["auto", "decode", "prefill"])
+def test_page_fixture(oracle_lib, fx, sched):
+    inp = fixture_inputs(fx)
+    check(oracle_lib, inp, {"auto": B.PA_SCHED_AUTO, **SCHEDULES}[sched])
+
+
+def test_output_dtype_stays_bf16():
+    import torch
+    inp = fixture_inputs(FIXTURES[-1])
+    out, _ = gu.run(inp)
+    assert out.dtype == torch.bfloat16 and tuple(out.shape) == inp.query.shape
+
+
+def test_non_consecutive_pages_are_scattered():
+    inp = fixture_inputs(next(f for f in FIXTURES if f["name"] == "non_consecutive_physical_pages"))
+    used = inp.block_table[inp.block_table >= 0]
+    assert np.any(np.diff(used) != 1)
+
+
+# ---- the operator grid of "Week 2 Day 5", Task 3, restated on pages -----------
+GRID = pins.golden("week2_operator_grid.json")
+
+
+def grid_cases():
+    for ctx in GRID["contexts"]:
+        for L in GRID["query_lengths"]:
+            for gqa in GRID["gqa_ratios"]:
+                for causal in (True, False):
+                    if causal and L > ctx:
+                        continue
+                    yield ctx, L, gqa, causal
+
+
+@pytest.mark.parametrize("ctx,L,gqa,causal", list(grid_cases()))
+def test_operator_grid(oracle_lib, ctx, L, gqa, causal):
+    inp = synth.generate(B=2, H_q=2 * gqa, H_kv=2, L=L, D=128, page_size=16,
+                         context_lens=[ctx, max(ctx, L) + 3], seed=1000 + ctx * 7 + L + gqa,
+                         causal=causal, name=f"grid{ctx}")
+    for s in (B.PA_SCHED_AUTO, B.PA_SCHED_DECODE, B.PA_SCHED_PREFILL):
+        check(oracle_lib, inp, s, skip=False, what=f"grid ctx={ctx} L={L} gqa={gqa} causal={causal}")
+
+
+# ---- edge shapes -------------------------------------------------------------
+EDGE = [
+    # (name, kwargs)
+    ("page_size_1", dict(B=2, H_q=4, H_kv=2, L=2, page_size=1, context_lens=[37, 5])),
+    ("page_size_3", dict(B=2, H_q=4, H_kv=4, L=3, page_size=3, context_lens=[50, 3])),
+    ("page_size_256", dict(B=2, H_q=8, H_kv=2, L=1, page_size=256, context_lens=[700, 256])),
+    ("full_block_table", dict(B=2, H_q=4, H_kv=1, L=4, page_size=16, context_lens=[64, 64],
+                              max_pages_per_seq=4)),
+    ("context_equals_L", dict(B=2, H_q=2, H_kv=2, L=9, page_size=4, context_lens=[9, 12])),
+    ("one_key", dict(B=3, H_q=2, H_kv=1, L=1, page_size=16, context_lens=[1, 1, 2])),
+    ("gqa8_rows8", dict(B=2, H_q=16, H_kv=2, L=1, page_size=16, context_lens=[300, 33])),
+    ("gqa16_two_chunks", dict(B=1, H_q=16, H_kv=1, L=1, page_size=64, context_lens=[1000])),
+    ("mha_single_row", dict(B=4, H_q=4, H_kv=4, L=1, page_size=32, context_lens=[10, 900, 33, 1])),
+    ("rows_not_multiple_of_8", dict(B=2, H_q=6, H_kv=2, L=3, page_size=8, context_lens=[77, 40])),
+    ("many_short_sequences", dict(B=300, H_q=4, H_kv=1, L=1, page_size=16,
+                                  ctx_range=(1, 40))),
+    ("long_and_short_mixed", dict(B=5, H_q=8, H_kv=2, L=1, page_size=16,
+                                  context_lens=[20000, 3, 700, 1, 9000])),
+]
+
+
+@pytest.mark.parametrize("name,kw", EDGE, ids=[e[0] for e in EDGE])
+@pytest.mark.parametrize("causal", [True, False])
+def test_edge_shapes(oracle_lib, name, kw, causal):
+    inp = synth.generate(D=128, seed=sum(map(ord, name)), causal=causal, name=name, **kw)
+    for s in (B.PA_SCHED_AUTO, B.PA_SCHED_DECODE, B.PA_SCHED_PREFILL):
+        check(oracle_lib, inp, s, what=f"{name}/{s}", skip=False)
+
+
+# ---- fp32 control ---------------------------------------------------------------
+@pytest.mark.parametrize("name", ["tiny", "fixture_L65", "fixture_crossing", "short_decode"])
+def test_fp32_control(oracle_lib, name):
+    if name == "tiny":
+        inp = workload("tiny", "f32")
+    elif name == "fixture_L65":
+        inp = fixture_inputs(FIXTURES[3], "f32")
+    elif name == "fixture_crossing":
+        inp = fixture_inputs(FIXTURES[1], "f32")
+    else:
+        inp = synth.generate(B=8, H_q=32, H_kv=8, L=1, D=128, page_size=128,
+                             ctx_range=(128, 2048), seed=77, dtype="f32")
+    check(oracle_lib, inp, B.PA_SCHED_DECODE, what=f"fp32 {name}")
+
+
+# ---- bit-exact page translation ---------------------------------------------------
+@pytest.mark.parametrize("case", ["tiny", "crossing", "page1"])
+def test_gather_is_bit_exact(oracle_lib, case):
+    import torch
+    if case == "tiny":
+        inp = workload("tiny")
+    elif case == "crossing":
+        inp = fixture_inputs(FIXTURES[1])
+    else:
+        inp = synth.generate(B=2, H_q=2, H_kv=2, L=1, D=128, page_size=1, context_lens=[9, 4],
+                             seed=5)
+    dev = gu.to_device(inp)
+    shape = B.shape_of(dev["query"], dev["key_pages"], dev["block_table"])
+    max_S = int(inp.context_lens.max()) + 5
+    kd = torch.empty((inp.B, inp.H_kv, max_S, inp.D), dtype=dev["key_pages"].dtype,
+                     device="cuda")
+    vd = torch.empty_like(kd)
+    ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
+    st = B.pa_gather_debug(shape, dev["key_pages"], dev["value_pages"], dev["block_table"],
+                           dev["context_lens"], max_S, kd, vd, ws)
+    assert st == B.PA_OK
+    torch.cuda.synchronize()
+    k_ref, v_ref = oracle_lib.gather(inp.key_pages, inp.value_pages, inp.block_table,
+                                     inp.context_lens, max_S)
+    assert np.array_equal(gu.out_to_f64(kd), k_ref)
+    assert np.array_equal(gu.out_to_f64(vd), v_ref)
+    assert B.pa_check_device_flag(ws)[1] == 0
+
+
+def permuted(inp, seed):
+    """Same logical K/V, different physical placement of every page."""
+    perm = np.random.default_rng(seed).permutation(inp.num_pages).astype(np.int32)
+    kp = np.empty_like(inp.key_pages)
+    vp = np.empty_like(inp.value_pages)
+    kp[perm] = inp.key_pages
+    vp[perm] = inp.value_pages
+    bt = inp.block_table.copy()
+    bt[bt >= 0] = perm[bt[bt >= 0]]
+    return synth.PagedInputs(inp.query, kp, vp, bt, inp.context_lens, inp.page_size,
+                             inp.scale, inp.causal, inp.dtype, inp.name + "-perm")
+
+
+@pytest.mark.parametrize("name", ["tiny", "decode", "tails"])
+def test_page_permutation_is_bitwise_invisible(name):
+    import torch
+    inp = workload(name)
+    a, _ = gu.run(inp)
+    b, _ = gu.run(permuted(inp, 11))
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+def test_unused_block_table_entries_are_never_read():
+    import torch
+    inp = workload("decode")
+    a, _ = gu.run(inp)
+    for fill in (-1, 2 ** 31 - 1, inp.num_pages, -12345):
+        bt = inp.block_table.copy()
+        for b in range(inp.B):
+            npg = (int(inp.context_lens[b]) + inp.page_size - 1) // inp.page_size
+            bt[b, npg:] = fill
+        out, flag = gu.run(inp, block_table=torch.from_numpy(bt).cuda())
+        assert flag == 0
+        assert torch.equal(a.view(torch.int16), out.view(torch.int16))
+
+
+def test_repeatable_bitwise():
+    import torch
+    inp = workload("tails")
+    a, _ = gu.run(inp)
+    b, _ = gu.run(inp)
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+# ---- errors the kernels record instead of faulting ---------------------------------
+def test_bad_page_id_sets_flag(oracle_lib):
+    import torch
+    inp = workload("tiny")
+    bt = inp.block_table.copy()
+    bt[0, 0] = inp.num_pages + 5
+    out, flag = gu.run(inp, block_table=torch.from_numpy(bt).cuda(), check_flag=False)
+    assert flag & B.PA_FLAG_BAD_PAGE
+    # the other sequence is untouched by the bad entry
+    ref = gu.oracle_full(oracle_lib, inp)
+    gu.assert_parity(gu.out_to_f64(out)[1], ref[1], "bf16", "untouched sequence")
+
+
+@pytest.mark.parametrize("bad", [0, -3, 10 ** 6, 2])
+def test_bad_context_length_sets_flag_and_zeros(oracle_lib, bad):
+    import torch
+    inp = workload("tiny")  # L = 5, so a context of 2 breaks the causal contract
+    ctx = inp.context_lens.copy()
+    ctx[1] = bad
+    out, flag = gu.run(inp, context_lens=torch.from_numpy(ctx).cuda(), check_flag=False)
+    assert flag & B.PA_FLAG_BAD_CONTEXT
+    got = gu.out_to_f64(out)
+    assert not got[1].any()
+    ref = gu.oracle_full(oracle_lib, inp)
+    gu.assert_parity(got[0], ref[0], "bf16", "valid sequence")
+
+
+def test_validate_metadata():
+    import torch
+    inp = workload("tiny")
+    dev = gu.to_device(inp)
+    sh = B.shape_of(dev["query"], dev["key_pages"], dev["block_table"])
+    assert B.pa_validate_metadata(sh, dev["block_table"], dev["context_lens"], True) == B.PA_OK
+    bt = inp.block_table.copy()
+    bt[1, 2] = -1
+    assert B.pa_validate_metadata(sh, torch.from_numpy(bt).cuda(), dev["context_lens"],
+                                  True) == B.PA_ERR_BAD_BLOCK_TABLE
+    ctx = inp.context_lens.copy()
+    ctx[0] = 3
+    assert B.pa_validate_metadata(sh, dev["block_table"], torch.from_numpy(ctx).cuda(),
+                                  True) == B.PA_ERR_INVALID_ARG
+
+
+def test_output_guard_bands_untouched():
+    import torch
+    inp = workload("tails")
+    dev = gu.to_device(inp)
+    n = dev["query"].numel()
+    g = 4096
+    big = torch.full((n + 2 * g,), 7.0, dtype=torch.bfloat16, device="cuda")
+    out = big[g:g + n].view(dev["query"].shape)
+    shape = B.shape_of(dev["query"], dev["key_pages"], dev["block_table"])
+    ws = B.new_workspace(shape)
+    st = B.pa_paged_attention(shape, dev["query"], dev["key_pages"], dev["value_pages"],
+                              dev["block_table"], dev["context_lens"], inp.scale, True, out, ws,
+                              ws.numel())
+    assert st == B.PA_OK
+    torch.cuda.synchronize()
+    assert bool((big[:g] == 7.0).all()) and bool((big[g + n:] == 7.0).all())
+
+
+def test_small_workspace_is_rejected():
+    import torch
+    inp = workload("decode")
+    dev = gu.to_device(inp)
+    shape = B.shape_of(dev["query"], dev["key_pages"], dev["block_table"])
+    ws = torch.zeros(1024, dtype=torch.uint8, device="cuda")
+    out = torch.empty_like(dev["query"])
+    st = B.pa_paged_attention_sched(shape, dev["query"], dev["key_pages"], dev["value_pages"],
+                                    dev["block_table"], dev["context_lens"], inp.scale, True, out,
+                                    ws, ws.numel(), None, B.PA_SCHED_DECODE)
+    assert st == B.PA_ERR_WORKSPACE
+
+
+def test_side_stream(oracle_lib):
+    import torch
+    inp = workload("tiny")
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        out, _ = gu.run(inp)
+    gu.assert_parity(gu.out_to_f64(out), gu.oracle_full(oracle_lib, inp), "bf16", "side stream")
+
+
+def test_paged_attention_wrapper(oracle_lib):
+    import torch
+    inp = workload("tiny")
+    dev = gu.to_device(inp)
+    out = B.paged_attention(dev["query"], dev["key_pages"], dev["value_pages"],
+                            dev["block_table"], dev["context_lens"], inp.page_size,
+                            scale=inp.scale, causal=True)
+    torch.cuda.synchronize()
+    gu.assert_parity(gu.out_to_f64(out), gu.oracle_full(oracle_lib, inp), "bf16", "wrapper")

@@ -145,6 +145,34 @@ int pa_choose_schedule(const pa_shape* shape);
 /* Kernel launches one call of this shape and schedule enqueues. */
 int pa_launch_count(const pa_shape* shape, int schedule);
 
+/* Decode schedule without a caller workspace, for callers that cannot
+ * allocate device memory: for example a serving process whose free HBM is
+ * all owned by its K/V page pool and caching allocator, or a latency-bound
+ * decode loop that cannot afford the device-wide synchronisation cudaMalloc
+ * and cudaFree may cause.  The pages describe no such entry point; it has no
+ * counterpart there.
+ *
+ * Computes exactly what pa_paged_attention_sched(..., PA_SCHED_DECODE) does,
+ * with its scratch in one fixed array of 8 MiB that the library keeps on
+ * every device it is used on, for the life of the process.  Allocates
+ * nothing: no cudaMalloc, no cudaFree, no allocating library call.
+ *   - Shapes whose decode scratch (pa_workspace_bytes) exceeds 8 MiB are
+ *     rejected with PA_ERR_WORKSPACE before anything is enqueued.
+ *   - The first call on a device looks up the array's device address with
+ *     that device current and caches it; make that first call before any
+ *     stream capture.
+ *   - Each call clears the array's error flag, then runs; if device_flag_out
+ *     (a device pointer to one uint32, may be NULL) is given, this call's
+ *     PA_FLAG_* bits are copied there on the stream after the kernels.
+ *   - All calls share the array and it keeps the last call's contents; calls
+ *     whose kernels overlap on the GPU (e.g. on unordered streams) race. */
+pa_status pa_paged_attention_decode_noalloc(const pa_shape* shape, const void* query,
+                                            const void* key_pages, const void* value_pages,
+                                            const int32_t* block_table,
+                                            const int32_t* context_lens, float scale, int causal,
+                                            void* out, uint32_t* device_flag_out,
+                                            void* cuda_stream);
+
 const char* pa_status_str(pa_status status);
 
 #ifdef __cplusplus

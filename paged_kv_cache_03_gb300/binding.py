@@ -83,6 +83,10 @@ def load(auto_build: bool = True):
         lib.pa_paged_attention_sched.restype = ctypes.c_int
         lib.pa_paged_attention_profiled.argtypes = common + [ctypes.c_int, vp, vp]
         lib.pa_paged_attention_profiled.restype = ctypes.c_int
+        lib.pa_paged_attention_decode_noalloc.argtypes = [sp, vp, vp, vp, i32p, i32p,
+                                                          ctypes.c_float, ctypes.c_int, vp, vp,
+                                                          vp]
+        lib.pa_paged_attention_decode_noalloc.restype = ctypes.c_int
         lib.pa_gather_debug.argtypes = [sp, vp, vp, i32p, i32p, ctypes.c_int, vp, vp, vp, vp]
         lib.pa_gather_debug.restype = ctypes.c_int
         lib.pa_check_device_flag.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32), ctypes.c_int,
@@ -176,6 +180,19 @@ def pa_paged_attention_profiled(shape, query, key_pages, value_pages, block_tabl
         ctypes.byref(shape), _ptr(query), _ptr(key_pages), _ptr(value_pages), _ptr(block_table),
         _ptr(context_lens), float(scale), int(bool(causal)), _ptr(out), _ptr(workspace),
         int(workspace_bytes), _stream(stream), int(schedule), event_before, event_after)
+
+
+def pa_paged_attention_decode_noalloc(shape, query, key_pages, value_pages, block_table,
+                                      context_lens, scale, causal, out, device_flag_out=None,
+                                      stream=None) -> int:
+    """Decode schedule with the library's fixed scratch array instead of a
+    caller workspace (for callers that cannot allocate device memory).
+    device_flag_out: optional device tensor of one 32-bit word that receives
+    this call's PA_FLAG_* bits."""
+    return load().pa_paged_attention_decode_noalloc(
+        ctypes.byref(shape), _ptr(query), _ptr(key_pages), _ptr(value_pages), _ptr(block_table),
+        _ptr(context_lens), float(scale), int(bool(causal)), _ptr(out), _ptr(device_flag_out),
+        _stream(stream))
 
 
 def pa_gather_debug(shape, key_pages, value_pages, block_table, context_lens, max_S, k_dense,

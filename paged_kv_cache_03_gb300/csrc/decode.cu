@@ -12,13 +12,16 @@
 //   * A segment is (b, kv_head, chunk of <= RB query rows).  All G = H_q/H_kv
 //     query heads and L positions of one kv head are rows of the same
 //     segments, so each K/V byte is read from HBM once.
-//   * Segments are cut into tiles of TK keys.  The flattened tile list of the
-//     whole batch is split evenly over a persistent grid of one CTA per SM
-//     (stream-K), so ragged context lengths do not unbalance the SMs.  A CTA
-//     whose range covers a whole segment writes the normalised output; a
-//     segment split across CTAs leaves one fp32 partial (m, l, o[D]) per
-//     piece, merged by decode_combine_kernel (the split-combine of "Week 2
-//     Day 5", Task 2, across CTAs instead of SIMD groups).
+//   * The keys of all segments, counted in units of TK/7 keys, are cut into
+//     about eight equal chunks per SM (stream-K with dynamic chunks): a
+//     persistent grid of one CTA per SM starts on one chunk each and claims
+//     the rest from an atomic counter, so neither ragged context lengths nor
+//     SMs that stream at different speeds leave the grid unbalanced.  Each
+//     chunk is cut into tiles of up to TK keys.  A chunk that holds a whole
+//     segment writes its normalised output; a segment split across chunks
+//     leaves one fp32 partial (m, l, o[D]) per piece, merged by
+//     decode_combine_kernel (the split-combine of "Week 2 Day 5", Task 2,
+//     across CTAs instead of SIMD groups).
 //   * One producer warp resolves page ids through the block table and issues
 //     1-D bulk (TMA) copies of the page-contiguous K and V rows of each tile
 //     into a 3-stage shared-memory ring (mbarrier completion by bytes).  A
@@ -58,8 +61,10 @@ struct DecodeParams {
     void* out;
     float2* part_ml;  // [slots][RB] (m, l) per piece and row
     float* part_o;    // [slots][RB][D]
-    int* prefix;      // [B] exclusive tile prefix; [B] = total tiles; [B+1] = tiles per CTA
+    int* prefix;      // [B] exclusive unit prefix; [B] = total units; [B+1] = units per chunk
     uint32_t* flag;
+    int* chunk_counter;  // next dynamic chunk (fixed workspace offset, 0 between calls)
+    int* done_counter;   // CTAs finished (the last one resets both counters)
     int B, H_q, H_kv, L, G, num_pages, ps, max_npg, nchunk, causal;
     long long max_S;
     float scale_log2;
@@ -85,6 +90,9 @@ struct Cfg {
     static constexpr int SMEM = NST * STAGE + MERGE + NBARS * 8;
     static constexpr int THREADS = (NCW + 1) * 32;
     static constexpr int KPW = TK / NCW;  // keys per warp per stage
+    // Keys per unit of the even split over CTAs; tiles start on unit
+    // boundaries and hold at most NCW units.
+    static constexpr int GRAN = KPW;
     static constexpr int KPI = 32 / P;    // keys per warp instruction
     static constexpr int IT = KPW / KPI;
     static constexpr int DPL = kD / P;    // dims held per lane
@@ -98,9 +106,25 @@ struct Cfg {
 };
 
 struct StageHdr {
-    int seg_id, b, kvh, chunk, key0, nvalid, S, flags;
+    int seg_id, b, kvh, chunk, key0, nvalid, S, flags, slot;
 };
-enum : int { kStart = 1, kEnd = 2, kFinal = 4 };
+enum : int { kStart = 1, kEnd = 2, kFinal = 4, kLast = 8 };
+
+// Chunks of work per CTA on average (the first is static, the rest are
+// claimed dynamically).
+constexpr int kChunksPerCta = 8;
+
+// Counts this CTA as finished; the last CTA of the grid resets the chunk
+// counter and itself, so the next call starts from zero.  Every CTA calls it
+// once, after its last claim on the chunk counter.
+__device__ __forceinline__ void finish_chunk_counters(const DecodeParams& p, int grid) {
+    __threadfence();
+    if (atomicAdd(p.done_counter, 1) == grid - 1) {
+        atomicExch(p.chunk_counter, 0);
+        atomicExch(p.done_counter, 0);
+        __threadfence();
+    }
+}
 
 // The context length the kernels use for sequence b: 0 (no work, rows
 // written as zeros) when it breaks the contract.
@@ -219,26 +243,31 @@ __global__ void __launch_bounds__(C::THREADS, 1) decode_split_kernel(const Decod
     }
     fence_proxy_async_smem();
 
-    // ---- even split of the batch's tiles over the grid ----------------------
+    // ---- split of the batch's keys into chunks --------------------------------
+    // Work is counted in units of C::GRAN keys per segment and cut into about
+    // kChunksPerCta equal chunks per CTA.  CTA c starts with chunk c and then
+    // claims further chunks from a counter, so SMs that stream faster take
+    // more of them.
     const int segs_per_b = p.H_kv * p.nchunk;
     int mine = 0;
     for (int b = tid; b < p.B; b += C::THREADS)
-        mine += segs_per_b * ((checked_len(p, b, blockIdx.x == 0) + C::TK - 1) / C::TK);
+        mine += segs_per_b * ((checked_len(p, b, blockIdx.x == 0) + C::GRAN - 1) / C::GRAN);
     int total;
     block_incl_scan<C::THREADS>(mine, s_scan, &total);
-    const int per = (total + gridDim.x - 1) / gridDim.x;
-    const int t0 = blockIdx.x * per;
-    const int t1 = min(t0 + per, total);
+    const int grid = static_cast<int>(gridDim.x);
+    const int cu = max(1, (total + grid * kChunksPerCta - 1) / (grid * kChunksPerCta));
+    const int nchunks = (total + cu - 1) / cu;
+    const int u0 = static_cast<int>(blockIdx.x) * cu;
     int carry = 0;
     for (int base = 0; base < p.B; base += C::THREADS) {
         const int b = base + tid;
-        const int v = b < p.B ? segs_per_b * ((checked_len(p, b, false) + C::TK - 1) / C::TK) : 0;
+        const int v = b < p.B ? segs_per_b * ((checked_len(p, b, false) + C::GRAN - 1) / C::GRAN) : 0;
         int tot;
         const int incl = block_incl_scan<C::THREADS>(v, s_scan, &tot);
         const int excl = carry + incl - v;
         if (b < p.B) {
             if (blockIdx.x == 0) p.prefix[b] = excl;
-            if (v > 0 && excl <= t0 && t0 < excl + v) {
+            if (v > 0 && excl <= u0 && u0 < excl + v) {
                 s_start_b = b;
                 s_start_pref = excl;
             }
@@ -247,12 +276,14 @@ __global__ void __launch_bounds__(C::THREADS, 1) decode_split_kernel(const Decod
     }
     if (blockIdx.x == 0 && tid == 0) {
         p.prefix[p.B] = total;
-        p.prefix[p.B + 1] = per;
+        p.prefix[p.B + 1] = cu;
     }
     __syncthreads();
     pdl_launch_dependents();
-    if (t0 >= t1) return;
-    const int ntiles = t1 - t0;
+    if (static_cast<int>(blockIdx.x) >= nchunks) {
+        if (tid == 0) finish_chunk_counters(p, grid);
+        return;
+    }
 
     if (warp == C::NCW) {
         // =========================== producer warp ===========================
@@ -262,101 +293,123 @@ __global__ void __launch_bounds__(C::THREADS, 1) decode_split_kernel(const Decod
         const uint8_t* const qp = static_cast<const uint8_t*>(p.q);
         int b = s_start_b, bpref = s_start_pref;
         int S = checked_len(p, b, false);
-        int nts = (S + C::TK - 1) / C::TK;
-        int tiles_b = segs_per_b * nts;
-        int issued = 0;
-        for (int t = t0; t < t1; ++t) {
-            while (t >= bpref + tiles_b) {
-                bpref += tiles_b;
-                ++b;
-                S = checked_len(p, b, false);
-                nts = (S + C::TK - 1) / C::TK;
-                tiles_b = segs_per_b * nts;
-            }
-            const int loc = t - bpref;
-            const int sib = loc / nts;
-            const int j = loc - sib * nts;
-            const int kvh = sib / p.nchunk, chunk = sib - kvh * p.nchunk;
-            const int i = t - t0;
-            const int stage = i % C::NST;
-            const uint32_t fb = full0 + 8 * stage, eb = empty0 + 8 * stage;
-            if (i >= C::NST && !mbar_wait(eb, ((i / C::NST) - 1) & 1)) {
-                atomicOr(p.flag, PA_FLAG_TIMEOUT);
-                s_abort = 1;
-                break;
-            }
-            if (s_abort) break;
-            uint8_t* const st = stage0 + stage * C::STAGE;
-            const int key0 = j * C::TK;
-            const int nvalid = min(C::TK, S - key0);
-            const int lp0 = key0 / p.ps;
-            const int nseg = (key0 + nvalid - 1) / p.ps - lp0 + 1;
-            int pp[4];
-            uint32_t bytes = 0;
+        int ng = (S + C::GRAN - 1) / C::GRAN;
+        int units_b = segs_per_b * ng;
+        int issued = 0, i = 0;
+        int chunk = static_cast<int>(blockIdx.x);
+        int next = __shfl_sync(0xffffffffu, lane == 0 ? atomicAdd(p.chunk_counter, 1) : 0, 0) + grid;
+        bool stop = false;
+        while (!stop) {
+            const int cu0 = chunk * cu, cu1 = min(cu0 + cu, total);
+            const bool last_chunk = next >= nchunks;
+            for (int u = cu0; u < cu1; ++i) {
+                while (u >= bpref + units_b) {
+                    bpref += units_b;
+                    ++b;
+                    S = checked_len(p, b, false);
+                    ng = (S + C::GRAN - 1) / C::GRAN;
+                    units_b = segs_per_b * ng;
+                }
+                const int loc = u - bpref;
+                const int sib = loc / ng;
+                const int g = loc - sib * ng;
+                const int kvh = sib / p.nchunk, chunk_r = sib - kvh * p.nchunk;
+                const int seg_u0 = bpref + sib * ng, seg_u1 = seg_u0 + ng;  // segment's units
+                const int piece_u1 = min(cu1, seg_u1);
+                const int stage = i % C::NST;
+                const uint32_t fb = full0 + 8 * stage, eb = empty0 + 8 * stage;
+                if (i >= C::NST &&
+                    !__all_sync(0xffffffffu, mbar_wait(eb, ((i / C::NST) - 1) & 1))) {
+                    if (lane == 0) atomicOr(p.flag, PA_FLAG_TIMEOUT);
+                    s_abort = 1;
+                    stop = true;
+                    break;
+                }
+                if (__any_sync(0xffffffffu, s_abort != 0)) {
+                    stop = true;
+                    break;
+                }
+                uint8_t* const st = stage0 + stage * C::STAGE;
+                const int key0 = g * C::GRAN;
+                const int piece_key1 = min(S, (piece_u1 - seg_u0) * C::GRAN);
+                const int nvalid = min(C::TK, piece_key1 - key0);
+                const int u_next = u + (nvalid + C::GRAN - 1) / C::GRAN;
+                const int lp0 = key0 / p.ps;
+                const int nseg = (key0 + nvalid - 1) / p.ps - lp0 + 1;
+                int pp[4];
+                uint32_t bytes = 0;
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int sidx = lane + 32 * u;
-                pp[u] = -1;
-                if (sidx < nseg) {
-                    const int lp = lp0 + sidx;
-                    const int v = __ldg(p.bt + static_cast<long long>(b) * p.max_npg + lp);
-                    const int klo = max(key0, lp * p.ps);
-                    const int khi = min(key0 + nvalid, (lp + 1) * p.ps);
-                    if (v >= 0 && v < p.num_pages) {
-                        pp[u] = v;
-                        bytes += 2u * static_cast<uint32_t>(khi - klo) * C::ROW;
-                    } else {
-                        atomicOr(p.flag, PA_FLAG_BAD_PAGE);
+                for (int w = 0; w < 4; ++w) {
+                    const int sidx = lane + 32 * w;
+                    pp[w] = -1;
+                    if (sidx < nseg) {
+                        const int lp = lp0 + sidx;
+                        const int v = __ldg(p.bt + static_cast<long long>(b) * p.max_npg + lp);
+                        const int klo = max(key0, lp * p.ps);
+                        const int khi = min(key0 + nvalid, (lp + 1) * p.ps);
+                        if (v >= 0 && v < p.num_pages) {
+                            pp[w] = v;
+                            bytes += 2u * static_cast<uint32_t>(khi - klo) * C::ROW;
+                        } else {
+                            atomicOr(p.flag, PA_FLAG_BAD_PAGE);
+                        }
                     }
                 }
-            }
-            const bool start = (t == t0) || (j == 0);
-            const int row0 = chunk * C::RB;
-            const int nrows = min(C::RB, p.G * p.L - row0);
-            if (lane == 0 && start) bytes += static_cast<uint32_t>(nrows) * C::ROW;
-            bytes = static_cast<uint32_t>(warp_sum(static_cast<int>(bytes)));
-            if (lane == 0) {
-                StageHdr* h = reinterpret_cast<StageHdr*>(st);
-                h->seg_id = (b * p.H_kv + kvh) * p.nchunk + chunk;
-                h->b = b;
-                h->kvh = kvh;
-                h->chunk = chunk;
-                h->key0 = key0;
-                h->nvalid = nvalid;
-                h->S = S;
-                const int first_t = t - j, last_t = t - j + nts - 1;
-                h->flags = (start ? kStart : 0) | ((t == t1 - 1 || j == nts - 1) ? kEnd : 0) |
-                           ((first_t >= t0 && last_t < t1) ? kFinal : 0);
-                mbar_arrive_expect_tx(fb, bytes);
-            }
-            __syncwarp();
-            const uint32_t kdst = smem_u32(st) + C::HDR + C::QBYTES;
+                const bool start = (u == cu0) || (g == 0);
+                const int row0 = chunk_r * C::RB;
+                const int nrows = min(C::RB, p.G * p.L - row0);
+                if (lane == 0 && start) bytes += static_cast<uint32_t>(nrows) * C::ROW;
+                bytes = static_cast<uint32_t>(warp_sum(static_cast<int>(bytes)));
+                if (lane == 0) {
+                    StageHdr* h = reinterpret_cast<StageHdr*>(st);
+                    h->seg_id = (b * p.H_kv + kvh) * p.nchunk + chunk_r;
+                    h->b = b;
+                    h->kvh = kvh;
+                    h->chunk = chunk_r;
+                    h->key0 = key0;
+                    h->nvalid = nvalid;
+                    h->S = S;
+                    h->slot = h->seg_id + chunk;
+                    const bool end = u_next >= piece_u1;
+                    h->flags = (start ? kStart : 0) | (end ? kEnd : 0) |
+                               ((seg_u0 >= cu0 && seg_u1 <= cu1) ? kFinal : 0) |
+                               ((end && piece_u1 == cu1 && last_chunk) ? kLast : 0);
+                    mbar_arrive_expect_tx(fb, bytes);
+                }
+                __syncwarp();
+                const uint32_t kdst = smem_u32(st) + C::HDR + C::QBYTES;
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                if (pp[u] < 0) continue;
-                const int lp = lp0 + lane + 32 * u;
-                const int klo = max(key0, lp * p.ps);
-                const int khi = min(key0 + nvalid, (lp + 1) * p.ps);
-                const long long row =
-                    (static_cast<long long>(pp[u]) * p.H_kv + kvh) * p.ps + (klo - lp * p.ps);
-                const uint32_t nb = static_cast<uint32_t>(khi - klo) * C::ROW;
-                const uint32_t off = static_cast<uint32_t>(klo - key0) * C::ROW;
-                bulk_g2s(kdst + off, kp + row * C::ROW, nb, fb, pol);
-                bulk_g2s(kdst + C::KBYTES + off, vp + row * C::ROW, nb, fb, pol);
+                for (int w = 0; w < 4; ++w) {
+                    if (pp[w] < 0) continue;
+                    const int lp = lp0 + lane + 32 * w;
+                    const int klo = max(key0, lp * p.ps);
+                    const int khi = min(key0 + nvalid, (lp + 1) * p.ps);
+                    const long long row =
+                        (static_cast<long long>(pp[w]) * p.H_kv + kvh) * p.ps + (klo - lp * p.ps);
+                    const uint32_t nb = static_cast<uint32_t>(khi - klo) * C::ROW;
+                    const uint32_t off = static_cast<uint32_t>(klo - key0) * C::ROW;
+                    bulk_g2s(kdst + off, kp + row * C::ROW, nb, fb, pol);
+                    bulk_g2s(kdst + C::KBYTES + off, vp + row * C::ROW, nb, fb, pol);
+                }
+                if (lane == 0 && start) {
+                    const long long qrow =
+                        (static_cast<long long>(b) * p.H_q + static_cast<long long>(kvh) * p.G) * p.L +
+                        row0;
+                    bulk_g2s(smem_u32(st) + C::HDR, qp + qrow * C::ROW,
+                             static_cast<uint32_t>(nrows) * C::ROW, fb, pol);
+                }
+                issued = i + 1;
+                u = u_next;
             }
-            if (lane == 0 && start) {
-                const long long qrow =
-                    (static_cast<long long>(b) * p.H_q + static_cast<long long>(kvh) * p.G) * p.L +
-                    row0;
-                bulk_g2s(smem_u32(st) + C::HDR, qp + qrow * C::ROW,
-                         static_cast<uint32_t>(nrows) * C::ROW, fb, pol);
-            }
-            issued = i + 1;
+            if (stop || last_chunk) break;
+            chunk = next;
+            next = __shfl_sync(0xffffffffu, lane == 0 ? atomicAdd(p.chunk_counter, 1) : 0, 0) + grid;
         }
         // Never leave with copies in flight into this CTA's shared memory.
         for (int k = max(0, issued - C::NST); k < issued; ++k)
             if (!mbar_wait(full0 + 8 * (k % C::NST), (k / C::NST) & 1))
                 atomicOr(p.flag, PA_FLAG_TIMEOUT);
+        if (lane == 0) finish_chunk_counters(p, grid);
         return;
     }
 
@@ -381,14 +434,14 @@ __global__ void __launch_bounds__(C::THREADS, 1) decode_split_kernel(const Decod
         }
     }
 
-    for (int i = 0; i < ntiles; ++i) {
+    for (int i = 0;; ++i) {
         const int stage = i % C::NST;
-        if (!mbar_wait(full0 + 8 * stage, (i / C::NST) & 1)) {
-            atomicOr(p.flag, PA_FLAG_TIMEOUT);
+        if (!__all_sync(0xffffffffu, mbar_wait(full0 + 8 * stage, (i / C::NST) & 1))) {
+            if (lane == 0) atomicOr(p.flag, PA_FLAG_TIMEOUT);
             s_abort = 1;
             break;
         }
-        if (s_abort) break;
+        if (__any_sync(0xffffffffu, s_abort != 0)) break;
         const uint8_t* const st = stage0 + stage * C::STAGE;
         const StageHdr h = *reinterpret_cast<const StageHdr*>(st);
 
@@ -529,8 +582,8 @@ __global__ void __launch_bounds__(C::THREADS, 1) decode_split_kernel(const Decod
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(mfull);
-            if (!mbar_wait(mfull, nend & 1)) {
-                atomicOr(p.flag, PA_FLAG_TIMEOUT);
+            if (!__all_sync(0xffffffffu, mbar_wait(mfull, nend & 1))) {
+                if (lane == 0) atomicOr(p.flag, PA_FLAG_TIMEOUT);
                 s_abort = 1;
                 break;
             }
@@ -538,7 +591,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) decode_split_kernel(const Decod
             const long long base_row =
                 (static_cast<long long>(h.b) * p.H_q + static_cast<long long>(h.kvh) * p.G) * p.L +
                 static_cast<long long>(h.chunk) * C::RB;
-            const long long slot = static_cast<long long>(h.seg_id) + blockIdx.x;
+            const long long slot = h.slot;
             for (int idx = tid; idx < C::RB * kD; idx += C::NCW * 32) {
                 const int r = idx / kD, d = idx - r * kD;
                 if (r >= rows_valid) continue;
@@ -564,20 +617,36 @@ __global__ void __launch_bounds__(C::THREADS, 1) decode_split_kernel(const Decod
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(mdone);
-            if (!mbar_wait(mdone, nend & 1)) {
-                atomicOr(p.flag, PA_FLAG_TIMEOUT);
+            if (!__all_sync(0xffffffffu, mbar_wait(mdone, nend & 1))) {
+                if (lane == 0) atomicOr(p.flag, PA_FLAG_TIMEOUT);
                 s_abort = 1;
                 break;
             }
             ++nend;
         }
+        if (h.flags & kLast) break;
     }
 }
 
-// Merges the pieces of every segment that was split across CTAs; writes
-// zeros for sequences whose context length broke the contract.
+// Four output dims of one row, stored together.
+template <typename T>
+__device__ __forceinline__ void store4(T* base, long long idx, float4 v);
+template <>
+__device__ __forceinline__ void store4<__nv_bfloat16>(__nv_bfloat16* base, long long idx, float4 v) {
+    *reinterpret_cast<uint2*>(reinterpret_cast<uint16_t*>(base) + idx) =
+        make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
+}
+template <>
+__device__ __forceinline__ void store4<float>(float* base, long long idx, float4 v) {
+    *reinterpret_cast<float4*>(base + idx) = v;
+}
+
+// Merges the pieces of every segment that was split across CTAs (one CTA per
+// segment, one warp per row, four dims per lane; the pieces' (m, l) are read
+// by the lanes in parallel), and writes zeros for sequences whose context
+// length broke the contract.
 template <class C>
-__global__ void __launch_bounds__(kD) decode_combine_kernel(const DecodeParams p) {
+__global__ void __launch_bounds__(128) decode_combine_kernel(const DecodeParams p) {
     using T = typename C::Elem;
     pdl_wait_primary();
     const int seg = blockIdx.x;
@@ -585,36 +654,59 @@ __global__ void __launch_bounds__(kD) decode_combine_kernel(const DecodeParams p
     const int b = seg / segs_per_b, sib = seg - b * segs_per_b;
     const int kvh = sib / p.nchunk, chunk = sib - kvh * p.nchunk;
     const int S = checked_len(p, b, false);
-    const int nts = (S + C::TK - 1) / C::TK;
+    const int ng = (S + C::GRAN - 1) / C::GRAN;
     const int rows_valid = min(C::RB, p.G * p.L - chunk * C::RB);
     const long long base_row =
         (static_cast<long long>(b) * p.H_q + static_cast<long long>(kvh) * p.G) * p.L +
         static_cast<long long>(chunk) * C::RB;
     T* const out = static_cast<T*>(p.out);
-    const int d = threadIdx.x;
-    if (nts == 0) {
-        for (int r = 0; r < rows_valid; ++r) store_elem<T>(out, (base_row + r) * kD + d, 0.f);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int d0 = lane * 4;
+    if (ng == 0) {
+        for (int r = warp; r < rows_valid; r += 4)
+            store4<T>(out, (base_row + r) * kD + d0, make_float4(0.f, 0.f, 0.f, 0.f));
         return;
     }
     const int per = p.prefix[p.B + 1];
-    const int first = p.prefix[b] + sib * nts;
-    const int c0 = first / per, c1 = (first + nts - 1) / per;
+    const int first = p.prefix[b] + sib * ng;
+    const int c0 = first / per, c1 = (first + ng - 1) / per;
     if (c0 == c1) return;  // the segment lay in one CTA, which wrote it
-    for (int r = 0; r < rows_valid; ++r) {
+    const int np = c1 - c0 + 1;
+    const long long slot0 = static_cast<long long>(seg) + c0;
+    for (int r = warp; r < rows_valid; r += 4) {
         float M = neg_inf();
-        for (int c = c0; c <= c1; ++c)
-            M = fmaxf(M, p.part_ml[(static_cast<long long>(seg) + c) * C::RB + r].x);
-        float den = 0.f, acc = 0.f;
+        for (int i = lane; i < np; i += 32) M = fmaxf(M, p.part_ml[(slot0 + i) * C::RB + r].x);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        float den = 0.f;
         if (M != neg_inf()) {
-            for (int c = c0; c <= c1; ++c) {
-                const long long slot = static_cast<long long>(seg) + c;
-                const float2 ml = p.part_ml[slot * C::RB + r];
-                const float a = fast_exp2(ml.x - M);
-                den += a * ml.y;
-                acc += a * p.part_o[(slot * C::RB + r) * kD + d];
+            for (int base = 0; base < np; base += 32) {
+                const int i = base + lane;
+                float a = 0.f;
+                if (i < np) {
+                    const float2 ml = p.part_ml[(slot0 + i) * C::RB + r];
+                    a = fast_exp2(ml.x - M);
+                    den += a * ml.y;
+                }
+                const int n = min(32, np - base);
+#pragma unroll 4
+                for (int j = 0; j < n; ++j) {
+                    const float aj = __shfl_sync(0xffffffffu, a, j);
+                    const float4 o = *reinterpret_cast<const float4*>(
+                        p.part_o + ((slot0 + base + j) * C::RB + r) * kD + d0);
+                    acc.x += aj * o.x;
+                    acc.y += aj * o.y;
+                    acc.z += aj * o.z;
+                    acc.w += aj * o.w;
+                }
             }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
         }
-        store_elem<T>(out, (base_row + r) * kD + d, den > 0.f ? acc / den : 0.f);
+        const float inv = den > 0.f ? 1.f / den : 0.f;
+        store4<T>(out, (base_row + r) * kD + d0,
+                  make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv));
     }
 }
 
@@ -631,7 +723,7 @@ WsLayout ws_layout(const pa_shape& sh, int grid, int RB) {
     const long long nchunk = (G * sh.L + RB - 1) / RB;
     WsLayout w;
     w.nseg = static_cast<long long>(sh.B) * sh.H_kv * nchunk;
-    w.slots = w.nseg + grid;
+    w.slots = w.nseg + static_cast<long long>(grid) * kChunksPerCta;
     size_t off = kFlagBytes;
     w.prefix_off = off;
     off = align_up(off + 4 * (static_cast<size_t>(sh.B) + 2), 256);
@@ -649,10 +741,10 @@ pa_status launch_cfg(const Call& c) {
     const int grid = decode_grid(sh, c.dev.sm_count);
     const WsLayout w = ws_layout(sh, grid, C::RB);
     if (c.ws_bytes < w.total) return PA_ERR_WORKSPACE;
-    // Bound on the flattened tile count: every index stays inside int.
-    const long long max_tiles = w.nseg * ((static_cast<long long>(sh.max_pages_per_seq) *
-                                               sh.page_size + C::TK - 1) / C::TK);
-    if (max_tiles >= INT_MAX / 2) return PA_ERR_UNSUPPORTED;
+    // Bound on the flattened unit count: every index stays inside int.
+    const long long max_units = w.nseg * ((static_cast<long long>(sh.max_pages_per_seq) *
+                                               sh.page_size + C::GRAN - 1) / C::GRAN);
+    if (max_units >= INT_MAX / 2) return PA_ERR_UNSUPPORTED;
 
     static int attr_done[64] = {0};
     if (c.dev.device >= 0 && c.dev.device < 64 && !attr_done[c.dev.device]) {
@@ -673,6 +765,8 @@ pa_status launch_cfg(const Call& c) {
     p.part_o = reinterpret_cast<float*>(ws + w.o_off);
     p.prefix = reinterpret_cast<int*>(ws + w.prefix_off);
     p.flag = reinterpret_cast<uint32_t*>(ws);
+    p.chunk_counter = reinterpret_cast<int*>(ws + kChunkCounterOffset);
+    p.done_counter = reinterpret_cast<int*>(ws + kDoneCounterOffset);
     p.B = sh.B;
     p.H_q = sh.H_q;
     p.H_kv = sh.H_kv;
@@ -693,7 +787,7 @@ pa_status launch_cfg(const Call& c) {
 
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(w.nseg));
-    cfg.blockDim = dim3(kD);
+    cfg.blockDim = dim3(128);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = c.stream;
     cudaLaunchAttribute attr[1];

@@ -11,8 +11,11 @@
 namespace pa {
 
 constexpr int kHeadDim = 128;
-// Workspace: [0, kFlagBytes) holds the sticky flag word.
+// Workspace: [0, kFlagBytes) holds the sticky flag word (offset 0) and the
+// decode schedule's chunk counters, all zero between calls.
 constexpr size_t kFlagBytes = 256;
+constexpr size_t kChunkCounterOffset = 64;
+constexpr size_t kDoneCounterOffset = 128;
 
 struct DeviceInfo {
     int device = -1;

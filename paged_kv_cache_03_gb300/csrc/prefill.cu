@@ -1,10 +1,515 @@
 // prefill.cu -- schedule (b): long causal prefills on tcgen05 tensor cores.
+//
+// What it computes is the same exact paged attention as the page walk
+// ("Week 3 Day 5: Paged FlashAttention"): Task 1's page translation while
+// staging K/V tiles, Task 2's tiled online softmax (Q.K^T -> scale and causal
+// bounds -> merge the max -> rescale sum and accumulator -> exponentials and
+// sum -> P.V), whole K/V tiles past the causal frontier skipped, and the
+// normalised bf16 output written once.
+//
+// How it is laid out on GB300 (one CTA per 128-row query tile):
+//   * The 128 rows of a tile are Lt = 128/G consecutive positions l of all G
+//     query heads that share one kv head (GQA packing), so one K/V tile feeds
+//     128 rows and the causal frontier moves by only Lt keys across the tile.
+//   * Warp 0 stages tiles with 2-D TMA loads (128-byte swizzle): the query
+//     tile once (one box per head), then 128-key K and V tiles into a 2-stage
+//     ring.  Every box lies inside one page: box height = gcd(page_size, 128)
+//     rows, its row coordinate (physical_page * H_kv + kv_head) * page_size +
+//     slot comes from the block table, so a tile that crosses pages is just
+//     several boxes.
+//   * Warp 1 allocates 512 TMEM columns (S double-buffered at columns 0 and
+//     128, O at 256) and one thread issues tcgen05.mma: S = Q.K^T (M=N=128,
+//     K=16 steps over D), then O += P.V with V read MN-major from its
+//     natural [key][dim] layout.
+//   * Warps 2-5 (128 threads, one TMEM lane = one query row each) run the
+//     softmax: S row from TMEM, scale*log2(e), causal/length mask, running
+//     max moved only when it grows by more than 2^8 (then O is rescaled in
+//     TMEM), exp2, P rounded to bf16 into swizzled shared memory for the P.V
+//     MMA, running sum of those bf16 weights; at the end O/l -> bf16 -> global.
+//   * All waits are bounded; on a timeout the CTA records PA_FLAG_TIMEOUT,
+//     lets its copies and MMAs finish, frees TMEM and exits.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
 #include "internal.h"
+#include "ptx.cuh"
+#include "tc.cuh"
 
 namespace pa {
+namespace {
 
-bool prefill_supported(const pa_shape& /*sh*/) { return false; }
+constexpr int kD = kHeadDim;
+constexpr int BM = 128;  // query rows per tile
+constexpr int BN = 128;  // keys per K/V tile
+constexpr int kStages = 2;
+constexpr int kThreads = 192;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColS = 0, kColO = 256;
+constexpr float kLazyRescaleLog2 = 8.0f;
 
-pa_status prefill_launch(const Call& /*c*/) { return PA_ERR_UNSUPPORTED; }
+// shared memory map (offsets from a 1024-byte aligned base)
+constexpr int kHalf = BM * 128;  // 128 rows x 64 bf16 (one 128-byte swizzle column block)
+constexpr int kTile = 2 * kHalf; // 128 rows x 128 bf16
+constexpr int kOffQ = 0;
+constexpr int kOffKV = kOffQ + kTile;  // stage s: K at kOffKV + 2*s*kTile, V after it
+constexpr int kOffP = kOffKV + kStages * 2 * kTile;
+constexpr int kOffBar = kOffP + kTile;
+enum Bar {
+    kQFull = 0,
+    kKVFull = 1,   // + stage
+    kKVEmpty = 3,  // + stage
+    kSFull = 5,    // + buffer
+    kSFree = 7,    // + buffer
+    kPFull = 9,
+    kODone = 10,
+    kMmaDone = 11,
+    kNumBars = 12
+};
+constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
+constexpr int kOffAbort = kOffTmemSlot + 8;
+constexpr int kSmemUsed = kOffAbort + 8;
+constexpr int kSmemBytes = kSmemUsed + 1024;  // slack to align the base
+
+struct PrefillParams {
+    const int32_t* bt;
+    const int32_t* ctx;
+    void* out;
+    uint32_t* flag;
+    int B, H_q, H_kv, L, G, Lt, nM, num_pages, ps, max_npg, box_rows, causal;
+    long long max_S;
+    float scale_log2;
+};
+
+__device__ __forceinline__ float neg_inf() { return __int_as_float(0xff800000); }
+
+// All 32 lanes wait; the warp agrees on the outcome (a lane that timed out
+// makes the whole warp give up, so warp-collective instructions stay uniform).
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity) {
+    const bool ok = mbar_wait(bar, parity);
+    return __all_sync(0xffffffffu, ok);
+}
+
+// Warp-uniform read of the CTA's abort flag.
+__device__ __forceinline__ bool aborted(volatile int* f) {
+    return __any_sync(0xffffffffu, *f != 0);
+}
+
+__device__ __forceinline__ void give_up(const PrefillParams& p, volatile int* abort_flag) {
+    *abort_flag = 1;
+    atomicOr(p.flag, PA_FLAG_TIMEOUT);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    prefill_tile_kernel(const __grid_constant__ CUtensorMap tm_q,
+                        const __grid_constant__ CUtensorMap tm_k,
+                        const __grid_constant__ CUtensorMap tm_v, const PrefillParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t* const sbase = smem_raw + (base - raw);
+    const uint32_t bar0 = base + kOffBar;
+    auto bar = [&](int i) { return bar0 + 8u * static_cast<uint32_t>(i); };
+    volatile int* const abort_flag = reinterpret_cast<volatile int*>(sbase + kOffAbort);
+    uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(sbase + kOffTmemSlot);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+    // ---- which tile ---------------------------------------------------------
+    const int per_m = p.H_kv * p.B;
+    const int m = p.nM - 1 - static_cast<int>(blockIdx.x) / per_m;  // heavy tiles first
+    const int rest = static_cast<int>(blockIdx.x) % per_m;
+    const int b = rest / p.H_kv, kvh = rest % p.H_kv;
+    const int l0 = m * p.Lt;
+    const int S = p.ctx[b];
+    const bool valid_seq =
+        S >= 1 && static_cast<long long>(S) <= p.max_S && !(p.causal && S < p.L);
+    const int l_last = min(l0 + p.Lt, p.L) - 1;
+    const int lim_max = p.causal ? l_last + S - p.L : S - 1;  // last key any row sees
+    const int lim_min = p.causal ? l0 + S - p.L : S - 1;      // last key row l0 sees
+    const int nk = valid_seq ? lim_max / BN + 1 : 0;
+
+    // ---- set-up: barriers, V stages zeroed, TMEM ---------------------------
+    if (tid == 0) {
+        mbar_init(bar(kQFull), 1);
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(bar(kKVFull + s), 1);
+            mbar_init(bar(kKVEmpty + s), 1);
+            mbar_init(bar(kSFull + s), 1);
+            mbar_init(bar(kSFree + s), 4);
+        }
+        mbar_init(bar(kPFull), 4);
+        mbar_init(bar(kODone), 1);
+        mbar_init(bar(kMmaDone), 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    // key rows that are never loaded must hold finite values (their weight is
+    // exactly 0, and 0 * NaN would not be)
+    for (int s = 0; s < kStages; ++s) {
+        uint4* v = reinterpret_cast<uint4*>(sbase + kOffKV + (2 * s + 1) * kTile);
+        for (int i = tid; i < kTile / 16; i += kThreads) v[i] = make_uint4(0u, 0u, 0u, 0u);
+    }
+    fence_proxy_async_smem();
+    if (warp == 1) {
+        tc::tmem_alloc(base + kOffTmemSlot, kTmemCols);
+        tc::tmem_relinquish();
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+    if (!valid_seq && tid == 0) atomicOr(p.flag, PA_FLAG_BAD_CONTEXT);
+
+    if (warp == 0 && nk > 0) {
+        // ============================ TMA producer ============================
+        const uint64_t pol_q = l2_policy_evict_first();
+        const uint64_t pol_kv = l2_policy_evict_last();
+        if (lane == 0) {
+            tc::prefetch_tensormap(&tm_q);
+            tc::prefetch_tensormap(&tm_k);
+            tc::prefetch_tensormap(&tm_v);
+            // query tile: one box of Lt rows per head, both 64-dim halves
+            mbar_arrive_expect_tx(bar(kQFull), static_cast<uint32_t>(p.G * p.Lt * 128 * 2));
+            for (int g = 0; g < p.G; ++g) {
+                const int row = ((b * p.H_q) + kvh * p.G + g) * p.L + l0;
+                for (int h = 0; h < 2; ++h)
+                    tc::tma_load_2d(base + kOffQ + h * kHalf + g * p.Lt * 128, &tm_q, h * 64, row,
+                                    bar(kQFull), pol_q);
+            }
+        }
+        __syncwarp();
+        const int nbox = BN / p.box_rows;  // boxes per K/V tile (<= 128)
+        const uint32_t box_bytes = static_cast<uint32_t>(p.box_rows) * 128u;
+        int issued = 0;
+        for (int j = 0; j < nk; ++j) {
+            const int s = j & 1;
+            if (j >= kStages && !warp_wait(bar(kKVEmpty + s), ((j >> 1) - 1) & 1)) {
+                if (lane == 0) give_up(p, abort_flag);
+                break;
+            }
+            if (aborted(abort_flag)) break;
+            int prow[4];
+            uint32_t bytes = 0;
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
+                const int bi = lane + 32 * w;
+                prow[w] = -1;
+                const int key = j * BN + bi * p.box_rows;
+                if (bi < nbox && key < S) {
+                    const int lp = key / p.ps, slot = key - lp * p.ps;
+                    const int pp = __ldg(p.bt + static_cast<long long>(b) * p.max_npg + lp);
+                    if (pp >= 0 && pp < p.num_pages) {
+                        prow[w] = (pp * p.H_kv + kvh) * p.ps + slot;
+                        bytes += 4u * box_bytes;  // K and V, two halves each
+                    } else {
+                        atomicOr(p.flag, PA_FLAG_BAD_PAGE);
+                    }
+                }
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) bytes += __shfl_xor_sync(0xffffffffu, bytes, o);
+            if (lane == 0) mbar_arrive_expect_tx(bar(kKVFull + s), bytes);
+            __syncwarp();
+            const uint32_t kdst = base + kOffKV + 2 * s * kTile;
+            const uint32_t vdst = kdst + kTile;
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
+                if (prow[w] < 0) continue;
+                const uint32_t off = static_cast<uint32_t>(lane + 32 * w) * box_bytes;
+                for (int h = 0; h < 2; ++h) {
+                    tc::tma_load_2d(kdst + h * kHalf + off, &tm_k, h * 64, prow[w],
+                                    bar(kKVFull + s), pol_kv);
+                    tc::tma_load_2d(vdst + h * kHalf + off, &tm_v, h * 64, prow[w],
+                                    bar(kKVFull + s), pol_kv);
+                }
+            }
+            issued = j + 1;
+        }
+        // let every copy into this CTA's shared memory land before leaving
+        if (!mbar_wait(bar(kQFull), 0)) give_up(p, abort_flag);
+        for (int j = max(0, issued - kStages); j < issued; ++j)
+            if (!mbar_wait(bar(kKVFull + (j & 1)), (j >> 1) & 1)) give_up(p, abort_flag);
+    } else if (warp == 1 && nk > 0) {
+        // ============================ MMA issuer =============================
+        if (lane == 0) {
+            constexpr uint32_t idS = tc::idesc_bf16(BM, BN, 0, 0);   // Q, K both K-major
+            constexpr uint32_t idO = tc::idesc_bf16(BM, kD, 0, 1);   // P K-major, V MN-major
+            bool ok = mbar_wait(bar(kQFull), 0);
+            for (int j = 0; ok && j <= nk; ++j) {
+                if (j < nk) {
+                    const int s = j & 1;
+                    ok = mbar_wait(bar(kKVFull + s), (j >> 1) & 1) &&
+                         (j < kStages || mbar_wait(bar(kSFree + s), ((j >> 1) - 1) & 1));
+                    if (!ok || *abort_flag) break;
+                    tc::fence_after_sync();
+                    const uint32_t kaddr = base + kOffKV + 2 * s * kTile;
+#pragma unroll
+                    for (int kk = 0; kk < kD / 16; ++kk) {
+                        const uint32_t koff = (kk >> 2) * kHalf + (kk & 3) * 32;
+                        tc::mma_bf16(tmem + kColS + s * BN,
+                                     tc::smem_desc_sw128(base + kOffQ + koff, 16, 1024),
+                                     tc::smem_desc_sw128(kaddr + koff, 16, 1024), idS, kk > 0);
+                    }
+                    tc::commit(bar(kSFull + s));
+                }
+                if (j >= 1) {
+                    const int jp = j - 1, sp = jp & 1;
+                    ok = mbar_wait(bar(kPFull), jp & 1);
+                    if (!ok || *abort_flag) break;
+                    tc::fence_after_sync();
+                    const uint32_t vaddr = base + kOffKV + (2 * sp + 1) * kTile;
+#pragma unroll
+                    for (int kk = 0; kk < BN / 16; ++kk) {
+                        const uint32_t poff = (kk >> 2) * kHalf + (kk & 3) * 32;
+                        tc::mma_bf16(tmem + kColO, tc::smem_desc_sw128(base + kOffP + poff, 16, 1024),
+                                     tc::smem_desc_sw128(vaddr + kk * 16 * 128, kHalf, 1024), idO,
+                                     (jp > 0 || kk > 0) ? 1u : 0u);
+                    }
+                    tc::commit(bar(kODone));
+                    tc::commit(bar(kKVEmpty + sp));
+                }
+            }
+            if (!ok) give_up(p, abort_flag);
+            // nothing of ours may still be running when TMEM is freed
+            tc::commit(bar(kMmaDone));
+            if (!mbar_wait(bar(kMmaDone), 0)) give_up(p, abort_flag);
+        }
+        __syncwarp();
+    } else if (warp >= 2) {
+        // ============================= softmax ===============================
+        const int q4 = warp & 3;            // TMEM lane quarter of this warp
+        const int r = q4 * 32 + lane;       // query row of this thread
+        const uint32_t trow = tmem + (static_cast<uint32_t>(q4 * 32) << 16);
+        const int g = r / p.Lt, l = l0 + (r - g * p.Lt);
+        const bool row_valid = g < p.G && l < p.L;
+        const int h = kvh * p.G + g;
+        const int lim = min(p.causal ? l + S - p.L : S - 1, S - 1);
+        float mrow = neg_inf(), lsum = 0.f;
+        bool ok = true;
+        for (int j = 0; j < nk; ++j) {
+            const int s = j & 1;
+            ok = warp_wait(bar(kSFull + s), (j >> 1) & 1);
+            if (!ok || aborted(abort_flag)) break;
+            tc::fence_after_sync();
+            float x[4][32];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) tc::ld32(trow + kColS + s * BN + c * 32, x[c]);
+            tc::wait_ld();
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(kSFree + s));
+            // scale, mask, row max of this tile
+            const bool masking = j * BN + BN - 1 > lim_min;
+            const int cmax = lim - j * BN;  // columns c <= cmax are visible
+            float mt = neg_inf();
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+#pragma unroll
+                for (int e = 0; e < 32; ++e) {
+                    float v = x[c][e] * p.scale_log2;
+                    if (masking && c * 32 + e > cmax) v = neg_inf();
+                    x[c][e] = v;
+                    mt = fmaxf(mt, v);
+                }
+            }
+            const bool grow = mt > mrow + kLazyRescaleLog2;
+            // P.V of the previous tile must be done before O or P are touched
+            if (j > 0) {
+                ok = warp_wait(bar(kODone), (j - 1) & 1);
+                if (!ok || aborted(abort_flag)) break;
+                tc::fence_after_sync();
+            }
+            if (__any_sync(0xffffffffu, grow)) {
+                const float mn = grow ? mt : mrow;
+                const float alpha = grow ? fast_exp2(mrow - mn) : 1.f;  // 2^-inf = 0 at the start
+                if (j > 0) {
+#pragma unroll 1
+                    for (int c = 0; c < 4; ++c) {
+                        float o[32];
+                        tc::ld32(trow + kColO + c * 32, o);
+                        tc::wait_ld();
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) o[e] *= alpha;
+                        tc::st32(trow + kColO + c * 32, o);
+                    }
+                    tc::wait_st();
+                }
+                lsum *= alpha;
+                mrow = mn;
+            }
+            const float mu = (mrow == neg_inf()) ? 0.f : mrow;
+            uint8_t* const prow = sbase + kOffP + r * 128;
+#pragma unroll
+            for (int q = 0; q < 16; ++q) {  // 8 keys per 16-byte chunk
+                const int c = q >> 2, e0 = (q & 3) * 8;
+                float pv[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) pv[e] = fast_exp2(x[c][e0 + e] - mu);
+                const uint4 w = make_uint4(pack_bf16x2(pv[0], pv[1]), pack_bf16x2(pv[2], pv[3]),
+                                           pack_bf16x2(pv[4], pv[5]), pack_bf16x2(pv[6], pv[7]));
+                // the running sum adds the bf16 weights the tensor core multiplies,
+                // so the final division normalises exactly those weights
+                const float2 s0 = bf16x2_to_float2(w.x), s1 = bf16x2_to_float2(w.y);
+                const float2 s2 = bf16x2_to_float2(w.z), s3 = bf16x2_to_float2(w.w);
+                lsum += ((s0.x + s0.y) + (s1.x + s1.y)) + ((s2.x + s2.y) + (s3.x + s3.y));
+                const int half = q >> 3, cq = q & 7;
+                *reinterpret_cast<uint4*>(prow + half * kHalf + ((cq ^ (r & 7)) << 4)) = w;
+            }
+            fence_proxy_async_smem();
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(kPFull));
+        }
+        if (!ok) {
+            if (lane == 0) give_up(p, abort_flag);
+        } else if (nk > 0 && warp_wait(bar(kODone), (nk - 1) & 1)) {
+            tc::fence_after_sync();
+            const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+            uint16_t* const orow = static_cast<uint16_t*>(p.out) +
+                                   ((static_cast<long long>(b) * p.H_q + h) * p.L + l) * kD;
+#pragma unroll 1
+            for (int c = 0; c < 4; ++c) {
+                float o[32];
+                tc::ld32(trow + kColO + c * 32, o);
+                tc::wait_ld();
+                if (row_valid) {
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const uint4 w = make_uint4(
+                            pack_bf16x2(o[q * 8 + 0] * inv, o[q * 8 + 1] * inv),
+                            pack_bf16x2(o[q * 8 + 2] * inv, o[q * 8 + 3] * inv),
+                            pack_bf16x2(o[q * 8 + 4] * inv, o[q * 8 + 5] * inv),
+                            pack_bf16x2(o[q * 8 + 6] * inv, o[q * 8 + 7] * inv));
+                        *reinterpret_cast<uint4*>(orow + c * 32 + q * 8) = w;
+                    }
+                }
+            }
+        } else if (nk > 0) {
+            if (lane == 0) give_up(p, abort_flag);
+        }
+        if (!valid_seq && row_valid) {
+            uint4* orow = reinterpret_cast<uint4*>(
+                static_cast<uint16_t*>(p.out) +
+                ((static_cast<long long>(b) * p.H_q + h) * p.L + l) * kD);
+            for (int q = 0; q < kD / 8; ++q) orow[q] = make_uint4(0u, 0u, 0u, 0u);
+        }
+    }
+
+    // ---- tear-down: free TMEM once every role is done -----------------------
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        tc::fence_after_sync();
+        tc::tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static std::once_flag once;
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    std::call_once(once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+        else
+            cudaGetLastError();
+    });
+    return fn;
+}
+
+// 2-D bf16 map over a row-major [rows, 128] matrix, boxes of 64 x box_rows,
+// 128-byte swizzle.
+bool make_map(CUtensorMap* map, const void* ptr, long long rows, int box_rows) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(kD) * 2};
+    cuuint32_t box[2] = {64u, static_cast<cuuint32_t>(box_rows)};
+    cuuint32_t estr[2] = {1u, 1u};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int gcd_int(int a, int b) {
+    while (b) {
+        const int t = a % b;
+        a = b;
+        b = t;
+    }
+    return a;
+}
+
+}  // namespace
+
+bool prefill_supported(const pa_shape& sh) {
+    if (sh.dtype != PA_BF16 || sh.D != kD) return false;
+    const int G = sh.H_q / sh.H_kv;
+    // G must divide the 128-row tile, and every TMA box must start on a
+    // 1024-byte (8-row) boundary of the 128-byte swizzle: query boxes are
+    // 128/G rows, key/value boxes gcd(page_size, 128) rows.
+    if (G < 1 || G > 16 || (BM % G) != 0) return false;
+    if (sh.page_size % 8 != 0) return false;
+    const long long q_rows = static_cast<long long>(sh.B) * sh.H_q * sh.L;
+    if (q_rows >= (1ll << 31)) return false;
+    const long long nM = (sh.L + BM / G - 1) / (BM / G);
+    if (nM * sh.H_kv * sh.B >= (1ll << 31)) return false;
+    return true;
+}
+
+pa_status prefill_launch(const Call& c) {
+    const pa_shape& sh = c.sh;
+    if (!prefill_supported(sh)) return PA_ERR_UNSUPPORTED;
+    if (c.dev.smem_optin < kSmemBytes) return PA_ERR_UNSUPPORTED;
+    const int G = sh.H_q / sh.H_kv;
+    const int Lt = BM / G;
+    const int box_rows = gcd_int(sh.page_size, BN);
+    CUtensorMap tq, tk, tv;
+    const long long pool_rows = static_cast<long long>(sh.num_pages) * sh.H_kv * sh.page_size;
+    if (!make_map(&tq, c.q, static_cast<long long>(sh.B) * sh.H_q * sh.L, Lt) ||
+        !make_map(&tk, c.kp, pool_rows, box_rows) || !make_map(&tv, c.vp, pool_rows, box_rows))
+        return PA_ERR_CUDA;
+
+    static int attr_done[64] = {0};
+    if (c.dev.device >= 0 && c.dev.device < 64 && !attr_done[c.dev.device]) {
+        if (cudaFuncSetAttribute(prefill_tile_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kSmemBytes) != cudaSuccess)
+            return PA_ERR_CUDA;
+        attr_done[c.dev.device] = 1;
+    }
+    PrefillParams p;
+    p.bt = c.bt;
+    p.ctx = c.ctx;
+    p.out = c.out;
+    p.flag = static_cast<uint32_t*>(c.ws);
+    p.B = sh.B;
+    p.H_q = sh.H_q;
+    p.H_kv = sh.H_kv;
+    p.L = sh.L;
+    p.G = G;
+    p.Lt = Lt;
+    p.nM = (sh.L + Lt - 1) / Lt;
+    p.num_pages = sh.num_pages;
+    p.ps = sh.page_size;
+    p.max_npg = sh.max_pages_per_seq;
+    p.box_rows = box_rows;
+    p.causal = c.causal ? 1 : 0;
+    p.max_S = static_cast<long long>(sh.max_pages_per_seq) * sh.page_size;
+    p.scale_log2 = c.scale * 1.4426950408889634f;
+    const unsigned grid = static_cast<unsigned>(static_cast<long long>(p.nM) * sh.H_kv * sh.B);
+    if (c.ev_before && cudaEventRecord(c.ev_before, c.stream) != cudaSuccess) return PA_ERR_CUDA;
+    prefill_tile_kernel<<<grid, kThreads, kSmemBytes, c.stream>>>(tq, tk, tv, p);
+    if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
+    if (c.ev_after && cudaEventRecord(c.ev_after, c.stream) != cudaSuccess) return PA_ERR_CUDA;
+    return PA_OK;
+}
 
 }  // namespace pa

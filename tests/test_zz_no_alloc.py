@@ -5,9 +5,10 @@ is all owned by its K/V page pool and caching allocator, or a latency-bound
 decode loop that cannot afford the device-wide synchronisation cudaMalloc and
 cudaFree may cause.  For them the library keeps its decode scratch in one
 fixed device array.  These tests call that entry point through the C ABI and
-check it against the regular entry point, on consecutive calls that reuse the
-shared scratch, and check that a shape needing more scratch than the fixed
-maximum is refused.  This file is collected last on purpose.
+check it against the regular entry point running the same decode schedule,
+on consecutive calls that reuse the shared scratch, and check that a shape
+needing more scratch than the fixed maximum is refused.  This file is
+collected last on purpose.
 """
 import numpy as np
 import pytest
@@ -33,7 +34,8 @@ def test_noalloc_matches_regular_entry_point_on_consecutive_calls():
     for inp in _inputs():  # consecutive calls share (and reuse) the fixed scratch
         dev = gu.to_device(inp)
         shape = B.shape_of(dev["query"], dev["key_pages"], dev["block_table"])
-        ref, _ = gu.run(inp, B.PA_SCHED_AUTO, dev=dev)
+        # the regular entry point running the same (decode) schedule
+        ref, _ = gu.run(inp, B.PA_SCHED_DECODE, dev=dev)
         out = torch.full_like(dev["query"], float("nan"))
         flag = torch.full((1,), -1, dtype=torch.int32, device="cuda")
         st = B.pa_paged_attention_decode_noalloc(

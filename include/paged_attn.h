@@ -26,7 +26,8 @@
  *   out          [B, H_q, L, D]                  same dtype as query
  * D must be 128.  All device pointers must be 16-byte aligned.
  * Entries block_table[b, i] with i >= ceil(context_lens[b] / page_size) are
- * never read and may hold anything.
+ * never used and may hold anything (the kernels may load them, always inside
+ * the [B, max_pages_per_seq] table, but no page is read through them).
  *
  * Ownership: the caller allocates and owns every buffer, including the
  * workspace.  The library allocates no device memory in any call.  Calls are

@@ -13,7 +13,7 @@
 //     query heads and L positions of one kv head are rows of the same
 //     segments, so each K/V byte is read from HBM once.
 //   * The keys of all segments, counted in units of TK/7 keys, are cut into
-//     about eight equal chunks per SM (stream-K with dynamic chunks): a
+//     about four equal chunks per SM (stream-K with dynamic chunks): a
 //     persistent grid of one CTA per SM starts on one chunk each and claims
 //     the rest from an atomic counter, so neither ragged context lengths nor
 //     SMs that stream at different speeds leave the grid unbalanced.  Each
@@ -68,9 +68,10 @@ struct DecodeParams {
     int B, H_q, H_kv, L, G, num_pages, ps, max_npg, nchunk, causal;
     long long max_S;
     float scale_log2;
+    int tk_pages, tk_slots;  // a full tile of TK keys spans TK / ps pages + TK % ps slots
 };
 
-template <typename T, int RB_, int P_, int TK_, int NCW_, int NST_>
+template <typename T, int RB_, int P_, int TK_, int NCW_, int NST_, int MINB_ = 1, int GRAN_ = 0>
 struct Cfg {
     using Elem = T;
     static constexpr int RB = RB_;    // query rows per segment
@@ -78,21 +79,26 @@ struct Cfg {
     static constexpr int TK = TK_;    // keys per stage
     static constexpr int NCW = NCW_;  // consumer warps
     static constexpr int NST = NST_;  // pipeline stages
+    static constexpr int MINB = MINB_;  // CTAs resident per SM
     static constexpr int ES = sizeof(T);
     static constexpr int ROW = kD * ES;
     static constexpr int HDR = 128;
     static constexpr int QBYTES = RB * ROW;
     static constexpr int KBYTES = TK * ROW;
     static constexpr int STAGE = HDR + QBYTES + 2 * KBYTES;
-    static constexpr int MSTRIDE = kD + 2;  // floats per (warp, row) merge record
+    // merge record per (warp, row): o[128] then m, l (16-byte aligned rows)
+    static constexpr int MSTRIDE = kD + 4;
     static constexpr int MERGE = (NCW * RB * MSTRIDE * 4 + 127) / 128 * 128;
+    // per-warp softmax weights of one stage, [KPW keys][RB rows]
+    static constexpr int PBUF = (NCW * (TK / NCW) * RB * 4 + 127) / 128 * 128;
     static constexpr int NBARS = 2 * NST + 2;
-    static constexpr int SMEM = NST * STAGE + MERGE + NBARS * 8;
+    static constexpr int SMEM = NST * STAGE + MERGE + PBUF + NBARS * 8;
     static constexpr int THREADS = (NCW + 1) * 32;
     static constexpr int KPW = TK / NCW;  // keys per warp per stage
-    // Keys per unit of the even split over CTAs; tiles start on unit
-    // boundaries and hold at most NCW units.
-    static constexpr int GRAN = KPW;
+    // Keys per unit of the split over CTAs (a power of two dividing TK);
+    // tiles start on unit boundaries.
+    static constexpr int GRAN = GRAN_ > 0 ? GRAN_ : KPW;
+    static_assert(TK % GRAN == 0, "tiles are whole units");
     static constexpr int KPI = 32 / P;    // keys per warp instruction
     static constexpr int IT = KPW / KPI;
     static constexpr int DPL = kD / P;    // dims held per lane
@@ -101,18 +107,18 @@ struct Cfg {
     static_assert(KPW % KPI == 0, "keys per warp must fill whole instructions");
     static_assert(DPL % CH == 0 && DPL % 2 == 0, "lane dims must be whole chunks");
     static_assert(STAGE % 128 == 0, "stage alignment");
-    static_assert(TK <= 128, "at most 128 page pieces per tile (4 per producer lane)");
-    static_assert(THREADS % 128 == 0, "whole warps per SM sub-partition");
+    static constexpr int PIECE_ITERS = (TK + 31) / 32;  // page pieces per producer lane (ps = 1)
+    static_assert((THREADS * MINB) % 128 == 0, "whole warps per SM sub-partition");
 };
 
-struct StageHdr {
-    int seg_id, b, kvh, chunk, key0, nvalid, S, flags, slot;
+struct alignas(16) StageHdr {
+    int seg_id, b, kvh, chunk, key0, nvalid, S, flags, slot, pad0, pad1, pad2;
 };
 enum : int { kStart = 1, kEnd = 2, kFinal = 4, kLast = 8 };
 
 // Chunks of work per CTA on average (the first is static, the rest are
 // claimed dynamically).
-constexpr int kChunksPerCta = 8;
+constexpr int kChunksPerCta = 4;
 
 // Counts this CTA as finished; the last CTA of the grid resets the chunk
 // counter and itself, so the next call starts from zero.  Every CTA calls it
@@ -191,31 +197,148 @@ __device__ __forceinline__ void load_row(const uint8_t* row, int li, float2 (&v)
     }
 }
 
-// Dim index of lane-element e (0 <= e < DPL).
+
+
+// The producer's position in the flattened work list, advanced tile by tile
+// without divisions.  Page ids of the current sequence are held in two
+// 32-entry register windows (lane i: pages wb + i and wb + 32 + i), the
+// second one loaded while the first is in use, and the first window of the
+// next sequence is requested as soon as a sequence is entered, so block-table
+// lookups stay off the path from a freed stage to its next copy.
 template <class C>
-__device__ __forceinline__ int lane_dim(int li, int e) {
-    return (li + (e / C::CH) * C::P) * C::CH + e % C::CH;
+struct Walker {
+    int chunk, next, cu0, cu1;  // current chunk, the one claimed after it, its units
+    int u;                      // first unit of the next tile
+    int b, bpref, S, ng;        // sequence, its first unit, length, units per segment
+    int sib, g;                 // segment within the sequence, unit within the segment
+    int kvh, chunk_r;           // kv head and row chunk of the segment
+    int key0, lp, slot;         // first key of the next tile, its page and slot
+    int S_ahead;                // context length of sequence b + 1 (requested early)
+    int wb, win0, win1;         // page-id windows of sequence b
+    int nb_win;                 // pages 0..31 of sequence b + 1
+};
+
+__device__ __forceinline__ int sanitized_len(const DecodeParams& p, int S) {
+    return (S < 1 || static_cast<long long>(S) > p.max_S || (p.causal && S < p.L)) ? 0 : S;
 }
 
+// Block-table entry (b, lp), or -1 past the row.  The page windows may fetch
+// entries past a sequence's last page; those values are never used.
+__device__ __forceinline__ int bt_entry(const DecodeParams& p, int b, int lp) {
+    return lp < p.max_npg ? __ldg(p.bt + static_cast<long long>(b) * p.max_npg + lp) : -1;
+}
+
+template <class C>
+__device__ __forceinline__ void load_windows(const DecodeParams& p, int lane, Walker<C>& w) {
+    w.win0 = bt_entry(p, w.b, w.wb + lane);
+    w.win1 = bt_entry(p, w.b, w.wb + 32 + lane);
+}
+
+// Position the walker at unit w.u (a chunk start); sequences at or after w.b.
+template <class C>
+__device__ void walker_seek(const DecodeParams& p, int lane, int segs_per_b, Walker<C>& w) {
+    while (w.u >= w.bpref + segs_per_b * w.ng) {
+        w.bpref += segs_per_b * w.ng;
+        ++w.b;
+        w.S = sanitized_len(p, w.S_ahead);
+        w.ng = (w.S + C::GRAN - 1) / C::GRAN;
+        w.S_ahead = w.b + 1 < p.B ? __ldg(p.ctx + w.b + 1) : 0;
+    }
+    const int loc = w.u - w.bpref;
+    w.sib = loc / w.ng;
+    w.g = loc - w.sib * w.ng;
+    w.kvh = w.sib / p.nchunk;
+    w.chunk_r = w.sib - w.kvh * p.nchunk;
+    w.key0 = w.g * C::GRAN;
+    w.lp = w.key0 / p.ps;
+    w.slot = w.key0 - w.lp * p.ps;
+    w.wb = w.lp;
+    load_windows(p, lane, w);
+    w.nb_win = w.b + 1 < p.B ? bt_entry(p, w.b + 1, lane) : -1;
+}
+
+// Page id of page index `lpi` of sequence w.b (all lanes call it together;
+// lanes whose piece is not `active` get -1 without touching memory).
+template <class C>
+__device__ __forceinline__ int page_id(const DecodeParams& p, const Walker<C>& w, int lpi,
+                                       bool active) {
+    const int rel = lpi - w.wb;
+    const int a = __shfl_sync(0xffffffffu, w.win0, rel & 31);
+    const int c = __shfl_sync(0xffffffffu, w.win1, rel & 31);
+    if (!active) return -1;
+    if (rel >= 0 && rel < 32) return a;
+    if (rel >= 32 && rel < 64) return c;
+    return bt_entry(p, w.b, lpi);  // outside both windows (tiny pages): direct
+}
+
+// Row owned by in-group lane li after transpose_reduce<RB, P>: each
+// splitting step keeps the upper half of the remaining rows in lanes whose
+// step bit is set.
+template <int RB, int P>
+__device__ __forceinline__ int row_of_lane(int li) {
+    int rho = 0, rc = RB;
+#pragma unroll
+    for (int step = P / 2; step >= 1; step >>= 1) {
+        if (rc > 1) {
+            if (li & step) rho += rc / 2;
+            rc /= 2;
+        }
+    }
+    return rho;
+}
+
+// Sums v[r] over the P lanes of a group for every row r and leaves the total
+// of row row_of_lane(li) in this lane.  While more than one row is left, a
+// step exchanges half of them (the half the partner keeps) instead of all,
+// so RB rows over P lanes cost RB - 1 + log2(P / RB) shuffles, not
+// RB * log2(P).
+template <int RB, int P>
+__device__ __forceinline__ float transpose_reduce(float (&v)[RB], int li) {
+    static_assert(RB <= P, "one lane per row at least");
+    int rc = RB;
+#pragma unroll
+    for (int step = P / 2; step >= 1; step >>= 1) {
+        if (rc > 1) {
+            const bool up = (li & step) != 0;
+            const int half = rc / 2;
+#pragma unroll
+            for (int i = 0; i < RB / 2; ++i) {
+                if (i < half) {
+                    const float send = up ? v[i] : v[i + half];
+                    const float keep = up ? v[i + half] : v[i];
+                    v[i] = keep + __shfl_xor_sync(0xffffffffu, send, step);
+                }
+            }
+            rc = half;
+        } else {
+            v[0] += __shfl_xor_sync(0xffffffffu, v[0], step);
+        }
+    }
+    return v[0];
+}
+
+// Four output dims of one row, stored together.
 template <typename T>
-__device__ __forceinline__ void store_elem(T* base, long long idx, float v);
+__device__ __forceinline__ void store4(T* base, long long idx, float4 v);
 template <>
-__device__ __forceinline__ void store_elem<__nv_bfloat16>(__nv_bfloat16* base, long long idx,
-                                                          float v) {
-    reinterpret_cast<uint16_t*>(base)[idx] = float_to_bf16_bits(v);
+__device__ __forceinline__ void store4<__nv_bfloat16>(__nv_bfloat16* base, long long idx, float4 v) {
+    *reinterpret_cast<uint2*>(reinterpret_cast<uint16_t*>(base) + idx) =
+        make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
 }
 template <>
-__device__ __forceinline__ void store_elem<float>(float* base, long long idx, float v) {
-    base[idx] = v;
+__device__ __forceinline__ void store4<float>(float* base, long long idx, float4 v) {
+    *reinterpret_cast<float4*>(base + idx) = v;
 }
 
 template <class C>
-__global__ void __launch_bounds__(C::THREADS, 1) decode_split_kernel(const DecodeParams p) {
+__global__ void __launch_bounds__(C::THREADS, C::MINB) decode_split_kernel(const DecodeParams p) {
     using T = typename C::Elem;
     extern __shared__ __align__(128) uint8_t smem[];
     uint8_t* const stage0 = smem;
     float* const merge = reinterpret_cast<float*>(smem + C::NST * C::STAGE);
-    uint64_t* const bars = reinterpret_cast<uint64_t*>(smem + C::NST * C::STAGE + C::MERGE);
+    float* const pbuf_all = reinterpret_cast<float*>(smem + C::NST * C::STAGE + C::MERGE);
+    uint64_t* const bars =
+        reinterpret_cast<uint64_t*>(smem + C::NST * C::STAGE + C::MERGE + C::PBUF);
     __shared__ int s_scan[32];
     __shared__ int s_start_b, s_start_pref;
     __shared__ volatile int s_abort;
@@ -291,119 +414,171 @@ __global__ void __launch_bounds__(C::THREADS, 1) decode_split_kernel(const Decod
         const uint8_t* const kp = static_cast<const uint8_t*>(p.kp);
         const uint8_t* const vp = static_cast<const uint8_t*>(p.vp);
         const uint8_t* const qp = static_cast<const uint8_t*>(p.q);
-        int b = s_start_b, bpref = s_start_pref;
-        int S = checked_len(p, b, false);
-        int ng = (S + C::GRAN - 1) / C::GRAN;
-        int units_b = segs_per_b * ng;
-        int issued = 0, i = 0;
-        int chunk = static_cast<int>(blockIdx.x);
-        int next = __shfl_sync(0xffffffffu, lane == 0 ? atomicAdd(p.chunk_counter, 1) : 0, 0) + grid;
-        bool stop = false;
-        while (!stop) {
-            const int cu0 = chunk * cu, cu1 = min(cu0 + cu, total);
-            const bool last_chunk = next >= nchunks;
-            for (int u = cu0; u < cu1; ++i) {
-                while (u >= bpref + units_b) {
-                    bpref += units_b;
-                    ++b;
-                    S = checked_len(p, b, false);
-                    ng = (S + C::GRAN - 1) / C::GRAN;
-                    units_b = segs_per_b * ng;
-                }
-                const int loc = u - bpref;
-                const int sib = loc / ng;
-                const int g = loc - sib * ng;
-                const int kvh = sib / p.nchunk, chunk_r = sib - kvh * p.nchunk;
-                const int seg_u0 = bpref + sib * ng, seg_u1 = seg_u0 + ng;  // segment's units
-                const int piece_u1 = min(cu1, seg_u1);
-                const int stage = i % C::NST;
-                const uint32_t fb = full0 + 8 * stage, eb = empty0 + 8 * stage;
-                if (i >= C::NST &&
-                    !__all_sync(0xffffffffu, mbar_wait(eb, ((i / C::NST) - 1) & 1))) {
-                    if (lane == 0) atomicOr(p.flag, PA_FLAG_TIMEOUT);
-                    s_abort = 1;
-                    stop = true;
-                    break;
-                }
-                if (__any_sync(0xffffffffu, s_abort != 0)) {
-                    stop = true;
-                    break;
-                }
-                uint8_t* const st = stage0 + stage * C::STAGE;
-                const int key0 = g * C::GRAN;
-                const int piece_key1 = min(S, (piece_u1 - seg_u0) * C::GRAN);
-                const int nvalid = min(C::TK, piece_key1 - key0);
-                const int u_next = u + (nvalid + C::GRAN - 1) / C::GRAN;
-                const int lp0 = key0 / p.ps;
-                const int nseg = (key0 + nvalid - 1) / p.ps - lp0 + 1;
-                int pp[4];
-                uint32_t bytes = 0;
+        constexpr int kGranShift = __builtin_ctz(C::GRAN);
+        static_assert((C::GRAN & (C::GRAN - 1)) == 0, "unit size must be a power of two");
+        Walker<C> w;
+        w.chunk = static_cast<int>(blockIdx.x);
+        w.next = __shfl_sync(0xffffffffu, lane == 0 ? atomicAdd(p.chunk_counter, 1) : 0, 0) + grid;
+        w.cu0 = w.chunk * cu;
+        w.cu1 = min(w.cu0 + cu, total);
+        w.u = w.cu0;
+        w.b = s_start_b;
+        w.bpref = s_start_pref;
+        w.S = sanitized_len(p, __ldg(p.ctx + w.b));
+        w.ng = (w.S + C::GRAN - 1) / C::GRAN;
+        w.S_ahead = w.b + 1 < p.B ? __ldg(p.ctx + w.b + 1) : 0;
+        walker_seek<C>(p, lane, segs_per_b, w);
+        int issued = 0;
+        for (int i = 0;; ++i) {
+            // ---- this tile: keys [key0, key0 + nvalid) of segment (b, sib) ----
+            const int seg_u0 = w.bpref + w.sib * w.ng, seg_u1 = seg_u0 + w.ng;
+            const int piece_u1 = min(w.cu1, seg_u1);
+            const int piece_key1 = min(w.S, (piece_u1 - seg_u0) << kGranShift);
+            const int nvalid = min(C::TK, piece_key1 - w.key0);
+            const int units = (nvalid + C::GRAN - 1) >> kGranShift;
+            const bool last_chunk = w.next >= nchunks;
+            const bool start = (w.u == w.cu0) || (w.g == 0);
+            const bool end = w.u + units >= piece_u1;
+            const int flags = (start ? kStart : 0) | (end ? kEnd : 0) |
+                              ((seg_u0 >= w.cu0 && seg_u1 <= w.cu1) ? kFinal : 0) |
+                              ((end && piece_u1 == w.cu1 && last_chunk) ? kLast : 0);
+            // page pieces: piece j covers page lp + j (lane j + 32 k handles it);
+            // a tile spans at most TK / ps + 2 pages, one lane each unless ps < 4
+            const int row0 = w.chunk_r * C::RB;
+            const int nrows = min(C::RB, p.G * p.L - row0);
+            int pid[C::PIECE_ITERS], klo[C::PIECE_ITERS], kn[C::PIECE_ITERS];
+            bool any_bad = false;
 #pragma unroll
-                for (int w = 0; w < 4; ++w) {
-                    const int sidx = lane + 32 * w;
-                    pp[w] = -1;
-                    if (sidx < nseg) {
-                        const int lp = lp0 + sidx;
-                        const int v = __ldg(p.bt + static_cast<long long>(b) * p.max_npg + lp);
-                        const int klo = max(key0, lp * p.ps);
-                        const int khi = min(key0 + nvalid, (lp + 1) * p.ps);
-                        if (v >= 0 && v < p.num_pages) {
-                            pp[w] = v;
-                            bytes += 2u * static_cast<uint32_t>(khi - klo) * C::ROW;
-                        } else {
-                            atomicOr(p.flag, PA_FLAG_BAD_PAGE);
-                        }
+            for (int k = 0; k < C::PIECE_ITERS; ++k) {
+                pid[k] = -1;
+                klo[k] = 0;
+                kn[k] = 0;
+                if (k > 0 && p.ps >= 4) continue;  // uniform: whole warp skips
+                const int j = lane + 32 * k;
+                const int lo = j == 0 ? w.key0 : w.key0 - w.slot + j * p.ps;
+                const int hi = min(w.key0 + nvalid, w.key0 - w.slot + (j + 1) * p.ps);
+                const bool active = lo < hi;
+                const int id = page_id<C>(p, w, w.lp + j, active);
+                klo[k] = lo;
+                kn[k] = hi - lo;
+                if (active) {
+                    if (id >= 0 && id < p.num_pages) {
+                        pid[k] = id;
+                    } else {
+                        any_bad = true;
                     }
                 }
-                const bool start = (u == cu0) || (g == 0);
-                const int row0 = chunk_r * C::RB;
-                const int nrows = min(C::RB, p.G * p.L - row0);
-                if (lane == 0 && start) bytes += static_cast<uint32_t>(nrows) * C::ROW;
-                bytes = static_cast<uint32_t>(warp_sum(static_cast<int>(bytes)));
-                if (lane == 0) {
-                    StageHdr* h = reinterpret_cast<StageHdr*>(st);
-                    h->seg_id = (b * p.H_kv + kvh) * p.nchunk + chunk_r;
-                    h->b = b;
-                    h->kvh = kvh;
-                    h->chunk = chunk_r;
-                    h->key0 = key0;
-                    h->nvalid = nvalid;
-                    h->S = S;
-                    h->slot = h->seg_id + chunk;
-                    const bool end = u_next >= piece_u1;
-                    h->flags = (start ? kStart : 0) | (end ? kEnd : 0) |
-                               ((seg_u0 >= cu0 && seg_u1 <= cu1) ? kFinal : 0) |
-                               ((end && piece_u1 == cu1 && last_chunk) ? kLast : 0);
-                    mbar_arrive_expect_tx(fb, bytes);
-                }
-                __syncwarp();
-                const uint32_t kdst = smem_u32(st) + C::HDR + C::QBYTES;
-#pragma unroll
-                for (int w = 0; w < 4; ++w) {
-                    if (pp[w] < 0) continue;
-                    const int lp = lp0 + lane + 32 * w;
-                    const int klo = max(key0, lp * p.ps);
-                    const int khi = min(key0 + nvalid, (lp + 1) * p.ps);
-                    const long long row =
-                        (static_cast<long long>(pp[w]) * p.H_kv + kvh) * p.ps + (klo - lp * p.ps);
-                    const uint32_t nb = static_cast<uint32_t>(khi - klo) * C::ROW;
-                    const uint32_t off = static_cast<uint32_t>(klo - key0) * C::ROW;
-                    bulk_g2s(kdst + off, kp + row * C::ROW, nb, fb, pol);
-                    bulk_g2s(kdst + C::KBYTES + off, vp + row * C::ROW, nb, fb, pol);
-                }
-                if (lane == 0 && start) {
-                    const long long qrow =
-                        (static_cast<long long>(b) * p.H_q + static_cast<long long>(kvh) * p.G) * p.L +
-                        row0;
-                    bulk_g2s(smem_u32(st) + C::HDR, qp + qrow * C::ROW,
-                             static_cast<uint32_t>(nrows) * C::ROW, fb, pol);
-                }
-                issued = i + 1;
-                u = u_next;
             }
-            if (stop || last_chunk) break;
-            chunk = next;
-            next = __shfl_sync(0xffffffffu, lane == 0 ? atomicAdd(p.chunk_counter, 1) : 0, 0) + grid;
+            // bytes the stage will receive: all K/V rows of the tile (plus the
+            // query rows at a piece start), minus pieces with a bad page id
+            uint32_t bytes = 2u * static_cast<uint32_t>(nvalid) * C::ROW +
+                             (start ? static_cast<uint32_t>(nrows) * C::ROW : 0u);
+            if (__ballot_sync(0xffffffffu, any_bad)) {
+                uint32_t miss = 0;
+#pragma unroll
+                for (int k = 0; k < C::PIECE_ITERS; ++k)
+                    if (kn[k] > 0 && pid[k] < 0) miss += 2u * static_cast<uint32_t>(kn[k]) * C::ROW;
+                bytes -= static_cast<uint32_t>(warp_sum(static_cast<int>(miss)));
+                if (any_bad) atomicOr(p.flag, PA_FLAG_BAD_PAGE);
+            }
+
+            const int stage = i % C::NST;
+            const uint32_t fb = full0 + 8 * stage, eb = empty0 + 8 * stage;
+            if (i >= C::NST &&
+                !__all_sync(0xffffffffu, mbar_wait(eb, ((i / C::NST) - 1) & 1))) {
+                if (lane == 0) atomicOr(p.flag, PA_FLAG_TIMEOUT);
+                s_abort = 1;
+                break;
+            }
+            if ((i & 7) == 0 && __any_sync(0xffffffffu, s_abort != 0)) break;
+            uint8_t* const st = stage0 + stage * C::STAGE;
+            if (lane == 0) {
+                const int seg_id = (w.b * p.H_kv + w.kvh) * p.nchunk + w.chunk_r;
+                uint4* h = reinterpret_cast<uint4*>(st);
+                h[0] = make_uint4(seg_id, w.b, w.kvh, w.chunk_r);
+                h[1] = make_uint4(w.key0, nvalid, w.S, flags);
+                h[2] = make_uint4(seg_id + w.chunk, 0, 0, 0);
+                mbar_arrive_expect_tx(fb, bytes);
+            }
+            __syncwarp();
+            const uint32_t kdst = smem_u32(st) + C::HDR + C::QBYTES;
+#pragma unroll
+            for (int k = 0; k < C::PIECE_ITERS; ++k) {
+                if (pid[k] < 0) continue;
+                const int j = lane + 32 * k;
+                const long long row = (static_cast<long long>(pid[k]) * p.H_kv + w.kvh) * p.ps +
+                                      (j == 0 ? w.slot : 0);
+                const uint32_t nb = static_cast<uint32_t>(kn[k]) * C::ROW;
+                const uint32_t off = static_cast<uint32_t>(klo[k] - w.key0) * C::ROW;
+                bulk_g2s(kdst + off, kp + row * C::ROW, nb, fb, pol);
+                bulk_g2s(kdst + C::KBYTES + off, vp + row * C::ROW, nb, fb, pol);
+            }
+            if (lane == 0 && start) {
+                const long long qrow = (static_cast<long long>(w.b) * p.H_q +
+                                        static_cast<long long>(w.kvh) * p.G) * p.L + row0;
+                bulk_g2s(smem_u32(st) + C::HDR, qp + qrow * C::ROW,
+                         static_cast<uint32_t>(nrows) * C::ROW, fb, pol);
+            }
+            issued = i + 1;
+
+            // ---- advance to the next tile ----
+            w.u += units;
+            if (w.u >= w.cu1) {
+                if (last_chunk) break;
+                w.chunk = w.next;
+                w.next = __shfl_sync(0xffffffffu, lane == 0 ? atomicAdd(p.chunk_counter, 1) : 0,
+                                     0) + grid;
+                w.cu0 = w.chunk * cu;
+                w.cu1 = min(w.cu0 + cu, total);
+                w.u = w.cu0;
+                walker_seek<C>(p, lane, segs_per_b, w);
+            } else if (w.u >= seg_u1) {
+                // next segment: same sequence (next row chunk / kv head) or the next one
+                w.g = 0;
+                w.key0 = 0;
+                w.lp = 0;
+                w.slot = 0;
+                ++w.sib;
+                if (++w.chunk_r == p.nchunk) {
+                    w.chunk_r = 0;
+                    ++w.kvh;
+                }
+                if (w.sib == segs_per_b) {
+                    // next sequence with work (sequences with no keys are skipped)
+                    do {
+                        w.bpref += segs_per_b * w.ng;
+                        ++w.b;
+                        w.S = sanitized_len(p, w.S_ahead);
+                        w.ng = (w.S + C::GRAN - 1) / C::GRAN;
+                        w.S_ahead = w.b + 1 < p.B ? __ldg(p.ctx + w.b + 1) : 0;
+                        w.win0 = w.nb_win;
+                        w.nb_win = w.b + 1 < p.B ? bt_entry(p, w.b + 1, lane) : -1;
+                    } while (w.ng == 0);
+                    w.sib = 0;
+                    w.kvh = 0;
+                    w.chunk_r = 0;
+                    w.wb = 0;
+                    w.win1 = bt_entry(p, w.b, 32 + lane);
+                } else if (w.wb != 0) {
+                    w.wb = 0;
+                    load_windows(p, lane, w);
+                }
+            } else {
+                // a full tile (nvalid == TK) inside the segment
+                w.g += units;
+                w.key0 += nvalid;
+                w.lp += p.tk_pages;
+                w.slot += p.tk_slots;
+                if (w.slot >= p.ps) {
+                    w.slot -= p.ps;
+                    ++w.lp;
+                }
+                if (w.lp >= w.wb + 32) {  // slide the windows by 32 pages
+                    w.wb += 32;
+                    w.win0 = w.win1;
+                    w.win1 = bt_entry(p, w.b, w.wb + 32 + lane);
+                }
+            }
         }
         // Never leave with copies in flight into this CTA's shared memory.
         for (int k = max(0, issued - C::NST); k < issued; ++k)
@@ -414,24 +589,28 @@ __global__ void __launch_bounds__(C::THREADS, 1) decode_split_kernel(const Decod
     }
 
     // ============================ consumer warps ============================
+    // Q.K^T: P lanes share one key (each holds DPL dims of every query row in
+    // registers); after the transposed reduction each lane owns the score of
+    // row `rho` of its group's key, so exp2 and the running sum run once per
+    // (key, row).  P.V: lane i owns output dims 4i..4i+3 of every row and
+    // walks the warp's keys, reading the weights from a per-warp buffer, so
+    // the accumulator is 4 floats per row and never needs a cross-lane sum.
     const int grp = lane / C::P, li = lane % C::P;
+    const int rho = row_of_lane<C::RB, C::P>(li);
+    constexpr int SPREAD = C::P / C::RB;  // lanes of a group that own the same row
+    float* const pbuf = pbuf_all + warp * C::KPW * C::RB;
     float2 q2[C::RB][C::DPL / 2];
-    float2 o2[C::RB][C::DPL / 2];
-    float mrow[C::RB], lsum[C::RB];
-    int lrow[C::RB];
+    float2 o4[C::RB][2];                      // dims 4*lane .. 4*lane+3 of each row
+    float m_mine = neg_inf(), l_mine = 0.f;  // running max / sum of row rho
+    int lrow_mine = 0;
     int lmin = 0;
     int nend = 0;
     T* const out = static_cast<T*>(p.out);
 #pragma unroll
     for (int r = 0; r < C::RB; ++r) {
-        mrow[r] = neg_inf();
-        lsum[r] = 0.f;
-        lrow[r] = 0;
 #pragma unroll
-        for (int e = 0; e < C::DPL / 2; ++e) {
-            q2[r][e] = make_float2(0.f, 0.f);
-            o2[r][e] = make_float2(0.f, 0.f);
-        }
+        for (int e = 0; e < C::DPL / 2; ++e) q2[r][e] = make_float2(0.f, 0.f);
+        o4[r][0] = o4[r][1] = make_float2(0.f, 0.f);
     }
 
     for (int i = 0;; ++i) {
@@ -441,7 +620,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) decode_split_kernel(const Decod
             s_abort = 1;
             break;
         }
-        if (__any_sync(0xffffffffu, s_abort != 0)) break;
+        if ((i & 7) == 0 && __any_sync(0xffffffffu, s_abort != 0)) break;
         const uint8_t* const st = stage0 + stage * C::STAGE;
         const StageHdr h = *reinterpret_cast<const StageHdr*>(st);
 
@@ -455,35 +634,34 @@ __global__ void __launch_bounds__(C::THREADS, 1) decode_split_kernel(const Decod
                 for (int e = 0; e < C::DPL / 2; ++e) {
                     q2[r][e].x *= p.scale_log2;
                     q2[r][e].y *= p.scale_log2;
-                    o2[r][e] = make_float2(0.f, 0.f);
                 }
-                mrow[r] = neg_inf();
-                lsum[r] = 0.f;
-                lrow[r] = r < rows ? (h.chunk * C::RB + r) % p.L : p.L - 1;
-                lmin = min(lmin, lrow[r]);
+                o4[r][0] = o4[r][1] = make_float2(0.f, 0.f);
+                lmin = min(lmin, r < rows ? (h.chunk * C::RB + r) % p.L : p.L - 1);
             }
+            lrow_mine = rho < rows ? (h.chunk * C::RB + rho) % p.L : p.L - 1;
+            m_mine = neg_inf();
+            l_mine = 0.f;
         }
 
         const int kw0 = warp * C::KPW;
         if (h.nvalid > kw0) {
             const uint8_t* const Ks = st + C::HDR + C::QBYTES;
             const uint8_t* const Vs = Ks + C::KBYTES;
-            float s[C::IT][C::RB];
+            float sc[C::IT];  // score of (this group's key of iteration it, row rho)
 #pragma unroll
             for (int it = 0; it < C::IT; ++it) {
                 const int kl = kw0 + it * C::KPI + grp;
                 float2 k2[C::DPL / 2];
                 load_row<C>(Ks + kl * C::ROW, li, k2);
+                float d[C::RB];
 #pragma unroll
                 for (int r = 0; r < C::RB; ++r) {
                     float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
                     for (int e = 0; e < C::DPL / 2; ++e) acc = __ffma2_rn(q2[r][e], k2[e], acc);
-                    float d = acc.x + acc.y;
-#pragma unroll
-                    for (int o = 1; o < C::P; o <<= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
-                    s[it][r] = d;
+                    d[r] = acc.x + acc.y;
                 }
+                sc[it] = transpose_reduce<C::RB, C::P>(d, li);
             }
             // Score mask (the separate "second mask" of a masked load): keys
             // past the context or past a row's causal frontier get -inf.
@@ -494,91 +672,79 @@ __global__ void __launch_bounds__(C::THREADS, 1) decode_split_kernel(const Decod
                 for (int it = 0; it < C::IT; ++it) {
                     const int kl = kw0 + it * C::KPI + grp;
                     const int kg = h.key0 + kl;
-#pragma unroll
-                    for (int r = 0; r < C::RB; ++r) {
-                        const bool vis = kl < h.nvalid && (!p.causal || kg <= lrow[r] + h.S - p.L);
-                        if (!vis) s[it][r] = neg_inf();
-                    }
+                    const bool vis =
+                        kl < h.nvalid && (!p.causal || kg <= lrow_mine + h.S - p.L);
+                    if (!vis) sc[it] = neg_inf();
                 }
             }
-            float mt[C::RB];
-            bool resc = false;
+            float mt = sc[0];
 #pragma unroll
-            for (int r = 0; r < C::RB; ++r) {
-                float x = s[0][r];
+            for (int it = 1; it < C::IT; ++it) mt = fmaxf(mt, sc[it]);
 #pragma unroll
-                for (int it = 1; it < C::IT; ++it) x = fmaxf(x, s[it][r]);
-#pragma unroll
-                for (int o = C::P; o < 32; o <<= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
-                mt[r] = x;
-                resc |= x > mrow[r] + kLazyRescaleLog2;
-            }
-            if (resc) {
+            for (int o = C::P; o < 32; o <<= 1) mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, o));
+            const bool grow = mt > m_mine + kLazyRescaleLog2;
+            if (__any_sync(0xffffffffu, grow)) {
+                // rows whose max grew by more than 2^8 move it and rescale
+                const float a = grow ? fast_exp2(m_mine - mt) : 1.f;  // 2^-inf = 0 at the start
+                if (grow) m_mine = mt;
+                l_mine *= a;
 #pragma unroll
                 for (int r = 0; r < C::RB; ++r) {
-                    const float mn = fmaxf(mrow[r], mt[r]);
-                    const float a = (mn == neg_inf()) ? 1.f : fast_exp2(mrow[r] - mn);
-                    lsum[r] *= a;
-#pragma unroll
-                    for (int e = 0; e < C::DPL / 2; ++e) {
-                        o2[r][e].x *= a;
-                        o2[r][e].y *= a;
-                    }
-                    mrow[r] = mn;
+                    const float ar = __shfl_sync(0xffffffffu, a, r * SPREAD);
+                    o4[r][0].x *= ar;
+                    o4[r][0].y *= ar;
+                    o4[r][1].x *= ar;
+                    o4[r][1].y *= ar;
                 }
             }
-            float mu[C::RB];
-#pragma unroll
-            for (int r = 0; r < C::RB; ++r) mu[r] = (mrow[r] == neg_inf()) ? 0.f : mrow[r];
+            const float mu = (m_mine == neg_inf()) ? 0.f : m_mine;
 #pragma unroll
             for (int it = 0; it < C::IT; ++it) {
-                const int kl = kw0 + it * C::KPI + grp;
-                float2 v2[C::DPL / 2];
-                load_row<C>(Vs + kl * C::ROW, li, v2);
+                const float pm = fast_exp2(sc[it] - mu);
+                l_mine += pm;
+                if (li % SPREAD == 0) pbuf[(it * C::KPI + grp) * C::RB + rho] = pm;
+            }
+            __syncwarp();
+#pragma unroll 4
+            for (int k = 0; k < C::KPW; ++k) {
+                const int kl = kw0 + k;  // this warp's keys in order
+                float pw[C::RB];
+#pragma unroll
+                for (int r = 0; r < C::RB; ++r) pw[r] = pbuf[k * C::RB + r];
+                float2 v0, v1;
+                if constexpr (sizeof(T) == 2) {
+                    const uint2 u = *reinterpret_cast<const uint2*>(Vs + kl * C::ROW + lane * 8);
+                    v0 = bf16x2_to_float2(u.x);
+                    v1 = bf16x2_to_float2(u.y);
+                } else {
+                    const float4 f = *reinterpret_cast<const float4*>(Vs + kl * C::ROW + lane * 16);
+                    v0 = make_float2(f.x, f.y);
+                    v1 = make_float2(f.z, f.w);
+                }
 #pragma unroll
                 for (int r = 0; r < C::RB; ++r) {
-                    const float pr = fast_exp2(s[it][r] - mu[r]);
-                    lsum[r] += pr;
-                    const float2 pp2 = make_float2(pr, pr);
-#pragma unroll
-                    for (int e = 0; e < C::DPL / 2; ++e) o2[r][e] = __ffma2_rn(pp2, v2[e], o2[r][e]);
+                    const float2 pp2 = make_float2(pw[r], pw[r]);
+                    o4[r][0] = __ffma2_rn(pp2, v0, o4[r][0]);
+                    o4[r][1] = __ffma2_rn(pp2, v1, o4[r][1]);
                 }
             }
+            __syncwarp();
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(empty0 + 8 * stage);
 
         if (h.flags & kEnd) {
-            // groups of P lanes saw different keys: sum them (same m per warp)
+            // this warp's record: its dims of every row, and (m, l) per row
 #pragma unroll
-            for (int r = 0; r < C::RB; ++r) {
-#pragma unroll
-                for (int o = C::P; o < 32; o <<= 1) {
-                    lsum[r] += __shfl_xor_sync(0xffffffffu, lsum[r], o);
-#pragma unroll
-                    for (int e = 0; e < C::DPL / 2; ++e) {
-                        o2[r][e].x += __shfl_xor_sync(0xffffffffu, o2[r][e].x, o);
-                        o2[r][e].y += __shfl_xor_sync(0xffffffffu, o2[r][e].y, o);
-                    }
-                }
-            }
+            for (int o = C::P; o < 32; o <<= 1) l_mine += __shfl_xor_sync(0xffffffffu, l_mine, o);
             float* const mw = merge + warp * C::RB * C::MSTRIDE;
-            if (lane < C::P) {
 #pragma unroll
-                for (int r = 0; r < C::RB; ++r) {
-#pragma unroll
-                    for (int e = 0; e < C::DPL / 2; ++e) {
-                        mw[r * C::MSTRIDE + 2 + lane_dim<C>(li, 2 * e)] = o2[r][e].x;
-                        mw[r * C::MSTRIDE + 2 + lane_dim<C>(li, 2 * e + 1)] = o2[r][e].y;
-                    }
-                }
-            }
-            if (lane == 0) {
-#pragma unroll
-                for (int r = 0; r < C::RB; ++r) {
-                    mw[r * C::MSTRIDE] = mrow[r];
-                    mw[r * C::MSTRIDE + 1] = lsum[r];
-                }
+            for (int r = 0; r < C::RB; ++r)
+                *reinterpret_cast<float4*>(mw + r * C::MSTRIDE + 4 * lane) =
+                    make_float4(o4[r][0].x, o4[r][0].y, o4[r][1].x, o4[r][1].y);
+            if (lane < C::P && li % SPREAD == 0) {
+                mw[rho * C::MSTRIDE + kD] = m_mine;
+                mw[rho * C::MSTRIDE + kD + 1] = l_mine;
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(mfull);
@@ -592,27 +758,34 @@ __global__ void __launch_bounds__(C::THREADS, 1) decode_split_kernel(const Decod
                 (static_cast<long long>(h.b) * p.H_q + static_cast<long long>(h.kvh) * p.G) * p.L +
                 static_cast<long long>(h.chunk) * C::RB;
             const long long slot = h.slot;
-            for (int idx = tid; idx < C::RB * kD; idx += C::NCW * 32) {
-                const int r = idx / kD, d = idx - r * kD;
-                if (r >= rows_valid) continue;
+            // warp r merges row r (and r + NCW, ...), four dims per lane
+            for (int r = warp; r < rows_valid; r += C::NCW) {
                 float M = neg_inf();
 #pragma unroll
-                for (int w = 0; w < C::NCW; ++w) M = fmaxf(M, merge[(w * C::RB + r) * C::MSTRIDE]);
-                float den = 0.f, acc = 0.f;
+                for (int wq = 0; wq < C::NCW; ++wq)
+                    M = fmaxf(M, merge[(wq * C::RB + r) * C::MSTRIDE + kD]);
+                float den = 0.f;
+                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
                 if (M != neg_inf()) {
 #pragma unroll
-                    for (int w = 0; w < C::NCW; ++w) {
-                        const float* rec = merge + (w * C::RB + r) * C::MSTRIDE;
-                        const float a = fast_exp2(rec[0] - M);
-                        den += a * rec[1];
-                        acc += a * rec[2 + d];
+                    for (int wq = 0; wq < C::NCW; ++wq) {
+                        const float* rec = merge + (wq * C::RB + r) * C::MSTRIDE;
+                        const float a = fast_exp2(rec[kD] - M);
+                        den += a * rec[kD + 1];
+                        const float4 ov = *reinterpret_cast<const float4*>(rec + 4 * lane);
+                        acc.x += a * ov.x;
+                        acc.y += a * ov.y;
+                        acc.z += a * ov.z;
+                        acc.w += a * ov.w;
                     }
                 }
                 if (h.flags & kFinal) {
-                    store_elem<T>(out, (base_row + r) * kD + d, den > 0.f ? acc / den : 0.f);
+                    const float inv = den > 0.f ? 1.f / den : 0.f;
+                    store4<T>(out, (base_row + r) * kD + 4 * lane,
+                              make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv));
                 } else {
-                    p.part_o[(slot * C::RB + r) * kD + d] = acc;
-                    if (d == 0) p.part_ml[slot * C::RB + r] = make_float2(M, den);
+                    *reinterpret_cast<float4*>(p.part_o + (slot * C::RB + r) * kD + 4 * lane) = acc;
+                    if (lane == 0) p.part_ml[slot * C::RB + r] = make_float2(M, den);
                 }
             }
             __syncwarp();
@@ -626,19 +799,6 @@ __global__ void __launch_bounds__(C::THREADS, 1) decode_split_kernel(const Decod
         }
         if (h.flags & kLast) break;
     }
-}
-
-// Four output dims of one row, stored together.
-template <typename T>
-__device__ __forceinline__ void store4(T* base, long long idx, float4 v);
-template <>
-__device__ __forceinline__ void store4<__nv_bfloat16>(__nv_bfloat16* base, long long idx, float4 v) {
-    *reinterpret_cast<uint2*>(reinterpret_cast<uint16_t*>(base) + idx) =
-        make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
-}
-template <>
-__device__ __forceinline__ void store4<float>(float* base, long long idx, float4 v) {
-    *reinterpret_cast<float4*>(base + idx) = v;
 }
 
 // Merges the pieces of every segment that was split across CTAs (one CTA per
@@ -738,8 +898,9 @@ WsLayout ws_layout(const pa_shape& sh, int grid, int RB) {
 template <class C>
 pa_status launch_cfg(const Call& c) {
     const pa_shape& sh = c.sh;
-    const int grid = decode_grid(sh, c.dev.sm_count);
-    const WsLayout w = ws_layout(sh, grid, C::RB);
+    const int grid = c.dev.sm_count * C::MINB;
+    // the workspace is sized for the largest grid any configuration uses
+    const WsLayout w = ws_layout(sh, decode_grid(sh, c.dev.sm_count), C::RB);
     if (c.ws_bytes < w.total) return PA_ERR_WORKSPACE;
     // Bound on the flattened unit count: every index stays inside int.
     const long long max_units = w.nseg * ((static_cast<long long>(sh.max_pages_per_seq) *
@@ -779,6 +940,8 @@ pa_status launch_cfg(const Call& c) {
     p.causal = c.causal ? 1 : 0;
     p.max_S = static_cast<long long>(sh.max_pages_per_seq) * sh.page_size;
     p.scale_log2 = c.scale * 1.4426950408889634f;
+    p.tk_pages = C::TK / sh.page_size;
+    p.tk_slots = C::TK % sh.page_size;
 
     if (c.ev_before && cudaEventRecord(c.ev_before, c.stream) != cudaSuccess) return PA_ERR_CUDA;
     decode_split_kernel<C><<<grid, C::THREADS, C::SMEM, c.stream>>>(p);
@@ -809,6 +972,7 @@ int decode_rows_per_chunk(const pa_shape& sh) {
     return 8;
 }
 
+// Largest persistent grid of any decode configuration (one CTA per SM).
 int decode_grid(const pa_shape& /*sh*/, int sm_count) { return sm_count > 0 ? sm_count : 1; }
 
 size_t decode_workspace_bytes(const pa_shape& sh, int sm_count) {

@@ -7,25 +7,29 @@
 // sum -> P.V), whole K/V tiles past the causal frontier skipped, and the
 // normalised bf16 output written once.
 //
-// How it is laid out on GB300 (one CTA per 128-row query tile):
+// How it is laid out on GB300 (one CTA per pair of 128-row query tiles):
 //   * The 128 rows of a tile are Lt = 128/G consecutive positions l of all G
 //     query heads that share one kv head (GQA packing), so one K/V tile feeds
 //     128 rows and the causal frontier moves by only Lt keys across the tile.
-//   * Warp 0 stages tiles with 2-D TMA loads (128-byte swizzle): the query
-//     tile once (one box per head), then 128-key K and V tiles into a 2-stage
-//     ring.  Every box lies inside one page: box height = gcd(page_size, 128)
-//     rows, its row coordinate (physical_page * H_kv + kv_head) * page_size +
-//     slot comes from the block table, so a tile that crosses pages is just
-//     several boxes.
-//   * Warp 1 allocates 512 TMEM columns (S double-buffered at columns 0 and
-//     128, O at 256) and one thread issues tcgen05.mma: S = Q.K^T (M=N=128,
-//     K=16 steps over D), then O += P.V with V read MN-major from its
-//     natural [key][dim] layout.
-//   * Warps 2-5 (128 threads, one TMEM lane = one query row each) run the
-//     softmax: S row from TMEM, scale*log2(e), causal/length mask, running
-//     max moved only when it grows by more than 2^8 (then O is rescaled in
-//     TMEM), exp2, P rounded to bf16 into swizzled shared memory for the P.V
-//     MMA, running sum of those bf16 weights; at the end O/l -> bf16 -> global.
+//     A CTA owns two consecutive tiles, A and B, which share every K/V tile.
+//   * Warp 0 stages tiles with 2-D TMA loads (128-byte swizzle): both query
+//     tiles once (one box per head), then 128-key K tiles into a 2-slot ring
+//     and V tiles into one slot.  Every box lies inside one page: box height
+//     = gcd(page_size, 128) rows, its row coordinate (physical_page * H_kv +
+//     kv_head) * page_size + slot comes from the block table, so a tile that
+//     crosses pages is just several boxes.
+//   * Warp 1 allocates all 512 TMEM columns (S_A, S_B, O_A, O_B, 128 each)
+//     and one thread issues tcgen05.mma in the order PV_A(j), S_A(j+1),
+//     PV_B(j), S_B(j+1): while one softmax warpgroup works on its tile the
+//     tensor core runs the other tile's products.  S = Q.K^T uses K-major
+//     operands; O += P.V reads V MN-major from its natural [key][dim] layout.
+//   * Warps 4-7 (tile A) and 8-11 (tile B) run the softmax, one TMEM lane
+//     (query row) per thread: S row from TMEM, causal/length mask, row max of
+//     the raw scores, running max moved only when it grows by more than 2^8
+//     (then O is rescaled in TMEM), p = 2^(s*scale*log2 e - m) with one packed
+//     FMA and one exp2 per score, P rounded to bf16 into swizzled shared
+//     memory for the P.V MMA, running sum in fp32; at the end O/l -> bf16 ->
+//     global.  Whole K/V tiles past a tile's last causal frontier are skipped.
 //   * All waits are bounded; on a timeout the CTA records PA_FLAG_TIMEOUT,
 //     lets its copies and MMAs finish, frees TMEM and exits.
 #include <cuda.h>
@@ -43,29 +47,32 @@ namespace {
 constexpr int kD = kHeadDim;
 constexpr int BM = 128;  // query rows per tile
 constexpr int BN = 128;  // keys per K/V tile
-constexpr int kStages = 2;
-constexpr int kThreads = 192;
+constexpr int kThreads = 384;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS = 0, kColO = 256;
+// TMEM columns: S of tile t at 128 t, O of tile t at 256 + 128 t
+__host__ __device__ constexpr uint32_t col_s(int t) { return 128u * static_cast<uint32_t>(t); }
+__host__ __device__ constexpr uint32_t col_o(int t) { return 256u + 128u * static_cast<uint32_t>(t); }
 constexpr float kLazyRescaleLog2 = 8.0f;
 
 // shared memory map (offsets from a 1024-byte aligned base)
-constexpr int kHalf = BM * 128;  // 128 rows x 64 bf16 (one 128-byte swizzle column block)
-constexpr int kTile = 2 * kHalf; // 128 rows x 128 bf16
-constexpr int kOffQ = 0;
-constexpr int kOffKV = kOffQ + kTile;  // stage s: K at kOffKV + 2*s*kTile, V after it
-constexpr int kOffP = kOffKV + kStages * 2 * kTile;
-constexpr int kOffBar = kOffP + kTile;
+constexpr int kHalf = BM * 128;   // 128 rows x 64 bf16 (one 128-byte swizzle column block)
+constexpr int kTile = 2 * kHalf;  // 128 rows x 128 bf16
+constexpr int kOffQ = 0;                    // tile t at kOffQ + t * kTile
+constexpr int kOffK = kOffQ + 2 * kTile;    // slot s at kOffK + s * kTile
+constexpr int kOffV = kOffK + 2 * kTile;
+constexpr int kOffP = kOffV + kTile;        // tile t at kOffP + t * kTile
+constexpr int kOffBar = kOffP + 2 * kTile;
 enum Bar {
     kQFull = 0,
-    kKVFull = 1,   // + stage
-    kKVEmpty = 3,  // + stage
-    kSFull = 5,    // + buffer
-    kSFree = 7,    // + buffer
-    kPFull = 9,
-    kODone = 10,
-    kMmaDone = 11,
-    kNumBars = 12
+    kKFull = 1,   // + slot
+    kKEmpty = 3,  // + slot
+    kVFull = 5,
+    kVEmpty = 6,
+    kSFull = 7,   // + tile
+    kPFull = 9,   // + tile
+    kODone = 11,  // + tile
+    kMmaDone = 13,
+    kNumBars = 14
 };
 constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
 constexpr int kOffAbort = kOffTmemSlot + 8;
@@ -77,7 +84,7 @@ struct PrefillParams {
     const int32_t* ctx;
     void* out;
     uint32_t* flag;
-    int B, H_q, H_kv, L, G, Lt, nM, num_pages, ps, max_npg, box_rows, causal;
+    int B, H_q, H_kv, L, G, Lt, nM, nPairs, num_pages, ps, max_npg, box_rows, causal;
     long long max_S;
     float scale_log2;
 };
@@ -101,6 +108,43 @@ __device__ __forceinline__ void give_up(const PrefillParams& p, volatile int* ab
     atomicOr(p.flag, PA_FLAG_TIMEOUT);
 }
 
+// The block-table row coordinates of the boxes of K/V tile j (lane i: box i
+// and i + 32 ...); -1 for boxes past the context or with a bad page id.
+__device__ __forceinline__ void tile_boxes(const PrefillParams& p, int b, int kvh, int S, int j,
+                                           int lane, int (&row)[4], uint32_t& bytes) {
+    const int nbox = BN / p.box_rows;
+    bytes = 0;
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+        const int bi = lane + 32 * w;
+        row[w] = -1;
+        const int key = j * BN + bi * p.box_rows;
+        if (bi < nbox && key < S) {
+            const int lp = key / p.ps, slot = key - lp * p.ps;
+            const int pp = __ldg(p.bt + static_cast<long long>(b) * p.max_npg + lp);
+            if (pp >= 0 && pp < p.num_pages) {
+                row[w] = (pp * p.H_kv + kvh) * p.ps + slot;
+                bytes += 2u * static_cast<uint32_t>(p.box_rows) * 128u;  // two 64-dim halves
+            } else {
+                atomicOr(p.flag, PA_FLAG_BAD_PAGE);
+            }
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) bytes += __shfl_xor_sync(0xffffffffu, bytes, o);
+}
+
+__device__ __forceinline__ void issue_boxes(const CUtensorMap* map, uint32_t dst, const int (&row)[4],
+                                            int lane, int box_rows, uint32_t bar, uint64_t pol) {
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+        if (row[w] < 0) continue;
+        const uint32_t off = static_cast<uint32_t>(lane + 32 * w) * box_rows * 128u;
+        tc::tma_load_2d(dst + off, map, 0, row[w], bar, pol);
+        tc::tma_load_2d(dst + kHalf + off, map, 64, row[w], bar, pol);
+    }
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tile_kernel(const __grid_constant__ CUtensorMap tm_q,
                         const __grid_constant__ CUtensorMap tm_k,
@@ -116,39 +160,48 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
-    // ---- which tile ---------------------------------------------------------
+    // ---- which tiles ----------------------------------------------------------
     const int per_m = p.H_kv * p.B;
-    const int m = p.nM - 1 - static_cast<int>(blockIdx.x) / per_m;  // heavy tiles first
+    const int mp = p.nPairs - 1 - static_cast<int>(blockIdx.x) / per_m;  // heavy pairs first
     const int rest = static_cast<int>(blockIdx.x) % per_m;
     const int b = rest / p.H_kv, kvh = rest % p.H_kv;
-    const int l0 = m * p.Lt;
     const int S = p.ctx[b];
     const bool valid_seq =
         S >= 1 && static_cast<long long>(S) <= p.max_S && !(p.causal && S < p.L);
-    const int l_last = min(l0 + p.Lt, p.L) - 1;
-    const int lim_max = p.causal ? l_last + S - p.L : S - 1;  // last key any row sees
-    const int lim_min = p.causal ? l0 + S - p.L : S - 1;      // last key row l0 sees
-    const int nk = valid_seq ? lim_max / BN + 1 : 0;
+    int nk_t[2], lim_min_t[2], l0_t[2];
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+        const int m = 2 * mp + t;
+        l0_t[t] = m * p.Lt;
+        const bool exists = m < p.nM && valid_seq;
+        const int l_last = min(l0_t[t] + p.Lt, p.L) - 1;
+        const int lim_max = p.causal ? l_last + S - p.L : S - 1;  // last key any row sees
+        lim_min_t[t] = p.causal ? l0_t[t] + S - p.L : S - 1;      // last key row l0 sees
+        nk_t[t] = exists ? lim_max / BN + 1 : 0;
+    }
+    const int nk = max(nk_t[0], nk_t[1]);
+    const int ntiles = (2 * mp + 1 < p.nM) ? 2 : 1;
 
-    // ---- set-up: barriers, V stages zeroed, TMEM ---------------------------
+    // ---- set-up: barriers, V zeroed, TMEM --------------------------------------
     if (tid == 0) {
         mbar_init(bar(kQFull), 1);
-        for (int s = 0; s < kStages; ++s) {
-            mbar_init(bar(kKVFull + s), 1);
-            mbar_init(bar(kKVEmpty + s), 1);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(bar(kKFull + s), 1);
+            mbar_init(bar(kKEmpty + s), 1);
             mbar_init(bar(kSFull + s), 1);
-            mbar_init(bar(kSFree + s), 4);
+            mbar_init(bar(kPFull + s), 4);
+            mbar_init(bar(kODone + s), 1);
         }
-        mbar_init(bar(kPFull), 4);
-        mbar_init(bar(kODone), 1);
+        mbar_init(bar(kVFull), 1);
+        mbar_init(bar(kVEmpty), 1);
         mbar_init(bar(kMmaDone), 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
     // key rows that are never loaded must hold finite values (their weight is
     // exactly 0, and 0 * NaN would not be)
-    for (int s = 0; s < kStages; ++s) {
-        uint4* v = reinterpret_cast<uint4*>(sbase + kOffKV + (2 * s + 1) * kTile);
+    {
+        uint4* v = reinterpret_cast<uint4*>(sbase + kOffV);
         for (int i = tid; i < kTile / 16; i += kThreads) v[i] = make_uint4(0u, 0u, 0u, 0u);
     }
     fence_proxy_async_smem();
@@ -170,105 +223,120 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc::prefetch_tensormap(&tm_q);
             tc::prefetch_tensormap(&tm_k);
             tc::prefetch_tensormap(&tm_v);
-            // query tile: one box of Lt rows per head, both 64-dim halves
-            mbar_arrive_expect_tx(bar(kQFull), static_cast<uint32_t>(p.G * p.Lt * 128 * 2));
-            for (int g = 0; g < p.G; ++g) {
-                const int row = ((b * p.H_q) + kvh * p.G + g) * p.L + l0;
-                for (int h = 0; h < 2; ++h)
-                    tc::tma_load_2d(base + kOffQ + h * kHalf + g * p.Lt * 128, &tm_q, h * 64, row,
-                                    bar(kQFull), pol_q);
-            }
+            mbar_arrive_expect_tx(bar(kQFull),
+                                  static_cast<uint32_t>(ntiles * p.G * p.Lt * 128 * 2));
+            for (int t = 0; t < ntiles; ++t)
+                for (int g = 0; g < p.G; ++g) {
+                    const int row = ((b * p.H_q) + kvh * p.G + g) * p.L + l0_t[t];
+                    for (int h = 0; h < 2; ++h)
+                        tc::tma_load_2d(base + kOffQ + t * kTile + h * kHalf + g * p.Lt * 128,
+                                        &tm_q, h * 64, row, bar(kQFull), pol_q);
+                }
         }
         __syncwarp();
-        const int nbox = BN / p.box_rows;  // boxes per K/V tile (<= 128)
-        const uint32_t box_bytes = static_cast<uint32_t>(p.box_rows) * 128u;
-        int issued = 0;
+        int rows_cur[4], rows_next[4];
+        uint32_t bytes_cur, bytes_next;
+        tile_boxes(p, b, kvh, S, 0, lane, rows_cur, bytes_cur);
+        // K(0)
+        if (lane == 0) mbar_arrive_expect_tx(bar(kKFull), bytes_cur);
+        __syncwarp();
+        issue_boxes(&tm_k, base + kOffK, rows_cur, lane, p.box_rows, bar(kKFull), pol_kv);
+        int kissued = 1, vissued = 0;
         for (int j = 0; j < nk; ++j) {
-            const int s = j & 1;
-            if (j >= kStages && !warp_wait(bar(kKVEmpty + s), ((j >> 1) - 1) & 1)) {
+            // K(j+1) into slot (j+1)&1, once S(j-1) no longer needs it
+            if (j + 1 < nk) {
+                tile_boxes(p, b, kvh, S, j + 1, lane, rows_next, bytes_next);
+                const int t = j + 1, s = t & 1;
+                if (t >= 2 && !warp_wait(bar(kKEmpty + s), ((t >> 1) - 1) & 1)) {
+                    if (lane == 0) give_up(p, abort_flag);
+                    break;
+                }
+                if (aborted(abort_flag)) break;
+                if (lane == 0) mbar_arrive_expect_tx(bar(kKFull + s), bytes_next);
+                __syncwarp();
+                issue_boxes(&tm_k, base + kOffK + s * kTile, rows_next, lane, p.box_rows,
+                            bar(kKFull + s), pol_kv);
+                kissued = t + 1;
+            }
+            // V(j) once both P.V of tile j-1 are done
+            if (j >= 1 && !warp_wait(bar(kVEmpty), (j - 1) & 1)) {
                 if (lane == 0) give_up(p, abort_flag);
                 break;
             }
             if (aborted(abort_flag)) break;
-            int prow[4];
-            uint32_t bytes = 0;
-#pragma unroll
-            for (int w = 0; w < 4; ++w) {
-                const int bi = lane + 32 * w;
-                prow[w] = -1;
-                const int key = j * BN + bi * p.box_rows;
-                if (bi < nbox && key < S) {
-                    const int lp = key / p.ps, slot = key - lp * p.ps;
-                    const int pp = __ldg(p.bt + static_cast<long long>(b) * p.max_npg + lp);
-                    if (pp >= 0 && pp < p.num_pages) {
-                        prow[w] = (pp * p.H_kv + kvh) * p.ps + slot;
-                        bytes += 4u * box_bytes;  // K and V, two halves each
-                    } else {
-                        atomicOr(p.flag, PA_FLAG_BAD_PAGE);
-                    }
-                }
-            }
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) bytes += __shfl_xor_sync(0xffffffffu, bytes, o);
-            if (lane == 0) mbar_arrive_expect_tx(bar(kKVFull + s), bytes);
+            if (lane == 0) mbar_arrive_expect_tx(bar(kVFull), bytes_cur);
             __syncwarp();
-            const uint32_t kdst = base + kOffKV + 2 * s * kTile;
-            const uint32_t vdst = kdst + kTile;
+            issue_boxes(&tm_v, base + kOffV, rows_cur, lane, p.box_rows, bar(kVFull), pol_kv);
+            vissued = j + 1;
 #pragma unroll
-            for (int w = 0; w < 4; ++w) {
-                if (prow[w] < 0) continue;
-                const uint32_t off = static_cast<uint32_t>(lane + 32 * w) * box_bytes;
-                for (int h = 0; h < 2; ++h) {
-                    tc::tma_load_2d(kdst + h * kHalf + off, &tm_k, h * 64, prow[w],
-                                    bar(kKVFull + s), pol_kv);
-                    tc::tma_load_2d(vdst + h * kHalf + off, &tm_v, h * 64, prow[w],
-                                    bar(kKVFull + s), pol_kv);
-                }
-            }
-            issued = j + 1;
+            for (int w = 0; w < 4; ++w) rows_cur[w] = rows_next[w];
+            bytes_cur = bytes_next;
         }
         // let every copy into this CTA's shared memory land before leaving
         if (!mbar_wait(bar(kQFull), 0)) give_up(p, abort_flag);
-        for (int j = max(0, issued - kStages); j < issued; ++j)
-            if (!mbar_wait(bar(kKVFull + (j & 1)), (j >> 1) & 1)) give_up(p, abort_flag);
+        for (int t = max(0, kissued - 2); t < kissued; ++t)
+            if (!mbar_wait(bar(kKFull + (t & 1)), (t >> 1) & 1)) give_up(p, abort_flag);
+        if (vissued > 0 && !mbar_wait(bar(kVFull), (vissued - 1) & 1)) give_up(p, abort_flag);
     } else if (warp == 1 && nk > 0) {
         // ============================ MMA issuer =============================
         if (lane == 0) {
-            constexpr uint32_t idS = tc::idesc_bf16(BM, BN, 0, 0);   // Q, K both K-major
-            constexpr uint32_t idO = tc::idesc_bf16(BM, kD, 0, 1);   // P K-major, V MN-major
-            bool ok = mbar_wait(bar(kQFull), 0);
-            for (int j = 0; ok && j <= nk; ++j) {
-                if (j < nk) {
-                    const int s = j & 1;
-                    ok = mbar_wait(bar(kKVFull + s), (j >> 1) & 1) &&
-                         (j < kStages || mbar_wait(bar(kSFree + s), ((j >> 1) - 1) & 1));
-                    if (!ok || *abort_flag) break;
-                    tc::fence_after_sync();
-                    const uint32_t kaddr = base + kOffKV + 2 * s * kTile;
+            constexpr uint32_t idS = tc::idesc_bf16(BM, BN, 0, 0);  // Q, K both K-major
+            constexpr uint32_t idO = tc::idesc_bf16(BM, kD, 0, 1);  // P K-major, V MN-major
+            auto qk = [&](int t, int j) {
+                const uint32_t kaddr = base + kOffK + (j & 1) * kTile;
+                const uint32_t qaddr = base + kOffQ + t * kTile;
 #pragma unroll
-                    for (int kk = 0; kk < kD / 16; ++kk) {
-                        const uint32_t koff = (kk >> 2) * kHalf + (kk & 3) * 32;
-                        tc::mma_bf16(tmem + kColS + s * BN,
-                                     tc::smem_desc_sw128(base + kOffQ + koff, 16, 1024),
-                                     tc::smem_desc_sw128(kaddr + koff, 16, 1024), idS, kk > 0);
-                    }
-                    tc::commit(bar(kSFull + s));
+                for (int kk = 0; kk < kD / 16; ++kk) {
+                    const uint32_t koff = (kk >> 2) * kHalf + (kk & 3) * 32;
+                    tc::mma_bf16(tmem + col_s(t), tc::smem_desc_sw128(qaddr + koff, 16, 1024),
+                                 tc::smem_desc_sw128(kaddr + koff, 16, 1024), idS, kk > 0);
                 }
-                if (j >= 1) {
-                    const int jp = j - 1, sp = jp & 1;
-                    ok = mbar_wait(bar(kPFull), jp & 1);
+                tc::commit(bar(kSFull + t));
+            };
+            auto pv = [&](int t, int j) {
+                const uint32_t paddr = base + kOffP + t * kTile;
+#pragma unroll
+                for (int kk = 0; kk < BN / 16; ++kk) {
+                    const uint32_t poff = (kk >> 2) * kHalf + (kk & 3) * 32;
+                    tc::mma_bf16(tmem + col_o(t), tc::smem_desc_sw128(paddr + poff, 16, 1024),
+                                 tc::smem_desc_sw128(base + kOffV + kk * 16 * 128, kHalf, 1024),
+                                 idO, (j > 0 || kk > 0) ? 1u : 0u);
+                }
+                tc::commit(bar(kODone + t));
+            };
+            bool ok = mbar_wait(bar(kQFull), 0) && mbar_wait(bar(kKFull), 0);
+            if (ok) {
+                tc::fence_after_sync();
+                if (nk_t[0] > 0) qk(0, 0);
+                if (nk_t[1] > 0) qk(1, 0);
+                tc::commit(bar(kKEmpty));
+            }
+            for (int j = 0; ok && j < nk; ++j) {
+                ok = mbar_wait(bar(kVFull), j & 1);
+                if (!ok || *abort_flag) break;
+                const bool more = j + 1 < nk;
+                if (j < nk_t[0]) {
+                    ok = mbar_wait(bar(kPFull), j & 1);
                     if (!ok || *abort_flag) break;
                     tc::fence_after_sync();
-                    const uint32_t vaddr = base + kOffKV + (2 * sp + 1) * kTile;
-#pragma unroll
-                    for (int kk = 0; kk < BN / 16; ++kk) {
-                        const uint32_t poff = (kk >> 2) * kHalf + (kk & 3) * 32;
-                        tc::mma_bf16(tmem + kColO, tc::smem_desc_sw128(base + kOffP + poff, 16, 1024),
-                                     tc::smem_desc_sw128(vaddr + kk * 16 * 128, kHalf, 1024), idO,
-                                     (jp > 0 || kk > 0) ? 1u : 0u);
-                    }
-                    tc::commit(bar(kODone));
-                    tc::commit(bar(kKVEmpty + sp));
+                    pv(0, j);
+                }
+                if (more) {
+                    ok = mbar_wait(bar(kKFull + ((j + 1) & 1)), ((j + 1) >> 1) & 1);
+                    if (!ok || *abort_flag) break;
+                    tc::fence_after_sync();
+                    if (j + 1 < nk_t[0]) qk(0, j + 1);
+                }
+                if (j < nk_t[1]) {
+                    ok = mbar_wait(bar(kPFull + 1), j & 1);
+                    if (!ok || *abort_flag) break;
+                    tc::fence_after_sync();
+                    pv(1, j);
+                }
+                tc::commit(bar(kVEmpty));
+                if (more) {
+                    if (j + 1 < nk_t[1]) qk(1, j + 1);
+                    tc::commit(bar(kKEmpty + ((j + 1) & 1)));
                 }
             }
             if (!ok) give_up(p, abort_flag);
@@ -277,102 +345,104 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!mbar_wait(bar(kMmaDone), 0)) give_up(p, abort_flag);
         }
         __syncwarp();
-    } else if (warp >= 2) {
+    } else if (warp >= 4) {
         // ============================= softmax ===============================
+        const int t = (warp - 4) >> 2;      // tile of this warpgroup
         const int q4 = warp & 3;            // TMEM lane quarter of this warp
         const int r = q4 * 32 + lane;       // query row of this thread
         const uint32_t trow = tmem + (static_cast<uint32_t>(q4 * 32) << 16);
-        const int g = r / p.Lt, l = l0 + (r - g * p.Lt);
-        const bool row_valid = g < p.G && l < p.L;
+        const int g = r / p.Lt, l = l0_t[t] + (r - g * p.Lt);
+        const bool row_valid = t < ntiles && g < p.G && l < p.L;
         const int h = kvh * p.G + g;
         const int lim = min(p.causal ? l + S - p.L : S - 1, S - 1);
-        float mrow = neg_inf(), lsum = 0.f;
+        const int nkt = nk_t[t];
+        const float c = p.scale_log2;
+        float mrow = neg_inf();
+        float2 lsum2 = make_float2(0.f, 0.f);
         bool ok = true;
-        for (int j = 0; j < nk; ++j) {
-            const int s = j & 1;
-            ok = warp_wait(bar(kSFull + s), (j >> 1) & 1);
+        for (int j = 0; j < nkt; ++j) {
+            ok = warp_wait(bar(kSFull + t), j & 1);
             if (!ok || aborted(abort_flag)) break;
             tc::fence_after_sync();
             float x[4][32];
 #pragma unroll
-            for (int c = 0; c < 4; ++c) tc::ld32(trow + kColS + s * BN + c * 32, x[c]);
+            for (int cc = 0; cc < 4; ++cc) tc::ld32(trow + col_s(t) + cc * 32, x[cc]);
             tc::wait_ld();
-            tc::fence_before_sync();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar(kSFree + s));
-            // scale, mask, row max of this tile
-            const bool masking = j * BN + BN - 1 > lim_min;
-            const int cmax = lim - j * BN;  // columns c <= cmax are visible
+            // causal / length mask (frontier tiles only), row max of raw scores
+            const bool masking = j * BN + BN - 1 > lim_min_t[t];
+            const int cmax = lim - j * BN;  // columns <= cmax are visible
             float mt = neg_inf();
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
+            for (int cc = 0; cc < 4; ++cc) {
 #pragma unroll
                 for (int e = 0; e < 32; ++e) {
-                    float v = x[c][e] * p.scale_log2;
-                    if (masking && c * 32 + e > cmax) v = neg_inf();
-                    x[c][e] = v;
-                    mt = fmaxf(mt, v);
+                    if (masking && cc * 32 + e > cmax) x[cc][e] = neg_inf();
+                    mt = fmaxf(mt, x[cc][e]);
                 }
             }
+            mt *= c;
             const bool grow = mt > mrow + kLazyRescaleLog2;
             // P.V of the previous tile must be done before O or P are touched
             if (j > 0) {
-                ok = warp_wait(bar(kODone), (j - 1) & 1);
+                ok = warp_wait(bar(kODone + t), (j - 1) & 1);
                 if (!ok || aborted(abort_flag)) break;
                 tc::fence_after_sync();
             }
             if (__any_sync(0xffffffffu, grow)) {
                 const float mn = grow ? mt : mrow;
-                const float alpha = grow ? fast_exp2(mrow - mn) : 1.f;  // 2^-inf = 0 at the start
+                const float alpha = grow ? fast_exp2(mrow - mn) : 1.f;  // 2^-inf = 0 at start
                 if (j > 0) {
 #pragma unroll 1
-                    for (int c = 0; c < 4; ++c) {
+                    for (int cc = 0; cc < 4; ++cc) {
                         float o[32];
-                        tc::ld32(trow + kColO + c * 32, o);
+                        tc::ld32(trow + col_o(t) + cc * 32, o);
                         tc::wait_ld();
 #pragma unroll
                         for (int e = 0; e < 32; ++e) o[e] *= alpha;
-                        tc::st32(trow + kColO + c * 32, o);
+                        tc::st32(trow + col_o(t) + cc * 32, o);
                     }
                     tc::wait_st();
                 }
-                lsum *= alpha;
+                lsum2.x *= alpha;
+                lsum2.y *= alpha;
                 mrow = mn;
             }
             const float mu = (mrow == neg_inf()) ? 0.f : mrow;
-            uint8_t* const prow = sbase + kOffP + r * 128;
+            const float2 c2 = make_float2(c, c), nm2 = make_float2(-mu, -mu);
+            uint8_t* const prow = sbase + kOffP + t * kTile + r * 128;
 #pragma unroll
             for (int q = 0; q < 16; ++q) {  // 8 keys per 16-byte chunk
-                const int c = q >> 2, e0 = (q & 3) * 8;
+                const int cc = q >> 2, e0 = (q & 3) * 8;
                 float pv[8];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) pv[e] = fast_exp2(x[c][e0 + e] - mu);
+                for (int e = 0; e < 8; e += 2) {
+                    const float2 y = __ffma2_rn(make_float2(x[cc][e0 + e], x[cc][e0 + e + 1]), c2, nm2);
+                    pv[e] = fast_exp2(y.x);
+                    pv[e + 1] = fast_exp2(y.y);
+                    lsum2 = __fadd2_rn(lsum2, make_float2(pv[e], pv[e + 1]));
+                }
                 const uint4 w = make_uint4(pack_bf16x2(pv[0], pv[1]), pack_bf16x2(pv[2], pv[3]),
                                            pack_bf16x2(pv[4], pv[5]), pack_bf16x2(pv[6], pv[7]));
-                // the running sum adds the bf16 weights the tensor core multiplies,
-                // so the final division normalises exactly those weights
-                const float2 s0 = bf16x2_to_float2(w.x), s1 = bf16x2_to_float2(w.y);
-                const float2 s2 = bf16x2_to_float2(w.z), s3 = bf16x2_to_float2(w.w);
-                lsum += ((s0.x + s0.y) + (s1.x + s1.y)) + ((s2.x + s2.y) + (s3.x + s3.y));
                 const int half = q >> 3, cq = q & 7;
                 *reinterpret_cast<uint4*>(prow + half * kHalf + ((cq ^ (r & 7)) << 4)) = w;
             }
             fence_proxy_async_smem();
             tc::fence_before_sync();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar(kPFull));
+            if (lane == 0) mbar_arrive(bar(kPFull + t));
         }
+        const float lsum = lsum2.x + lsum2.y;
         if (!ok) {
             if (lane == 0) give_up(p, abort_flag);
-        } else if (nk > 0 && warp_wait(bar(kODone), (nk - 1) & 1)) {
+        } else if (nkt > 0 && warp_wait(bar(kODone + t), (nkt - 1) & 1)) {
             tc::fence_after_sync();
             const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
             uint16_t* const orow = static_cast<uint16_t*>(p.out) +
                                    ((static_cast<long long>(b) * p.H_q + h) * p.L + l) * kD;
 #pragma unroll 1
-            for (int c = 0; c < 4; ++c) {
+            for (int cc = 0; cc < 4; ++cc) {
                 float o[32];
-                tc::ld32(trow + kColO + c * 32, o);
+                tc::ld32(trow + col_o(t) + cc * 32, o);
                 tc::wait_ld();
                 if (row_valid) {
 #pragma unroll
@@ -382,11 +452,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                             pack_bf16x2(o[q * 8 + 2] * inv, o[q * 8 + 3] * inv),
                             pack_bf16x2(o[q * 8 + 4] * inv, o[q * 8 + 5] * inv),
                             pack_bf16x2(o[q * 8 + 6] * inv, o[q * 8 + 7] * inv));
-                        *reinterpret_cast<uint4*>(orow + c * 32 + q * 8) = w;
+                        *reinterpret_cast<uint4*>(orow + cc * 32 + q * 8) = w;
                     }
                 }
             }
-        } else if (nk > 0) {
+        } else if (nkt > 0) {
             if (lane == 0) give_up(p, abort_flag);
         }
         if (!valid_seq && row_valid) {
@@ -497,6 +567,7 @@ pa_status prefill_launch(const Call& c) {
     p.G = G;
     p.Lt = Lt;
     p.nM = (sh.L + Lt - 1) / Lt;
+    p.nPairs = (p.nM + 1) / 2;
     p.num_pages = sh.num_pages;
     p.ps = sh.page_size;
     p.max_npg = sh.max_pages_per_seq;
@@ -504,7 +575,7 @@ pa_status prefill_launch(const Call& c) {
     p.causal = c.causal ? 1 : 0;
     p.max_S = static_cast<long long>(sh.max_pages_per_seq) * sh.page_size;
     p.scale_log2 = c.scale * 1.4426950408889634f;
-    const unsigned grid = static_cast<unsigned>(static_cast<long long>(p.nM) * sh.H_kv * sh.B);
+    const unsigned grid = static_cast<unsigned>(static_cast<long long>(p.nPairs) * sh.H_kv * sh.B);
     if (c.ev_before && cudaEventRecord(c.ev_before, c.stream) != cudaSuccess) return PA_ERR_CUDA;
     prefill_tile_kernel<<<grid, kThreads, kSmemBytes, c.stream>>>(tq, tk, tv, p);
     if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;

@@ -13,8 +13,8 @@
 //     128 rows and the causal frontier moves by only Lt keys across the tile.
 //     A CTA owns two consecutive tiles, A and B, which share every K/V tile.
 //   * Warp 0 stages tiles with 2-D TMA loads (128-byte swizzle): both query
-//     tiles once (one box per head), then 128-key K tiles into a 2-slot ring
-//     and V tiles into one slot.  Every box lies inside one page: box height
+//     tiles once (one box per head), then 128-key K and V tiles into 2-slot
+//     rings.  Every box lies inside one page: box height
 //     = gcd(page_size, 128) rows, its row coordinate (physical_page * H_kv +
 //     kv_head) * page_size + slot comes from the block table, so a tile that
 //     crosses pages is just several boxes.
@@ -28,8 +28,9 @@
 //     the raw scores, running max moved only when it grows by more than 2^8
 //     (then O is rescaled in TMEM), p = 2^(s*scale*log2 e - m) with one packed
 //     FMA and one exp2 per score, P rounded to bf16 into swizzled shared
-//     memory for the P.V MMA, running sum in fp32; at the end O/l -> bf16 ->
-//     global.  Whole K/V tiles past a tile's last causal frontier are skipped.
+//     memory for the P.V MMA (one buffer, written by A and B in turn), running
+//     sum in fp32; at the end O/l -> bf16 -> global.  Whole K/V tiles past a
+//     tile's last causal frontier are skipped.
 //   * All waits are bounded; on a timeout the CTA records PA_FLAG_TIMEOUT,
 //     lets its copies and MMAs finish, frees TMEM and exits.
 #include <cuda.h>
@@ -59,20 +60,20 @@ constexpr int kHalf = BM * 128;   // 128 rows x 64 bf16 (one 128-byte swizzle co
 constexpr int kTile = 2 * kHalf;  // 128 rows x 128 bf16
 constexpr int kOffQ = 0;                    // tile t at kOffQ + t * kTile
 constexpr int kOffK = kOffQ + 2 * kTile;    // slot s at kOffK + s * kTile
-constexpr int kOffV = kOffK + 2 * kTile;
-constexpr int kOffP = kOffV + kTile;        // tile t at kOffP + t * kTile
-constexpr int kOffBar = kOffP + 2 * kTile;
+constexpr int kOffV = kOffK + 2 * kTile;    // slot s at kOffV + s * kTile
+constexpr int kOffP = kOffV + 2 * kTile;    // one P buffer, used by A and B in turn
+constexpr int kOffBar = kOffP + kTile;
 enum Bar {
     kQFull = 0,
     kKFull = 1,   // + slot
     kKEmpty = 3,  // + slot
-    kVFull = 5,
-    kVEmpty = 6,
-    kSFull = 7,   // + tile
-    kPFull = 9,   // + tile
-    kODone = 11,  // + tile
-    kMmaDone = 13,
-    kNumBars = 14
+    kVFull = 5,   // + slot
+    kVEmpty = 7,  // + slot
+    kSFull = 9,   // + tile
+    kPFull = 11,  // + tile
+    kODone = 13,  // + tile
+    kMmaDone = 15,
+    kNumBars = 16
 };
 constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
 constexpr int kOffAbort = kOffTmemSlot + 8;
@@ -145,6 +146,20 @@ __device__ __forceinline__ void issue_boxes(const CUtensorMap* map, uint32_t dst
     }
 }
 
+// p = 2^(s * c - m) for one 128-key row: packed to bf16 pairs in pw, summed
+// in fp32 into ts.
+__device__ __forceinline__ void exp_pack(const float (&x)[4][32], float2 c2, float2 nm2,
+                                         uint32_t (&pw)[64], float2& ts) {
+#pragma unroll
+    for (int k = 0; k < 64; ++k) {
+        const int cc = k >> 4, e = (k & 15) * 2;
+        const float2 y = __ffma2_rn(make_float2(x[cc][e], x[cc][e + 1]), c2, nm2);
+        const float2 pp = make_float2(fast_exp2(y.x), fast_exp2(y.y));
+        ts = __fadd2_rn(ts, pp);
+        pw[k] = pack_bf16x2(pp.x, pp.y);
+    }
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tile_kernel(const __grid_constant__ CUtensorMap tm_q,
                         const __grid_constant__ CUtensorMap tm_k,
@@ -192,8 +207,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(bar(kPFull + s), 4);
             mbar_init(bar(kODone + s), 1);
         }
-        mbar_init(bar(kVFull), 1);
-        mbar_init(bar(kVEmpty), 1);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(bar(kVFull + s), 1);
+            mbar_init(bar(kVEmpty + s), 1);
+        }
         mbar_init(bar(kMmaDone), 1);
         *abort_flag = 0;
         fence_mbar_init();
@@ -202,7 +219,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // exactly 0, and 0 * NaN would not be)
     {
         uint4* v = reinterpret_cast<uint4*>(sbase + kOffV);
-        for (int i = tid; i < kTile / 16; i += kThreads) v[i] = make_uint4(0u, 0u, 0u, 0u);
+        for (int i = tid; i < 2 * kTile / 16; i += kThreads) v[i] = make_uint4(0u, 0u, 0u, 0u);
     }
     fence_proxy_async_smem();
     if (warp == 1) {
@@ -237,46 +254,41 @@ __global__ void __launch_bounds__(kThreads, 1)
         int rows_cur[4], rows_next[4];
         uint32_t bytes_cur, bytes_next;
         tile_boxes(p, b, kvh, S, 0, lane, rows_cur, bytes_cur);
-        // K(0)
-        if (lane == 0) mbar_arrive_expect_tx(bar(kKFull), bytes_cur);
-        __syncwarp();
-        issue_boxes(&tm_k, base + kOffK, rows_cur, lane, p.box_rows, bar(kKFull), pol_kv);
-        int kissued = 1, vissued = 0;
-        for (int j = 0; j < nk; ++j) {
-            // K(j+1) into slot (j+1)&1, once S(j-1) no longer needs it
-            if (j + 1 < nk) {
-                tile_boxes(p, b, kvh, S, j + 1, lane, rows_next, bytes_next);
-                const int t = j + 1, s = t & 1;
-                if (t >= 2 && !warp_wait(bar(kKEmpty + s), ((t >> 1) - 1) & 1)) {
-                    if (lane == 0) give_up(p, abort_flag);
-                    break;
-                }
-                if (aborted(abort_flag)) break;
-                if (lane == 0) mbar_arrive_expect_tx(bar(kKFull + s), bytes_next);
-                __syncwarp();
-                issue_boxes(&tm_k, base + kOffK + s * kTile, rows_next, lane, p.box_rows,
-                            bar(kKFull + s), pol_kv);
-                kissued = t + 1;
-            }
-            // V(j) once both P.V of tile j-1 are done
-            if (j >= 1 && !warp_wait(bar(kVEmpty), (j - 1) & 1)) {
+        int issued = 0;
+        for (int t = 0; t < nk; ++t) {
+            // rows of the next tile requested before waiting for a free slot
+            if (t + 1 < nk) tile_boxes(p, b, kvh, S, t + 1, lane, rows_next, bytes_next);
+            const int s = t & 1;
+            if (t >= 2 && !warp_wait(bar(kKEmpty + s), ((t >> 1) - 1) & 1)) {
                 if (lane == 0) give_up(p, abort_flag);
                 break;
             }
             if (aborted(abort_flag)) break;
-            if (lane == 0) mbar_arrive_expect_tx(bar(kVFull), bytes_cur);
+            if (lane == 0) mbar_arrive_expect_tx(bar(kKFull + s), bytes_cur);
             __syncwarp();
-            issue_boxes(&tm_v, base + kOffV, rows_cur, lane, p.box_rows, bar(kVFull), pol_kv);
-            vissued = j + 1;
+            issue_boxes(&tm_k, base + kOffK + s * kTile, rows_cur, lane, p.box_rows,
+                        bar(kKFull + s), pol_kv);
+            if (t >= 2 && !warp_wait(bar(kVEmpty + s), ((t >> 1) - 1) & 1)) {
+                if (lane == 0) give_up(p, abort_flag);
+                issued = -(t + 1);  // K(t) issued, V(t) not
+                break;
+            }
+            if (lane == 0) mbar_arrive_expect_tx(bar(kVFull + s), bytes_cur);
+            __syncwarp();
+            issue_boxes(&tm_v, base + kOffV + s * kTile, rows_cur, lane, p.box_rows,
+                        bar(kVFull + s), pol_kv);
+            issued = t + 1;
 #pragma unroll
             for (int w = 0; w < 4; ++w) rows_cur[w] = rows_next[w];
             bytes_cur = bytes_next;
         }
         // let every copy into this CTA's shared memory land before leaving
         if (!mbar_wait(bar(kQFull), 0)) give_up(p, abort_flag);
-        for (int t = max(0, kissued - 2); t < kissued; ++t)
+        const int kdone = issued < 0 ? -issued : issued, vdone = issued < 0 ? -issued - 1 : issued;
+        for (int t = max(0, kdone - 2); t < kdone; ++t)
             if (!mbar_wait(bar(kKFull + (t & 1)), (t >> 1) & 1)) give_up(p, abort_flag);
-        if (vissued > 0 && !mbar_wait(bar(kVFull), (vissued - 1) & 1)) give_up(p, abort_flag);
+        for (int t = max(0, vdone - 2); t < vdone; ++t)
+            if (!mbar_wait(bar(kVFull + (t & 1)), (t >> 1) & 1)) give_up(p, abort_flag);
     } else if (warp == 1 && nk > 0) {
         // ============================ MMA issuer =============================
         if (lane == 0) {
@@ -294,13 +306,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc::commit(bar(kSFull + t));
             };
             auto pv = [&](int t, int j) {
-                const uint32_t paddr = base + kOffP + t * kTile;
+                const uint32_t paddr = base + kOffP;
+                const uint32_t vaddr = base + kOffV + (j & 1) * kTile;
 #pragma unroll
                 for (int kk = 0; kk < BN / 16; ++kk) {
                     const uint32_t poff = (kk >> 2) * kHalf + (kk & 3) * 32;
                     tc::mma_bf16(tmem + col_o(t), tc::smem_desc_sw128(paddr + poff, 16, 1024),
-                                 tc::smem_desc_sw128(base + kOffV + kk * 16 * 128, kHalf, 1024),
-                                 idO, (j > 0 || kk > 0) ? 1u : 0u);
+                                 tc::smem_desc_sw128(vaddr + kk * 16 * 128, kHalf, 1024), idO,
+                                 (j > 0 || kk > 0) ? 1u : 0u);
                 }
                 tc::commit(bar(kODone + t));
             };
@@ -312,7 +325,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc::commit(bar(kKEmpty));
             }
             for (int j = 0; ok && j < nk; ++j) {
-                ok = mbar_wait(bar(kVFull), j & 1);
+                ok = mbar_wait(bar(kVFull + (j & 1)), (j >> 1) & 1);
                 if (!ok || *abort_flag) break;
                 const bool more = j + 1 < nk;
                 if (j < nk_t[0]) {
@@ -333,7 +346,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tc::fence_after_sync();
                     pv(1, j);
                 }
-                tc::commit(bar(kVEmpty));
+                tc::commit(bar(kVEmpty + (j & 1)));
                 if (more) {
                     if (j + 1 < nk_t[1]) qk(1, j + 1);
                     tc::commit(bar(kKEmpty + ((j + 1) & 1)));
@@ -369,60 +382,76 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int cc = 0; cc < 4; ++cc) tc::ld32(trow + col_s(t) + cc * 32, x[cc]);
             tc::wait_ld();
             // causal / length mask (frontier tiles only), row max of raw scores
-            const bool masking = j * BN + BN - 1 > lim_min_t[t];
-            const int cmax = lim - j * BN;  // columns <= cmax are visible
-            float mt = neg_inf();
+            const bool masking = j * BN + BN - 1 > lim_min_t[t];  // uniform over the CTA
+            if (masking) {
+                const int cmax = lim - j * BN;  // columns <= cmax are visible
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc)
+#pragma unroll
+                    for (int e = 0; e < 32; ++e)
+                        if (cc * 32 + e > cmax) x[cc][e] = neg_inf();
+            }
+            float mq[4];
 #pragma unroll
             for (int cc = 0; cc < 4; ++cc) {
+                mq[cc] = x[cc][0];
 #pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    if (masking && cc * 32 + e > cmax) x[cc][e] = neg_inf();
-                    mt = fmaxf(mt, x[cc][e]);
-                }
+                for (int e = 1; e < 31; e += 2) mq[cc] = fmax3(mq[cc], x[cc][e], x[cc][e + 1]);
+                mq[cc] = fmaxf(mq[cc], x[cc][31]);
             }
+            float mt = fmax3(mq[0], mq[1], fmaxf(mq[2], mq[3]));
             mt *= c;
             const bool grow = mt > mrow + kLazyRescaleLog2;
-            // P.V of the previous tile must be done before O or P are touched
-            if (j > 0) {
+            const bool any_grow = __any_sync(0xffffffffu, grow);
+            const float mn = grow ? mt : mrow;
+            const float alpha = grow ? fast_exp2(mrow - mn) : 1.f;  // 2^-inf = 0 at start
+            mrow = mn;
+            // P = 2^(s*c - m) packed to bf16 pairs in registers, before any wait
+            const float mu = (mrow == neg_inf()) ? 0.f : mrow;
+            const float2 c2 = make_float2(c, c), nm2 = make_float2(-mu, -mu);
+            float2 ts = make_float2(0.f, 0.f);
+            uint32_t pw[64];
+            exp_pack(x, c2, nm2, pw, ts);
+            lsum2.x = lsum2.x * alpha + ts.x;
+            lsum2.y = lsum2.y * alpha + ts.y;
+            // O is rescaled once this tile's previous P.V is done
+            if (any_grow && j > 0) {
                 ok = warp_wait(bar(kODone + t), (j - 1) & 1);
                 if (!ok || aborted(abort_flag)) break;
                 tc::fence_after_sync();
-            }
-            if (__any_sync(0xffffffffu, grow)) {
-                const float mn = grow ? mt : mrow;
-                const float alpha = grow ? fast_exp2(mrow - mn) : 1.f;  // 2^-inf = 0 at start
-                if (j > 0) {
 #pragma unroll 1
-                    for (int cc = 0; cc < 4; ++cc) {
-                        float o[32];
-                        tc::ld32(trow + col_o(t) + cc * 32, o);
-                        tc::wait_ld();
+                for (int cc = 0; cc < 4; ++cc) {
+                    float o[32];
+                    tc::ld32(trow + col_o(t) + cc * 32, o);
+                    tc::wait_ld();
 #pragma unroll
-                        for (int e = 0; e < 32; ++e) o[e] *= alpha;
-                        tc::st32(trow + col_o(t) + cc * 32, o);
-                    }
-                    tc::wait_st();
+                    for (int e = 0; e < 32; ++e) o[e] *= alpha;
+                    tc::st32(trow + col_o(t) + cc * 32, o);
                 }
-                lsum2.x *= alpha;
-                lsum2.y *= alpha;
-                mrow = mn;
+                tc::wait_st();
             }
-            const float mu = (mrow == neg_inf()) ? 0.f : mrow;
-            const float2 c2 = make_float2(c, c), nm2 = make_float2(-mu, -mu);
-            uint8_t* const prow = sbase + kOffP + t * kTile + r * 128;
+            // the shared P buffer is free once the P.V that read it last is done:
+            // A(j) follows B(j-1), B(j) follows A(j) (or its own tile's previous
+            // P.V when the other tile has none there)
+            {
+                int wt = -1, wj = -1;
+                if (t == 0) {
+                    if (j - 1 >= 0 && j - 1 < nk_t[1]) wt = 1, wj = j - 1;
+                    else if (j > 0) wt = 0, wj = j - 1;
+                } else {
+                    if (j < nk_t[0]) wt = 0, wj = j;
+                    else if (j > 0) wt = 1, wj = j - 1;
+                }
+                if (wt >= 0) {
+                    ok = warp_wait(bar(kODone + wt), wj & 1);
+                    if (!ok || aborted(abort_flag)) break;
+                }
+            }
+            tc::fence_after_sync();
+            uint8_t* const prow = sbase + kOffP + r * 128;
 #pragma unroll
             for (int q = 0; q < 16; ++q) {  // 8 keys per 16-byte chunk
-                const int cc = q >> 2, e0 = (q & 3) * 8;
-                float pv[8];
-#pragma unroll
-                for (int e = 0; e < 8; e += 2) {
-                    const float2 y = __ffma2_rn(make_float2(x[cc][e0 + e], x[cc][e0 + e + 1]), c2, nm2);
-                    pv[e] = fast_exp2(y.x);
-                    pv[e + 1] = fast_exp2(y.y);
-                    lsum2 = __fadd2_rn(lsum2, make_float2(pv[e], pv[e + 1]));
-                }
-                const uint4 w = make_uint4(pack_bf16x2(pv[0], pv[1]), pack_bf16x2(pv[2], pv[3]),
-                                           pack_bf16x2(pv[4], pv[5]), pack_bf16x2(pv[6], pv[7]));
+                const uint4 w = make_uint4(pw[4 * q], pw[4 * q + 1], pw[4 * q + 2], pw[4 * q + 3]);
                 const int half = q >> 3, cq = q & 7;
                 *reinterpret_cast<uint4*>(prow + half * kHalf + ((cq ^ (r & 7)) << 4)) = w;
             }

@@ -109,6 +109,13 @@ __device__ __forceinline__ float fast_exp2(float x) {
     return y;
 }
 
+// max(a, b, c) in one instruction.
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
 // bf16 pair (one 32-bit word, low half = first element) -> two floats.
 __device__ __forceinline__ float2 bf16x2_to_float2(uint32_t w) {
     return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));

@@ -63,13 +63,18 @@ pa_status check_shape(const pa_shape* s) {
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 int choose(const pa_shape& s) {
-    if (s.dtype != PA_BF16) return PA_SCHED_DECODE;
+    if (s.dtype != PA_BF16 || !prefill_supported(s)) return PA_SCHED_DECODE;
     const long long rows = static_cast<long long>(s.H_q / s.H_kv) * s.L;
-    // A one-token query has no query-tile reuse: the page walk on CUDA cores
-    // is memory-bound and needs no tensor cores.  Enough rows per kv head to
-    // fill a 128-row tensor-core tile go to the tiled prefill.
-    if (rows <= 16 || !prefill_supported(s)) return PA_SCHED_DECODE;
-    return PA_SCHED_PREFILL;
+    // Measured crossover (operator sweep over G in {1, 4}, L in 1..128,
+    // contexts 64..16384, B in {8, 64}): with more than 4 query rows per kv
+    // head the tensor-core tiles win at every context length (1.3x at 8
+    // rows, 2-10x beyond); with at most 4 rows the page walk on CUDA cores
+    // wins, except on calls so small that the tile schedule's lower fixed
+    // cost decides (B * H_kv * context capacity up to 64K token rows).
+    if (rows > 4) return PA_SCHED_PREFILL;
+    const long long work =
+        static_cast<long long>(s.B) * s.H_kv * s.max_pages_per_seq * s.page_size;
+    return work <= 65536 ? PA_SCHED_PREFILL : PA_SCHED_DECODE;
 }
 
 pa_status run(const pa_shape* shape, const void* query, const void* key_pages,
@@ -168,6 +173,31 @@ pa_status pa_gather_debug(const pa_shape* shape, const void* key_pages, const vo
     if (!workspace || !aligned(workspace, 4)) return PA_ERR_WORKSPACE;
     return gather_launch(*shape, key_pages, value_pages, block_table, context_lens, max_S,
                          k_dense, v_dense, static_cast<uint32_t*>(workspace),
+                         static_cast<cudaStream_t>(cuda_stream));
+}
+
+pa_status pa_append_kv(const pa_shape* shape, const void* k_new, const void* v_new,
+                       void* key_pages, void* value_pages, const int32_t* block_table,
+                       const int32_t* context_lens, void* workspace, size_t workspace_bytes,
+                       void* cuda_stream) {
+    pa_status st = check_shape(shape);
+    if (st != PA_OK) return st;
+    if (!k_new || !v_new || !key_pages || !value_pages || !block_table || !context_lens)
+        return PA_ERR_INVALID_ARG;
+    if (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(key_pages, 16) ||
+        !aligned(value_pages, 16) || !aligned(block_table, 4) || !aligned(context_lens, 4))
+        return PA_ERR_INVALID_ARG;
+    if (!workspace || !aligned(workspace, 4) || workspace_bytes < kFlagBytes)
+        return PA_ERR_WORKSPACE;
+    const int es = shape->dtype == PA_BF16 ? 2 : 4;
+    const long long chunks = static_cast<long long>(shape->B) * shape->H_kv * shape->L *
+                             (shape->D * es / 16);
+    if (chunks >= (1ll << 31)) return PA_ERR_UNSUPPORTED;
+    DeviceInfo dev;
+    st = current_device_info(&dev);
+    if (st != PA_OK) return st;
+    return append_launch(*shape, k_new, v_new, key_pages, value_pages, block_table, context_lens,
+                         static_cast<uint32_t*>(workspace), dev.sm_count,
                          static_cast<cudaStream_t>(cuda_stream));
 }
 

@@ -98,9 +98,19 @@ def test_unknown_schedule_is_rejected():
 
 
 def test_schedule_rule():
-    # single-token decode and the fp32 control run on the page walk
-    assert B.pa_choose_schedule(good_shape(L=1)) == B.PA_SCHED_DECODE
+    """The dispatch follows the measured crossover of the operator sweep."""
+    decode_cfg = dict(B=64, H_q=32, H_kv=8, num_pages=2048, page_size=128, max_pages_per_seq=32)
+    # up to 4 query rows per kv head over a real batch: the page walk
+    assert B.pa_choose_schedule(good_shape(L=1, **decode_cfg)) == B.PA_SCHED_DECODE
+    assert B.pa_choose_schedule(good_shape(L=1, **{**decode_cfg, "H_q": 8})) == B.PA_SCHED_DECODE
+    # more than 4 rows per kv head: the tensor-core tiles
+    assert B.pa_choose_schedule(good_shape(L=2, **decode_cfg)) == B.PA_SCHED_PREFILL
+    assert B.pa_choose_schedule(good_shape(L=2048, **decode_cfg)) == B.PA_SCHED_PREFILL
+    # a tiny call: the tile schedule's lower fixed cost wins even for one row
+    assert B.pa_choose_schedule(good_shape(L=1)) == B.PA_SCHED_PREFILL
+    # fp32 and shapes the tiles do not take (page size not a multiple of 8)
     assert B.pa_choose_schedule(good_shape(L=2048, dtype=B.PA_F32)) == B.PA_SCHED_DECODE
+    assert B.pa_choose_schedule(good_shape(L=64, page_size=12, num_pages=40)) == B.PA_SCHED_DECODE
     assert B.pa_choose_schedule(good_shape(D=64)) == -1
     assert B.pa_launch_count(good_shape(L=1), B.PA_SCHED_DECODE) == 2
 

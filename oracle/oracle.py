@@ -91,6 +91,8 @@ class OracleLib:
             sp, vp, vp, vp, ip, ip, ctypes.c_double, ctypes.c_int, ip, ctypes.c_int, dp,
             ctypes.c_int]
         self.lib.oracle_paged_attention_rows.restype = ctypes.c_int
+        self.lib.oracle_append_kv.argtypes = [sp, vp, vp, vp, vp, ip, ip]
+        self.lib.oracle_append_kv.restype = ctypes.c_int
 
     @staticmethod
     def _shape(query, key_pages, block_table, L=None, H_q=None, B=None):
@@ -159,6 +161,28 @@ class OracleLib:
         if st != ORACLE_OK:
             raise OracleError(st)
         return k, v
+
+
+    def append_kv(self, k_new, v_new, key_pages, value_pages, block_table, context_lens):
+        """Copies of the pools after writing the new tokens' K/V rows
+        (k_new/v_new [B, H_kv, L, D], the last L positions of each context)
+        through the block table.  Returns (key_pages, value_pages, status);
+        status is ORACLE_OK or the error of a skipped sequence / token."""
+        self._check_arrays(k_new, v_new, key_pages, value_pages, block_table, context_lens)
+        assert k_new.dtype == key_pages.dtype and v_new.dtype == value_pages.dtype
+        P, H_kv, ps, D = key_pages.shape
+        B, Hk, L, Dn = k_new.shape
+        assert Hk == H_kv and Dn == D and v_new.shape == k_new.shape
+        sh = _Shape(B=B, H_q=H_kv, H_kv=H_kv, L=L, D=D, num_pages=P, page_size=ps,
+                    max_pages_per_seq=block_table.shape[1],
+                    dtype=0 if key_pages.dtype == np.uint16 else 1)
+        kp = key_pages.copy()
+        vp = value_pages.copy()
+        st = self.lib.oracle_append_kv(
+            ctypes.byref(sh), _ptr(k_new), _ptr(v_new), _ptr(kp), _ptr(vp),
+            block_table.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),
+            context_lens.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)))
+        return kp, vp, int(st)
 
 
 def load(mutant: int = 0) -> OracleLib:

@@ -22,6 +22,13 @@
  *                    "Week 3 Day 5", Task 2.  Natural exp in double; the max
  *                    is subtracted before exponentiating (stable softmax).
  *
+ *   oracle_append_kv() -- the step before the path: the new tokens' K/V rows
+ *                    are stored in their pages.  The pages introduce physical
+ *                    pages and block tables as the prerequisite of "Week 3 Day
+ *                    5: Paged FlashAttention" (Prerequisites) and give the
+ *                    read-side translation in Task 1; the write uses the same
+ *                    translation for the last L positions of each context.
+ *
  * No tiling, no online rescaling, no reordering beyond the definition.
  * Parallelism: independent (batch, kv_head) items run on OpenMP threads; each
  * row is computed by one thread in the definition's order.
@@ -269,4 +276,51 @@ int oracle_paged_attention_rows(const oracle_shape* sh, const void* query,
         free(x);
     }
     return failed ? ORACLE_ERR_NOMEM : ORACLE_OK;
+}
+
+/* Append of new keys and values.  The L new tokens of sequence b are the last
+ * L logical positions of its context, s = context_lens[b] - L + t, and are
+ * written through the block table into
+ *   pages[block_table[b, s / page_size], kv_head, s % page_size, :].
+ * Elements are copied as stored (bf16 bit patterns or fp32), so the append is
+ * exact.  Sequences whose context length is < L or > the table's capacity are
+ * skipped (ORACLE_ERR_INVALID_ARG); a token whose page id is out of range is
+ * skipped (ORACLE_ERR_BAD_BLOCK_TABLE); everything else is written. */
+int oracle_append_kv(const oracle_shape* sh, const void* k_new, const void* v_new,
+                     void* key_pages, void* value_pages, const int32_t* block_table,
+                     const int32_t* context_lens) {
+    int st = check_shape(sh);
+    if (st != ORACLE_OK) return st;
+    const int64_t es = sh->dtype == 0 ? 2 : 4;
+    const int64_t row_bytes = (int64_t)sh->D * es;
+    const int ps = sh->page_size, L = sh->L;
+    int bad_ctx = 0, bad_page = 0;
+    for (int b = 0; b < sh->B; ++b) {
+        const int S = context_lens[b];
+        if (S < L || (int64_t)S > (int64_t)sh->max_pages_per_seq * ps) {
+            bad_ctx = 1;
+            continue;
+        }
+        for (int kvh = 0; kvh < sh->H_kv; ++kvh) {
+            for (int t = 0; t < L; ++t) {
+                const int s = S - L + t;
+#if ORACLE_MUTANT == 8
+                const int slot = (s + 1) % ps; /* planted: slot off by one */
+#else
+                const int slot = s % ps;
+#endif
+                const int32_t pp = block_table[(int64_t)b * sh->max_pages_per_seq + s / ps];
+                if (pp < 0 || pp >= sh->num_pages) {
+                    bad_page = 1;
+                    continue;
+                }
+                const int64_t src = (((int64_t)b * sh->H_kv + kvh) * L + t) * row_bytes;
+                const int64_t dst = (((int64_t)pp * sh->H_kv + kvh) * ps + slot) * row_bytes;
+                memcpy((char*)key_pages + dst, (const char*)k_new + src, (size_t)row_bytes);
+                memcpy((char*)value_pages + dst, (const char*)v_new + src, (size_t)row_bytes);
+            }
+        }
+    }
+    if (bad_ctx) return ORACLE_ERR_INVALID_ARG;
+    return bad_page ? ORACLE_ERR_BAD_BLOCK_TABLE : ORACLE_OK;
 }

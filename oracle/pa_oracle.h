@@ -70,6 +70,20 @@ int oracle_paged_attention_rows(const oracle_shape* sh, const void* query,
                                 double scale, int causal, const int32_t* rows, int n_rows,
                                 double* out, int num_threads);
 
+/* Append of new keys and values (the step before the path: the new tokens'
+ * K/V stored in their pages).  Shape fields used: B, H_kv, L (new tokens per
+ * sequence), D, num_pages, page_size, max_pages_per_seq, dtype.  The new
+ * tokens of sequence b are its last L logical positions
+ * s = context_lens[b] - L + t; their rows are copied, as stored, from
+ * k_new/v_new [B, H_kv, L, D] to
+ *   key_pages/value_pages[block_table[b, s / page_size], kv_head, s % page_size, :].
+ * Sequences with context_lens[b] < L or beyond the table's capacity are
+ * skipped (ORACLE_ERR_INVALID_ARG); tokens whose page id is out of range are
+ * skipped (ORACLE_ERR_BAD_BLOCK_TABLE). */
+int oracle_append_kv(const oracle_shape* sh, const void* k_new, const void* v_new,
+                     void* key_pages, void* value_pages, const int32_t* block_table,
+                     const int32_t* context_lens);
+
 #ifdef __cplusplus
 }
 #endif

@@ -150,3 +150,10 @@ def workload(name: str, dtype: str = "bf16", **overrides) -> PagedInputs:
     kw = dict(WORKLOADS[name])
     kw.update(overrides)
     return generate(dtype=dtype, name=name, **kw)
+
+
+def new_kv(B: int, H_kv: int, L: int, D: int, seed: int, dtype: str = "bf16"):
+    """Seeded N(0,1) rows of the new tokens' keys and values, [B, H_kv, L, D]
+    each (bf16 bit patterns or fp32), for the K/V append."""
+    rng = np.random.default_rng(seed)
+    return _normal(rng, (B, H_kv, L, D), dtype), _normal(rng, (B, H_kv, L, D), dtype)

@@ -344,6 +344,113 @@ def pin_rows_api(lib):
         assert np.array_equal(got[i], full[b, h, l])
 
 
+# ---- K/V append ---------------------------------------------------------------
+# The append writes the new tokens' rows at the last L positions of each
+# context through the block table.  Facts that fix it:
+#   * with pages handed out in order, the pool is a plain reshape of a dense
+#     [B, H_kv, capacity, D] cache (numpy transpose/reshape), so the append is
+#     a slice assignment dense[b, :, S-L:S, :] = new[b];
+#   * physical page permutation is invisible: appending into a permuted pool
+#     and un-permuting gives the in-order result, bitwise;
+#   * nothing outside the targeted (page, slot) rows changes.
+def _append_case(seed, B, H_kv, L, D, ps, ctx, npg_cap, dtype="bf16", perm=True):
+    from paged_kv_cache_03_gb300.synth import new_kv
+    rng = np.random.default_rng(seed)
+    P = B * npg_cap
+    order = rng.permutation(P).astype(np.int32) if perm else np.arange(P, dtype=np.int32)
+    bt = order.reshape(B, npg_cap).copy()
+    if dtype == "bf16":
+        kp = bf16_bits(rng.standard_normal((P, H_kv, ps, D), dtype=np.float32))
+        vp = bf16_bits(rng.standard_normal((P, H_kv, ps, D), dtype=np.float32))
+    else:
+        kp = rng.standard_normal((P, H_kv, ps, D), dtype=np.float32)
+        vp = rng.standard_normal((P, H_kv, ps, D), dtype=np.float32)
+    kn, vn = new_kv(B, H_kv, L, D, seed + 7, dtype)
+    return kn, vn, kp, vp, bt, np.asarray(ctx, dtype=np.int32)
+
+
+def _dense_view(pool, bt, B, H_kv, ps, D):
+    """[B, H_kv, npg*ps, D] view of a pool whose sequence b owns pages
+    bt[b, 0], bt[b, 1], ... in order."""
+    npg = bt.shape[1]
+    out = np.empty((B, H_kv, npg * ps, D), dtype=pool.dtype)
+    for b in range(B):
+        pages = pool[bt[b]]                      # [npg, H_kv, ps, D]
+        out[b] = pages.transpose(1, 0, 2, 3).reshape(H_kv, npg * ps, D)
+    return out
+
+
+def pin_append_dense_slice(lib):
+    for seed, B, H_kv, L, ps, ctx, cap in ((201, 2, 2, 3, 4, [7, 12], 3),
+                                           (202, 3, 1, 1, 1, [1, 5, 2], 5),
+                                           (203, 2, 2, 5, 3, [5, 9], 4)):
+        for dtype in ("bf16", "f32"):
+            kn, vn, kp, vp, bt, c = _append_case(seed, B, H_kv, L, 16, ps, ctx, cap, dtype,
+                                                 perm=False)
+            k2, v2, st = lib.append_kv(kn, vn, kp, vp, bt, c)
+            assert st == oracle_mod.ORACLE_OK
+            for pool, new, after in ((kp, kn, k2), (vp, vn, v2)):
+                want = _dense_view(pool, bt, B, H_kv, ps, 16)
+                for b in range(B):
+                    want[b, :, c[b] - L:c[b], :] = new[b]
+                got = _dense_view(after, bt, B, H_kv, ps, 16)
+                assert np.array_equal(got, want), (seed, dtype)
+
+
+def pin_append_page_permutation(lib):
+    B, H_kv, L, ps, ctx, cap = 3, 2, 4, 4, [6, 11, 4], 3
+    kn, vn, kp, vp, bt, c = _append_case(211, B, H_kv, L, 16, ps, ctx, cap, perm=False)
+    k_ref, v_ref, st = lib.append_kv(kn, vn, kp, vp, bt, c)
+    assert st == oracle_mod.ORACLE_OK
+    perm = np.random.default_rng(212).permutation(kp.shape[0])
+    kpp = np.empty_like(kp)
+    vpp = np.empty_like(vp)
+    kpp[perm] = kp
+    vpp[perm] = vp
+    k2, v2, st = lib.append_kv(kn, vn, kpp, vpp, perm[bt].astype(np.int32), c)
+    assert st == oracle_mod.ORACLE_OK
+    assert np.array_equal(k2[perm], k_ref) and np.array_equal(v2[perm], v_ref)
+
+
+def pin_append_touches_only_new_rows(lib):
+    B, H_kv, L, ps, ctx, cap = 2, 2, 3, 4, [9, 3], 4
+    kn, vn, kp, vp, bt, c = _append_case(221, B, H_kv, L, 16, ps, ctx, cap)
+    bt[:, 3] = -7  # entries past each context's pages: never read
+    k2, v2, st = lib.append_kv(kn, vn, kp, vp, bt, c)
+    assert st == oracle_mod.ORACLE_OK
+    changed = np.any(k2 != kp, axis=-1) | np.any(v2 != vp, axis=-1)  # [P, H_kv, ps]
+    want = np.zeros_like(changed)
+    for b in range(B):
+        for t in range(L):
+            s = int(c[b]) - L + t
+            want[bt[b, s // ps], :, s % ps] = True
+    assert np.array_equal(changed, want)
+    # and the gather of the appended pools returns the new rows there
+    kd, vd = lib.gather(k2, v2, bt, c, int(c.max()))
+    for b in range(B):
+        assert np.array_equal(kd[b, :, c[b] - L:c[b]], bf16_to_f32(kn[b]).astype(np.float64))
+        assert np.array_equal(vd[b, :, c[b] - L:c[b]], bf16_to_f32(vn[b]).astype(np.float64))
+
+
+def pin_append_errors(lib):
+    B, H_kv, L, ps, ctx, cap = 2, 1, 3, 4, [2, 7], 2  # sequence 0 is shorter than L
+    kn, vn, kp, vp, bt, c = _append_case(231, B, H_kv, L, 16, ps, ctx, cap)
+    k2, v2, st = lib.append_kv(kn, vn, kp, vp, bt, c)
+    assert st == oracle_mod.ORACLE_ERR_INVALID_ARG
+    assert np.array_equal(k2[bt[0]], kp[bt[0]])  # nothing of sequence 0 written
+    kd, _ = lib.gather(k2, v2, bt[1:], c[1:], 7)
+    assert np.array_equal(kd[0, :, 4:7], bf16_to_f32(kn[1]).astype(np.float64))
+    bt2 = bt.copy()
+    bt2[1, 1] = kp.shape[0] + 3  # position 4..6 of sequence 1 sit on a bad page
+    c2 = np.array([3, 7], dtype=np.int32)
+    k3, _, st = lib.append_kv(kn, vn, kp, vp, bt2, c2)
+    assert st == oracle_mod.ORACLE_ERR_BAD_BLOCK_TABLE
+    kd, _ = lib.gather(k3, k3, bt2[:1], c2[:1], 3)
+    assert np.array_equal(kd[0, :, 0:3], bf16_to_f32(kn[0]).astype(np.float64))
+
+
 ALL_PINS = [pin_bruteforce, pin_torch_sdpa, pin_page_permutation, pin_unused_table_entries,
             pin_tile_size_invariance, pin_single_page, pin_one_hot, pin_uniform_visible_mean,
-            pin_gqa_equals_repeat, pin_gather, pin_errors, pin_rows_api]
+            pin_gqa_equals_repeat, pin_gather, pin_errors, pin_rows_api,
+            pin_append_dense_slice, pin_append_page_permutation, pin_append_touches_only_new_rows,
+            pin_append_errors]

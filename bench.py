@@ -6,7 +6,7 @@ One step = one call of the C-ABI entry point over one batch of the workload
 Prints ONE JSON line.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload decode|prefill|tails|long_decode|tiny]
+                  [--workload decode|prefill|tails|long_decode|tiny] [--op attention|append]
 
 Default workload: batched decode, B=64, L=1, H_q=32, H_kv=8, D=128,
 page_size=128, context lengths U{128..4096}, scattered pages (seeded).
@@ -14,6 +14,9 @@ Metric: achieved HBM GB/s = algorithmic bytes / device time (bf16).
 
 --impl reference times the fp64 CPU oracle on the host cores over a bounded
 sample of the same workload (the method has no other reference program).
+
+--op append measures the K/V append instead (pa_append_kv: the workload's L
+new tokens per sequence written into their pages), in HBM GB/s.
 Under torchrun each rank runs its own replica (the path has no exchange
 step); rank 0 prints.
 """
@@ -75,6 +78,20 @@ def algorithmic_flops(inp) -> int:
     """4 * H_q * D * visible pairs: a multiply-add per element of Q.K^T and
     of P.V."""
     return 4 * inp.H_q * inp.D * visible_pairs(inp)
+
+
+def append_bytes(inp) -> int:
+    """Minimum bytes one K/V append moves: the new K and V rows read once and
+    written once into the pool (2 tensors x 2 x B*H_kv*L*D*elt), the
+    block-table entries of the pages that receive them and the context
+    lengths."""
+    es = 2 if inp.dtype == "bf16" else 4
+    rows = 2 * inp.B * inp.H_kv * inp.L * inp.D * es
+    pages = 0
+    for s in inp.context_lens.astype(np.int64):
+        s = int(s)
+        pages += (s - 1) // inp.page_size - (s - inp.L) // inp.page_size + 1
+    return 2 * rows + 4 * pages + 4 * inp.B
 
 
 def workload_desc(name, inp) -> str:
@@ -448,6 +465,140 @@ def run_ours(args):
 # ---------------------------------------------------------------------------
 # reference arm: the fp64 oracle on the host cores
 # ---------------------------------------------------------------------------
+def run_append(args):
+    """One step = one pa_append_kv call storing the workload's L new tokens
+    per sequence (seeded N(0,1) rows) in their pages."""
+    import torch
+    from paged_kv_cache_03_gb300 import binding as B
+    world, rank, local = dist_env()
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist_init("nccl")
+    device = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(device)
+    B.load()
+    inp = synth.workload(args.workload)
+    kn_np, vn_np = synth.new_kv(inp.B, inp.H_kv, inp.L, inp.D, 4242, inp.dtype)
+    tdt = torch.bfloat16 if inp.dtype == "bf16" else torch.float32
+
+    def dev_tensor(a, dt=None):
+        t = torch.from_numpy(np.ascontiguousarray(a))
+        return (t.view(dt) if dt is not None else t).to(device)
+
+    kn, vn = dev_tensor(kn_np, tdt), dev_tensor(vn_np, tdt)
+    kp, vp = dev_tensor(inp.key_pages, tdt), dev_tensor(inp.value_pages, tdt)
+    bt, ctx = dev_tensor(inp.block_table), dev_tensor(inp.context_lens)
+    shape = B.make_shape(inp.B, inp.H_kv, inp.H_kv, inp.L, inp.D, inp.num_pages, inp.page_size,
+                         inp.block_table.shape[1], B.PA_BF16 if inp.dtype == "bf16" else B.PA_F32)
+    ws = torch.zeros(256, dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream(device)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+    bytes_step = append_bytes(inp)
+
+    def call():
+        st = B.pa_append_kv(shape, kn, vn, kp, vp, bt, ctx, ws, ws.numel(), stream)
+        if st != B.PA_OK:
+            raise RuntimeError(f"pa_append_kv: {B.status_str(st)}")
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        call()
+    torch.cuda.synchronize(device)
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
+    for e in ev:
+        for x in e:
+            x.record(stream)
+    torch.cuda.synchronize(device)
+    sampler = ClockSampler(device.index)
+    if rank == 0:
+        sampler.start()
+    barrier(device)
+    torch.cuda.synchronize(device)
+    for k in range(K):
+        flush.zero_()
+        ev[k][0].record(stream)
+        call()
+        ev[k][1].record(stream)
+    torch.cuda.synchronize(device)
+    barrier(device)
+    clocks = sampler.stop() if rank == 0 else None
+    step_ms = np.array([e[0].elapsed_time(e[1]) for e in ev])
+    _, flag = B.pa_check_device_flag(ws, stream=stream)
+    if flag:
+        raise RuntimeError(f"device flag {flag:#x} after timed steps")
+    value, t_max = aggregate(bytes_step, K, float(step_ms.sum()), world, device)
+    peaks, peaks_src = load_peaks()
+    achieved = bytes_step / (float(step_ms.mean()) * 1e-3) / 1e9
+    peak = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
+    roofline = {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 4),
+                "traffic": recorded_traffic("append_kv_kernel", args.workload),
+                "kernel": "append_kv_kernel", "kernel_ms_avg": round(float(step_ms.mean()), 5),
+                "peak_source": f"{peaks_src} (MEASURED_PEAKS.json)" if peaks_src == "measured"
+                else "fallback", "algorithmic_bytes": bytes_step}
+    e2e = None
+    if not args.no_e2e:
+        host = [torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
+                for a in (kn_np, vn_np, inp.block_table, inp.context_lens)]
+        dsts = [kn, vn, bt, ctx]
+        flag_host = torch.empty(1, dtype=torch.int32).pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in host)
+        Ke = max(3, min(args.e2e_steps, K))
+
+        def e2e_step():
+            for h, d in zip(host, dsts):
+                d.view(torch.uint8).view(-1).copy_(h.view(torch.uint8).view(-1), non_blocking=True)
+            call()
+            flag_host.copy_(ws[:4].view(torch.int32), non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize(device)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(Ke):
+            e2e_step()
+        b.record(stream)
+        torch.cuda.synchronize(device)
+        e2e_ms = reduce_max(a.elapsed_time(b), device)
+        e2e = {"value": round(bytes_step * Ke * world / (e2e_ms * 1e-3) / 1e9, 3), "unit": "GB/s",
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": 4, "steps": Ke,
+               "ms_per_step": round(e2e_ms / Ke, 4),
+               "note": "pinned host new rows, block table and context lengths copied to HBM, "
+                       "one call, flag word copied back, every step (the pools stay in HBM)"}
+    line = {
+        "metric": "paged K/V append HBM GB/s (bf16, d128)", "value": round(value / 1e9, 3),
+        "unit": "GB/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
+        "ms_per_step": round(t_max / K, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": inp.dtype,
+        "data": "synthetic (seeded N(0,1) new rows, scattered pages)",
+        "config": {"workload": "append of the new tokens of " + workload_desc(args.workload, inp),
+                   "l2": "flushed: 256 MiB write between timed steps (outside step events)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
+                   "algorithmic_bytes_per_step": bytes_step},
+        "clocks": clocks, "e2e": e2e, "gpu_launches": K, "roofline": roofline,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        import oracle
+        lib = oracle.load()
+        reps, t0 = 0, time.perf_counter()
+        while True:
+            lib.append_kv(kn_np, vn_np, inp.key_pages, inp.value_pages, inp.block_table,
+                          inp.context_lens)
+            reps += 1
+            if time.perf_counter() - t0 > min(args.cpu_seconds, 10.0):
+                break
+        secs = time.perf_counter() - t0
+        line["cpu_baseline"] = {"value": round(bytes_step * reps / secs / 1e9, 6), "unit": "GB/s",
+                                "cores": 1, "kind": "oracle",
+                                "sample": f"{reps} whole appends (includes the oracle's copy "
+                                          "of both pools)", "seconds": round(secs, 3)}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    return line
+
+
 def run_reference(args):
     world, rank, _ = dist_env()
     if world > 1 and rank != 0:
@@ -509,6 +660,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(synth.WORKLOADS), default="decode")
+    ap.add_argument("--op", choices=["attention", "append"], default="attention",
+                    help="the path (paged attention) or the K/V append before it")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -518,6 +671,12 @@ def main(argv=None):
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
+    if args.op == "append":
+        if args.impl == "reference":
+            print(json.dumps({"impl": "reference", "unavailable":
+                              "the append's reference arm is its oracle: see cpu_baseline"}))
+            return None
+        return run_append(args)
     if args.impl == "reference":
         return run_reference(args)
     return run_ours(args)

@@ -127,6 +127,36 @@ pa_status pa_gather_debug(const pa_shape* shape, const void* key_pages, const vo
                           const int32_t* block_table, const int32_t* context_lens, int max_S,
                           void* k_dense, void* v_dense, void* workspace, void* cuda_stream);
 
+/* Stores the new tokens' keys and values in their pages: the step that fills
+ * the pool before the path reads it.  The pages introduce pages and block
+ * tables as the prerequisite of "Week 3 Day 5: Paged FlashAttention"
+ * (Prerequisites) and give the read-side translation in its Task 1; this
+ * call writes through the same translation.
+ *
+ * Shape fields used: B, H_kv, L (new tokens per sequence), D, num_pages,
+ * page_size, max_pages_per_seq, dtype (H_q must still be a multiple of H_kv).
+ * k_new, v_new: [B, H_kv, L, D] device arrays in the pool's element type,
+ * 16-byte aligned.  The new tokens of sequence b are its last L logical
+ * positions s = context_lens[b] - L + t (t = 0..L-1; context_lens counts
+ * them, as in pa_paged_attention), and
+ *   key_pages[block_table[b, s / page_size], kv_head, s % page_size, :]
+ *       = k_new[b, kv_head, t, :]
+ * (the same for values).  The copy is exact.  Only block-table entries of the
+ * pages holding new tokens are read.  Positions of two sequences must not map
+ * to the same (page, slot): the pool is written, not reduced.
+ * The kernel reports in the workspace's flag word (offset 0, >= 256 bytes,
+ * zeroed by the caller once): PA_FLAG_BAD_CONTEXT for a sequence with
+ * context_lens[b] < L or > max_pages_per_seq * page_size (nothing of it is
+ * written), PA_FLAG_BAD_PAGE for a page id outside [0, num_pages) (that token
+ * is not written).  Asynchronous on cuda_stream; allocates nothing.
+ * Returns PA_ERR_INVALID_ARG for null or misaligned pointers,
+ * PA_ERR_UNSUPPORTED for D != 128 or more than 2^31 16-byte chunks,
+ * PA_ERR_WORKSPACE for a missing workspace, PA_ERR_CUDA for launch errors. */
+pa_status pa_append_kv(const pa_shape* shape, const void* k_new, const void* v_new,
+                       void* key_pages, void* value_pages, const int32_t* block_table,
+                       const int32_t* context_lens, void* workspace, size_t workspace_bytes,
+                       void* cuda_stream);
+
 /* Synchronises the stream, copies the flag word to *flag_out and, if clear is
  * non-zero, resets it to 0.  Returns PA_ERR_DEVICE_FLAG when any bit was set. */
 pa_status pa_check_device_flag(void* workspace, uint32_t* flag_out, int clear, void* cuda_stream);

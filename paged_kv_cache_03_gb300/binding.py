@@ -98,6 +98,8 @@ def load(auto_build: bool = True):
         lib.pa_choose_schedule.restype = ctypes.c_int
         lib.pa_launch_count.argtypes = [sp, ctypes.c_int]
         lib.pa_launch_count.restype = ctypes.c_int
+        lib.pa_append_kv.argtypes = [sp, vp, vp, vp, vp, i32p, i32p, vp, sz, vp]
+        lib.pa_append_kv.restype = ctypes.c_int
         lib.pa_status_str.argtypes = [ctypes.c_int]
         lib.pa_status_str.restype = ctypes.c_char_p
         _lib = lib
@@ -203,6 +205,14 @@ def pa_gather_debug(shape, key_pages, value_pages, block_table, context_lens, ma
         _stream(stream))
 
 
+def pa_append_kv(shape, k_new, v_new, key_pages, value_pages, block_table, context_lens,
+                 workspace, workspace_bytes, stream=None) -> int:
+    return load().pa_append_kv(
+        ctypes.byref(shape), _ptr(k_new), _ptr(v_new), _ptr(key_pages), _ptr(value_pages),
+        _ptr(block_table), _ptr(context_lens), _ptr(workspace), int(workspace_bytes),
+        _stream(stream))
+
+
 def pa_check_device_flag(workspace, clear=False, stream=None):
     """Returns (status, flag word)."""
     f = ctypes.c_uint32(0)
@@ -261,3 +271,25 @@ def paged_attention(query, key_pages, value_pages, block_table, context_lens, pa
     if st != PA_OK:
         raise PagedAttentionError(st, "pa_paged_attention")
     return out
+
+
+def append_kv(k_new, v_new, key_pages, value_pages, block_table, context_lens, *,
+              workspace=None, stream=None):
+    """Stores k_new/v_new [B, H_kv, L, D] -- the last L positions of each
+    context -- in their pages, through block_table (in place)."""
+    import torch
+    B_, H_kv, L, D = k_new.shape
+    P, Hk, ps, Dk = key_pages.shape
+    if Hk != H_kv or Dk != D or v_new.shape != k_new.shape:
+        raise ValueError("k_new/v_new must be [B, H_kv, L, D] matching the pools")
+    if k_new.dtype != key_pages.dtype or v_new.dtype != value_pages.dtype:
+        raise ValueError("new rows must have the pools' dtype")
+    dtype = PA_BF16 if key_pages.dtype == torch.bfloat16 else PA_F32
+    shape = make_shape(B_, H_kv, H_kv, L, D, P, ps, block_table.shape[1], dtype)
+    if workspace is None:
+        workspace = torch.zeros(256, dtype=torch.uint8, device=key_pages.device)
+    st = pa_append_kv(shape, k_new.contiguous(), v_new.contiguous(), key_pages, value_pages,
+                      block_table, context_lens, workspace, workspace.numel(), stream)
+    if st != PA_OK:
+        raise PagedAttentionError(st, "pa_append_kv")
+    return workspace

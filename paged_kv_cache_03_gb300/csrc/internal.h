@@ -58,6 +58,11 @@ pa_status decode_launch(const Call& c);
 bool prefill_supported(const pa_shape& sh);
 pa_status prefill_launch(const Call& c);
 
+// ---- K/V append -----------------------------------------------------------
+pa_status append_launch(const pa_shape& sh, const void* k_new, const void* v_new, void* kp,
+                        void* vp, const int32_t* bt, const int32_t* ctx, uint32_t* flag,
+                        int sm_count, cudaStream_t stream);
+
 // ---- debug gather ---------------------------------------------------------
 pa_status gather_launch(const pa_shape& sh, const void* kp, const void* vp, const int32_t* bt,
                         const int32_t* ctx, int max_S, void* kd, void* vd, uint32_t* flag,

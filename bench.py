@@ -114,13 +114,21 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
-def kernel_source_digest() -> str:
+# The sources each kernel is built from: its recorded DRAM traffic stays valid
+# while these are unchanged.
+KERNEL_SOURCES = {
+    "decode_split_kernel": ("decode.cu", "ptx.cuh", "internal.h"),
+    "prefill_tile_kernel": ("prefill.cu", "tc.cuh", "ptx.cuh", "internal.h"),
+    "append_kv_kernel": ("append.cu", "internal.h"),
+}
+
+
+def kernel_source_digest(kernel: str) -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "paged_kv_cache_03_gb300", "csrc")
-    for fn in sorted(os.listdir(csrc)):
-        if fn.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(csrc, fn), "rb") as f:
-                h.update(fn.encode() + b"\0" + f.read())
+    for fn in sorted(KERNEL_SOURCES[kernel]):
+        with open(os.path.join(csrc, fn), "rb") as f:
+            h.update(fn.encode() + b"\0" + f.read())
     return h.hexdigest()[:16]
 
 
@@ -132,7 +140,7 @@ def recorded_traffic(kernel: str, workload: str):
         with open(p) as f:
             d = json.load(f)
         e = d[f"{kernel}@{workload}"]
-        if e.get("source_digest") != kernel_source_digest():
+        if e.get("source_digest") != kernel_source_digest(kernel):
             return None
         return int(e["dram_bytes_per_launch"])
     except Exception:

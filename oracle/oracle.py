@@ -91,6 +91,11 @@ class OracleLib:
             sp, vp, vp, vp, ip, ip, ctypes.c_double, ctypes.c_int, ip, ctypes.c_int, dp,
             ctypes.c_int]
         self.lib.oracle_paged_attention_rows.restype = ctypes.c_int
+        fp = ctypes.POINTER(ctypes.c_float)
+        self.lib.oracle_paged_attention_masked.argtypes = [
+            sp, vp, vp, vp, ip, ip, ctypes.c_double, ctypes.c_int, fp, ctypes.c_int, dp,
+            ctypes.c_int]
+        self.lib.oracle_paged_attention_masked.restype = ctypes.c_int
         self.lib.oracle_append_kv.argtypes = [sp, vp, vp, vp, vp, ip, ip]
         self.lib.oracle_append_kv.restype = ctypes.c_int
 
@@ -109,16 +114,31 @@ class OracleLib:
             assert a.flags["C_CONTIGUOUS"], "oracle inputs must be C-contiguous"
 
     def paged_attention(self, query, key_pages, value_pages, block_table, context_lens,
-                        scale: float, causal: bool, num_threads: int = 0) -> np.ndarray:
+                        scale: float, causal: bool, num_threads: int = 0,
+                        mask=None) -> np.ndarray:
+        """mask: optional float32 additive mask [B * H_q, L, S_mask] over
+        logical key positions (S_mask >= every context length)."""
         self._check_arrays(query, key_pages, value_pages, block_table, context_lens)
         sh = self._shape(query, key_pages, block_table)
         out = np.zeros(query.shape, dtype=np.float64)
-        st = self.lib.oracle_paged_attention(
-            ctypes.byref(sh), _ptr(query), _ptr(key_pages), _ptr(value_pages),
-            block_table.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),
-            context_lens.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),
-            float(scale), int(bool(causal)), out.ctypes.data_as(ctypes.POINTER(ctypes.c_double)),
-            int(num_threads))
+        if mask is None:
+            st = self.lib.oracle_paged_attention(
+                ctypes.byref(sh), _ptr(query), _ptr(key_pages), _ptr(value_pages),
+                block_table.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),
+                context_lens.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),
+                float(scale), int(bool(causal)),
+                out.ctypes.data_as(ctypes.POINTER(ctypes.c_double)), int(num_threads))
+        else:
+            mask = np.ascontiguousarray(mask, dtype=np.float32)
+            B, Hq, L, _ = query.shape
+            assert mask.ndim == 3 and mask.shape[:2] == (B * Hq, L)
+            st = self.lib.oracle_paged_attention_masked(
+                ctypes.byref(sh), _ptr(query), _ptr(key_pages), _ptr(value_pages),
+                block_table.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),
+                context_lens.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),
+                float(scale), int(bool(causal)),
+                mask.ctypes.data_as(ctypes.POINTER(ctypes.c_float)), int(mask.shape[2]),
+                out.ctypes.data_as(ctypes.POINTER(ctypes.c_double)), int(num_threads))
         if st != ORACLE_OK:
             raise OracleError(st)
         return out

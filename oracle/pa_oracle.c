@@ -123,10 +123,14 @@ static void gather_one(const oracle_shape* sh, const void* key_pages, const void
 }
 
 /* One output row (b, h, l) from the gathered K/V of its kv head.
- * x is scratch for S scores, o receives D outputs. */
+ * x is scratch for S scores, o receives D outputs.  mask_row, when not NULL,
+ * is the row's additive mask over logical key positions: it is added to the
+ * scaled score before the softmax ("Week 2 Day 5: Fused Decode Attention",
+ * Task 1: scale, optional mask, causal check).  A row whose every visible
+ * score is -inf has no softmax; its output is 0. */
 static void attend_row(const oracle_shape* sh, const void* query, int b, int h, int l, int S,
-                       const double* K, const double* V, double scale, int causal, double* x,
-                       double* o) {
+                       const double* K, const double* V, double scale, int causal,
+                       const float* mask_row, double* x, double* o) {
     const int D = sh->D, L = sh->L;
     const int64_t qbase = (((int64_t)b * sh->H_q + h) * L + l) * D;
     /* last visible key: s <= l + S - L under causal, s <= S - 1 otherwise */
@@ -148,10 +152,16 @@ static void attend_row(const oracle_shape* sh, const void* query, int b, int h, 
 #else
         x[s] = scale * acc;
 #endif
+#if ORACLE_MUTANT == 9
+        if (mask_row) x[s] -= (double)mask_row[s]; /* planted: mask subtracted */
+#else
+        if (mask_row) x[s] += (double)mask_row[s];
+#endif
         if (x[s] > M) M = x[s];
     }
     double den = 0.0;
     for (int d = 0; d < D; ++d) o[d] = 0.0;
+    if (M == -INFINITY) return; /* every visible key masked out */
     for (int s = 0; s <= last; ++s) {
         const double w = exp(x[s] - M);
 #if ORACLE_MUTANT == 6
@@ -201,10 +211,22 @@ int oracle_paged_attention(const oracle_shape* sh, const void* query, const void
                            const void* value_pages, const int32_t* block_table,
                            const int32_t* context_lens, double scale, int causal,
                            double* out, int num_threads) {
+    return oracle_paged_attention_masked(sh, query, key_pages, value_pages, block_table,
+                                         context_lens, scale, causal, NULL, 0, out, num_threads);
+}
+
+int oracle_paged_attention_masked(const oracle_shape* sh, const void* query,
+                                  const void* key_pages, const void* value_pages,
+                                  const int32_t* block_table, const int32_t* context_lens,
+                                  double scale, int causal, const float* mask, int mask_S,
+                                  double* out, int num_threads) {
     if (!query || !key_pages || !value_pages || !block_table || !context_lens || !out)
         return ORACLE_ERR_INVALID_ARG;
     int st = validate_all(sh, block_table, context_lens, causal);
     if (st) return st;
+    if (mask)
+        for (int b = 0; b < sh->B; ++b)
+            if (context_lens[b] > mask_S) return ORACLE_ERR_INVALID_ARG;
     const int G = sh->H_q / sh->H_kv, D = sh->D;
     const int n_items = sh->B * sh->H_kv;
     int failed = 0;
@@ -225,8 +247,10 @@ int oracle_paged_attention(const oracle_shape* sh, const void* query, const void
             for (int h = 0; h < sh->H_q; ++h) {
                 if (kv_head_of(sh, h) != kvh) continue;
                 for (int l = 0; l < sh->L; ++l)
-                    attend_row(sh, query, b, h, l, S, K, V, scale, causal, x,
-                               out + (((int64_t)b * sh->H_q + h) * sh->L + l) * D);
+                    attend_row(sh, query, b, h, l, S, K, V, scale, causal,
+                               mask ? mask + (((int64_t)b * sh->H_q + h) * sh->L + l) * mask_S
+                                    : NULL,
+                               x, out + (((int64_t)b * sh->H_q + h) * sh->L + l) * D);
             }
         }
         free(K);
@@ -269,7 +293,7 @@ int oracle_paged_attention_rows(const oracle_shape* sh, const void* query,
             failed = 1;
         } else {
             gather_one(sh, key_pages, value_pages, block_table, b, kvh, S, K, V);
-            attend_row(sh, query, b, h, l, S, K, V, scale, causal, x, out + (int64_t)i * D);
+            attend_row(sh, query, b, h, l, S, K, V, scale, causal, NULL, x, out + (int64_t)i * D);
         }
         free(K);
         free(V);

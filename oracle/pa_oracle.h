@@ -62,6 +62,19 @@ int oracle_paged_attention(const oracle_shape* sh, const void* query, const void
                            const int32_t* context_lens, double scale, int causal,
                            double* out, int num_threads);
 
+/* Full attention with an explicit additive mask (fp32) over logical key
+ * positions, laid out [B * H_q, L, mask_S] with mask_S >= every context
+ * length: mask[(b * H_q + h) * L + l][s] is added to the scaled score of key
+ * s for row (b, h, l) before the softmax ("Week 2 Day 5: Fused Decode
+ * Attention", Task 1 normalises explicit masks to [B * H_q, L, S]); the causal
+ * rule still applies when causal != 0.  A row whose every visible score is
+ * -inf outputs 0.  mask == NULL is oracle_paged_attention. */
+int oracle_paged_attention_masked(const oracle_shape* sh, const void* query,
+                                  const void* key_pages, const void* value_pages,
+                                  const int32_t* block_table, const int32_t* context_lens,
+                                  double scale, int causal, const float* mask, int mask_S,
+                                  double* out, int num_threads);
+
 /* The same, for a chosen list of rows only: rows is [n_rows][3] = (b, q_head, l);
  * out is [n_rows, D] double. */
 int oracle_paged_attention_rows(const oracle_shape* sh, const void* query,

@@ -449,8 +449,87 @@ def pin_append_errors(lib):
     assert np.array_equal(kd[0, :, 0:3], bf16_to_f32(kn[0]).astype(np.float64))
 
 
+# ---- explicit additive masks -------------------------------------------------
+# "Week 2 Day 5: Fused Decode Attention", Task 1 normalises explicit masks to
+# [B * H_q, L, S] and keeps the causal flag next to them; the mask is added to
+# the scaled scores before the softmax.  Facts that fix the masked oracle:
+#   * brute force: the dense attention above with the mask added to its logits;
+#   * a zero mask is no mask (bitwise), a per-row constant mask cancels in the
+#     softmax (closed form);
+#   * a mask that lifts one visible key far above the rest gives exactly that
+#     key's value row; a row with every key at -inf outputs 0.
+def _mask_for(c, S_mask, seed, dense=True):
+    rng = np.random.default_rng(seed)
+    m = rng.standard_normal((c.B * c.H_q, c.L, S_mask)).astype(np.float32)
+    if dense:  # knock out a random third of the positions as well
+        m[rng.random(m.shape) < 0.33] = -np.inf
+    return m
+
+
+def _dense_masked(c, mask):
+    G = c.H_q // c.H_kv
+    out = np.zeros((c.B, c.H_q, c.L, c.D))
+    for b in range(c.B):
+        S = int(c.ctx[b])
+        Kr = np.repeat(c.K[b, :, :S], G, axis=0)
+        Vr = np.repeat(c.V[b, :, :S], G, axis=0)
+        scores = np.einsum("hld,hsd->hls", c.q[b], Kr) * c.scale
+        scores = scores + mask[b * c.H_q:(b + 1) * c.H_q, :, :S].astype(np.float64)
+        scores = np.where(visible_mask(c.L, S, c.causal)[None], scores, -np.inf)
+        for h in range(c.H_q):
+            for l in range(c.L):
+                row = scores[h, l]
+                if np.all(row == -np.inf):
+                    continue  # nothing visible: 0
+                P = scipy.special.softmax(row)
+                out[b, h, l] = P @ Vr[h]
+    return out
+
+
+def pin_mask_bruteforce(lib):
+    for seed, B, Hq, Hkv, L, D, ps, ctx, causal, dt in BRUTE_CASES[:5]:
+        c = make_case(seed + 500, B, Hq, Hkv, L, D, ps, ctx, dtype=dt, causal=causal)
+        S_mask = int(max(ctx)) + 3
+        mask = _mask_for(c, S_mask, seed + 600)
+        got = lib.paged_attention(c.q_store, c.kp, c.vp, c.bt, c.ctx, c.scale, c.causal,
+                                  mask=mask)
+        assert_close(got, _dense_masked(c, mask), what=f"masked brute force {seed}")
+
+
+def pin_mask_zero_and_row_constant(lib):
+    c = make_case(701, 2, 4, 2, 3, 16, 4, [11, 6])
+    ref = run_oracle(lib, c)
+    zero = np.zeros((c.B * c.H_q, c.L, 12), dtype=np.float32)
+    got = lib.paged_attention(c.q_store, c.kp, c.vp, c.bt, c.ctx, c.scale, c.causal, mask=zero)
+    assert np.array_equal(got, ref), "a zero mask must be no mask"
+    rowc = np.random.default_rng(702).standard_normal((c.B * c.H_q, c.L, 1)).astype(np.float32)
+    const = np.broadcast_to(rowc * 7, (c.B * c.H_q, c.L, 12)).copy()
+    got = lib.paged_attention(c.q_store, c.kp, c.vp, c.bt, c.ctx, c.scale, c.causal, mask=const)
+    assert_close(got, ref, what="per-row constant mask")
+
+
+def pin_mask_dominant_and_empty_rows(lib):
+    c = make_case(711, 1, 2, 1, 4, 16, 4, [10])
+    mask = np.zeros((2, 4, 10), dtype=np.float32)
+    j = 3  # visible to every row (rows see keys 0..6+l)
+    mask[:, :, j] = 800.0
+    got = lib.paged_attention(c.q_store, c.kp, c.vp, c.bt, c.ctx, c.scale, True, mask=mask)
+    for h in range(2):
+        for l in range(4):
+            assert_close(got[0, h, l], c.V[0, 0, j], what="dominant masked key")
+    mask = np.zeros((2, 4, 10), dtype=np.float32)
+    mask[1, 2, :] = -np.inf  # every key of row (h=1, l=2)
+    got = lib.paged_attention(c.q_store, c.kp, c.vp, c.bt, c.ctx, c.scale, True, mask=mask)
+    assert np.array_equal(got[0, 1, 2], np.zeros(16)), "a fully masked row outputs 0"
+    ref = run_oracle(lib, c)
+    keep = np.ones((2, 4), dtype=bool)
+    keep[1, 2] = False
+    assert np.array_equal(got[0][keep], ref[0][keep])
+
+
 ALL_PINS = [pin_bruteforce, pin_torch_sdpa, pin_page_permutation, pin_unused_table_entries,
             pin_tile_size_invariance, pin_single_page, pin_one_hot, pin_uniform_visible_mean,
             pin_gqa_equals_repeat, pin_gather, pin_errors, pin_rows_api,
             pin_append_dense_slice, pin_append_page_permutation, pin_append_touches_only_new_rows,
-            pin_append_errors]
+            pin_append_errors, pin_mask_bruteforce, pin_mask_zero_and_row_constant,
+            pin_mask_dominant_and_empty_rows]

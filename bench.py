@@ -7,6 +7,7 @@ Prints ONE JSON line.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                   [--workload decode|prefill|tails|long_decode|tiny] [--op attention|append]
+                  [--no-causal] [--mask]
 
 Default workload: batched decode, B=64, L=1, H_q=32, H_kv=8, D=128,
 page_size=128, context lengths U{128..4096}, scattered pages (seeded).
@@ -14,6 +15,14 @@ Metric: achieved HBM GB/s = algorithmic bytes / device time (bf16).
 
 --impl reference times the fp64 CPU oracle on the host cores over a bounded
 sample of the same workload (the method has no other reference program).
+
+--no-causal runs the workload with mask=None (every key of the context visible)
+instead of the causal rule.
+
+--mask adds a seeded fp32 additive mask [B * H_q, L, S_mask] (N(0,1) biases,
+a third of the positions at -inf) to every call; the mask read makes every
+workload HBM-bound, so the line is in GB/s with the visible mask bytes
+counted.
 
 --op append measures the K/V append instead (pa_append_kv: the workload's L
 new tokens per sequence written into their pages), in HBM GB/s.
@@ -40,6 +49,7 @@ if ROOT not in sys.path:
 from paged_kv_cache_03_gb300 import synth  # noqa: E402
 
 METRIC = "paged-attn decode HBM GB/s & prefill TFLOP/s vs GB300 roofline (bf16, d128)"
+METRIC_MASKED = "paged-attn with an fp32 additive mask, HBM GB/s (bf16, d128)"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 L2_FLUSH_BYTES = 256 << 20
 
@@ -80,6 +90,19 @@ def algorithmic_flops(inp) -> int:
     return 4 * inp.H_q * inp.D * visible_pairs(inp)
 
 
+def mask_bytes(inp) -> int:
+    """Bytes of an fp32 additive mask a call must read: one element per
+    visible (query row, key) pair of every query head."""
+    return 4 * inp.H_q * visible_pairs(inp)
+
+
+def mask_width(inp) -> int:
+    """S_mask of the benchmarked masks: the block table's capacity rounded up
+    to a multiple of 4."""
+    cap = inp.block_table.shape[1] * inp.page_size
+    return (cap + 3) // 4 * 4
+
+
 def append_bytes(inp) -> int:
     """Minimum bytes one K/V append moves: the new K and V rows read once and
     written once into the pool (2 tensors x 2 x B*H_kv*L*D*elt), the
@@ -102,6 +125,18 @@ def workload_desc(name, inp) -> str:
     return (f"{name}: B={inp.B} L={inp.L} H_q={inp.H_q} H_kv={inp.H_kv} D={inp.D} "
             f"page_size={inp.page_size} pool={inp.num_pages} pages {ctx} "
             f"{'causal' if inp.causal else 'full'}{ks} seed={kw['seed']}")
+
+
+def bench_inputs(args):
+    """The named workload, with every key before the frontier visible
+    (mask=None) under --no-causal."""
+    return synth.workload(args.workload, **({"causal": False} if args.no_causal else {}))
+
+
+def variant(args) -> str:
+    """Workload key of the recorded traffic: the workload name, +full for
+    --no-causal, +mask for --mask."""
+    return args.workload + ("+full" if args.no_causal else "") + ("+mask" if args.mask else "")
 
 
 def load_peaks():
@@ -266,18 +301,20 @@ def sub_batch(inp, n):
                              inp.scale, inp.causal, inp.dtype, inp.name)
 
 
-def time_oracle(inp, target_s: float, unit_fn):
+def time_oracle(inp, target_s: float, unit_fn, mask_fn=None):
     """Runs the oracle on growing leading sub-batches until one run takes
-    about target_s; returns (units/s, seconds, description, threads)."""
+    about target_s; returns (units/s, seconds, description, threads).
+    mask_fn(n), if given, returns the additive mask of the first n sequences."""
     import oracle
     lib = oracle.load()
     cores = oracle.host_cores()
     n = 1
     while True:
         sub = sub_batch(inp, n)
+        m = mask_fn(n) if mask_fn else None
         t0 = time.perf_counter()
         lib.paged_attention(sub.query, sub.key_pages, sub.value_pages, sub.block_table,
-                            sub.context_lens, sub.scale, sub.causal, num_threads=cores)
+                            sub.context_lens, sub.scale, sub.causal, num_threads=cores, mask=m)
         dt = time.perf_counter() - t0
         if dt >= target_s or n >= inp.B:
             break
@@ -300,9 +337,9 @@ def run_ours(args):
     torch.cuda.set_device(device)
     B.load()
 
-    inp = synth.workload(args.workload)
-    bound = WORKLOAD_BOUND[args.workload]
-    bytes_step = algorithmic_bytes(inp)
+    inp = bench_inputs(args)
+    bound = "hbm" if args.mask else WORKLOAD_BOUND[args.workload]
+    bytes_step = algorithmic_bytes(inp) + (mask_bytes(inp) if args.mask else 0)
     flops_step = algorithmic_flops(inp)
     es = 2 if inp.dtype == "bf16" else 4
     tdt = torch.bfloat16 if inp.dtype == "bf16" else torch.float32
@@ -327,10 +364,25 @@ def run_ours(args):
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
     dominant = {B.PA_SCHED_DECODE: "decode_split_kernel",
                 B.PA_SCHED_PREFILL: "prefill_tile_kernel"}[sched]
+    mask = None
+    if args.mask:
+        mask = synth.additive_mask_device(inp.B * inp.H_q, inp.L, mask_width(inp), 4343, device)
+        torch.cuda.empty_cache()  # the draw's temporaries
 
     def call(ev0=None, ev1=None):
-        st = B.pa_paged_attention_profiled(shape, q, kp, vp, bt, ctx, inp.scale, inp.causal, out,
-                                           ws, ws.numel(), stream, sched, ev0, ev1)
+        if mask is None:
+            st = B.pa_paged_attention_profiled(
+                shape, q, kp, vp, bt, ctx, inp.scale, inp.causal, out, ws, ws.numel(), stream,
+                sched, ev0.cuda_event if ev0 is not None else None,
+                ev1.cuda_event if ev1 is not None else None)
+        else:  # the masked entry has no kernel events: the whole call is timed
+            if ev0 is not None:
+                ev0.record(stream)
+            st = B.pa_paged_attention_masked(shape, q, kp, vp, bt, ctx, inp.scale, inp.causal,
+                                             mask, mask.shape[2], out, ws, ws.numel(), stream,
+                                             sched)
+            if ev1 is not None:
+                ev1.record(stream)
         if st != B.PA_OK:
             raise RuntimeError(f"pa_paged_attention: {B.status_str(st)}")
 
@@ -359,7 +411,7 @@ def run_ours(args):
         flush.zero_()  # L2 flush between timed steps (outside the step's events)
         e = ev[k]
         e[0].record(stream)
-        call(e[1].cuda_event, e[2].cuda_event)
+        call(e[1], e[2])
         e[3].record(stream)
     torch.cuda.synchronize(device)
     barrier(device)
@@ -390,8 +442,10 @@ def run_ours(args):
         runit = "GB/s"
     roofline = {"bound": bound, "achieved": round(achieved, 2), "peak": peak, "unit": runit,
                 "frac": round(achieved / peak, 4), "traffic": recorded_traffic(
-                    dominant, args.workload),
-                "kernel": dominant, "kernel_ms_avg": round(float(kern_ms.mean()), 5),
+                    dominant, variant(args)),
+                "kernel": dominant + (" (whole call)" if mask is not None and launches > 1
+                                      else ""),
+                "kernel_ms_avg": round(float(kern_ms.mean()), 5),
                 "kernel_ms_median": round(float(np.median(kern_ms)), 5),
                 "peak_source": f"{peaks_src} (MEASURED_PEAKS.json)" if peaks_src == "measured"
                 else "fallback", "algorithmic_bytes": bytes_step,
@@ -407,6 +461,9 @@ def run_ours(args):
         out_host = torch.empty(out.shape, dtype=tdt).pin_memory()
         dst = {"query": q, "key_pages": kp, "value_pages": vp, "block_table": bt,
                "context_lens": ctx}
+        if mask is not None:
+            host["mask"] = mask.cpu().pin_memory()
+            dst["mask"] = mask
         h2d = sum(t.numel() * t.element_size() for t in host.values())
         d2h = out.numel() * out.element_size()
         Ke = max(3, min(args.e2e_steps, K))
@@ -416,8 +473,13 @@ def run_ours(args):
                 d = dst[n]
                 d.view(torch.uint8).view(-1).copy_(t.view(torch.uint8).view(-1),
                                                    non_blocking=True)
-            st = B.pa_paged_attention(shape, q, kp, vp, bt, ctx, inp.scale, inp.causal, out, ws,
-                                      ws.numel(), stream)
+            if mask is None:
+                st = B.pa_paged_attention(shape, q, kp, vp, bt, ctx, inp.scale, inp.causal, out,
+                                          ws, ws.numel(), stream)
+            else:
+                st = B.pa_paged_attention_masked(shape, q, kp, vp, bt, ctx, inp.scale,
+                                                 inp.causal, mask, mask.shape[2], out, ws,
+                                                 ws.numel(), stream)
             if st != B.PA_OK:
                 raise RuntimeError(B.status_str(st))
             out_host.copy_(out, non_blocking=True)
@@ -442,10 +504,12 @@ def run_ours(args):
                "d2h_bytes_per_step": int(d2h), "steps": Ke,
                "ms_per_step": round(e2e_ms / Ke, 4),
                "note": "pinned host inputs (query, both page pools, block table, context "
-                       "lengths) copied to HBM, one call, output copied back, every step"}
+                       "lengths" + (", mask" if mask is not None else "") + ") copied to HBM, "
+                       "one call, output copied back, every step"}
 
     line = {
-        "metric": METRIC, "value": round(value, 3), "unit": value_unit, "n_gpus": world,
+        "metric": METRIC_MASKED if mask is not None else METRIC, "value": round(value, 3),
+        "unit": value_unit, "n_gpus": world,
         "steps": K, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": inp.dtype,
         "data": "synthetic (seeded N(0,1) bf16, scattered pages)",
@@ -454,7 +518,10 @@ def run_ours(args):
                    "l2": "flushed: 256 MiB write between timed steps (outside step events)",
                    "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
                    "algorithmic_bytes_per_step": bytes_step,
-                   "algorithmic_flops_per_step": flops_step},
+                   "algorithmic_flops_per_step": flops_step,
+                   **({"mask": f"fp32 [B*H_q, L, {mask.shape[2]}], N(0,1) biases, 1/3 -inf, "
+                               f"seed 4343 (device draw); {mask_bytes(inp)} visible bytes"}
+                      if mask is not None else {})},
         "clocks": clocks, "e2e": e2e, "gpu_launches": K * launches, "roofline": roofline,
         "step_ms_median": round(float(np.median(step_ms)), 5),
         "wall_s_timed_region": round(wall, 3),
@@ -462,7 +529,11 @@ def run_ours(args):
     if rank == 0 and not args.no_cpu_baseline:
         unit_fn = (lambda s: algorithmic_flops(s) / 1e12) if bound == "tensor" else (
             lambda s: algorithmic_bytes(s) / 1e9)
-        v, secs, desc, cores = time_oracle(inp, args.cpu_seconds, unit_fn)
+        mask_fn = None
+        if mask is not None:
+            unit_fn = lambda s: (algorithmic_bytes(s) + mask_bytes(s)) / 1e9  # noqa: E731
+            mask_fn = lambda n: mask[:n * inp.H_q].cpu().numpy()  # noqa: E731
+        v, secs, desc, cores = time_oracle(inp, args.cpu_seconds, unit_fn, mask_fn)
         line["cpu_baseline"] = {"value": round(v, 6), "unit": value_unit, "cores": cores,
                                 "kind": "oracle", "sample": desc, "seconds": round(secs, 3)}
     if rank == 0:
@@ -614,7 +685,7 @@ def run_reference(args):
     import oracle
     lib = oracle.load()
     cores = oracle.host_cores()
-    inp = synth.workload(args.workload)
+    inp = bench_inputs(args)
     bound = WORKLOAD_BOUND[args.workload]
     unit_fn = (lambda s: algorithmic_flops(s) / 1e12) if bound == "tensor" else (
         lambda s: algorithmic_bytes(s) / 1e9)
@@ -670,6 +741,10 @@ def main(argv=None):
     ap.add_argument("--workload", choices=sorted(synth.WORKLOADS), default="decode")
     ap.add_argument("--op", choices=["attention", "append"], default="attention",
                     help="the path (paged attention) or the K/V append before it")
+    ap.add_argument("--no-causal", action="store_true",
+                    help="every key of the context visible (mask=None) instead of causal")
+    ap.add_argument("--mask", action="store_true",
+                    help="add a seeded fp32 additive mask to every call (attention only)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -686,6 +761,10 @@ def main(argv=None):
             return None
         return run_append(args)
     if args.impl == "reference":
+        if args.mask:
+            print(json.dumps({"impl": "reference", "unavailable":
+                              "the masked arm's reference is its oracle: see cpu_baseline"}))
+            return None
         return run_reference(args)
     return run_ours(args)
 

@@ -119,6 +119,24 @@ pa_status pa_paged_attention_profiled(const pa_shape* shape, const void* query,
                                       size_t workspace_bytes, void* cuda_stream, int schedule,
                                       void* event_before, void* event_after);
 
+/* pa_paged_attention_sched with an explicit additive mask: the pages
+ * normalise explicit masks to [B * H_q, L, S] and keep the causal flag next to
+ * them ("Week 2 Day 5: Fused Decode Attention", Task 1).  mask is an fp32
+ * device array [B * H_q, L, mask_S] over logical key positions, 16-byte
+ * aligned, mask_S a multiple of 4 and at least max_pages_per_seq * page_size;
+ * mask[(b * H_q + h) * L + l][s] is added to the scaled score of key s for
+ * row (b, h, l) before the softmax, and the causal rule still applies when
+ * causal != 0.  -inf removes a key; a row whose every visible key is removed
+ * outputs 0.  Both schedules take it; every mask element a row can see is
+ * read once.  Returns PA_ERR_INVALID_ARG for a null or misaligned mask or a
+ * bad mask_S, otherwise as pa_paged_attention_sched. */
+pa_status pa_paged_attention_masked(const pa_shape* shape, const void* query,
+                                    const void* key_pages, const void* value_pages,
+                                    const int32_t* block_table, const int32_t* context_lens,
+                                    float scale, int causal, const float* mask,
+                                    long long mask_S, void* out, void* workspace,
+                                    size_t workspace_bytes, void* cuda_stream, int schedule);
+
 /* Debug gather of "Week 3 Day 5", Task 1: writes the dense history of every
  * (b, kv_head) through the block table, k_dense/v_dense [B, H_kv, max_S, D]
  * in the pool's dtype, zeros at s >= context_lens[b].  Page translation is

@@ -98,6 +98,10 @@ def load(auto_build: bool = True):
         lib.pa_choose_schedule.restype = ctypes.c_int
         lib.pa_launch_count.argtypes = [sp, ctypes.c_int]
         lib.pa_launch_count.restype = ctypes.c_int
+        lib.pa_paged_attention_masked.argtypes = [sp, vp, vp, vp, i32p, i32p, ctypes.c_float,
+                                                  ctypes.c_int, vp, ctypes.c_longlong, vp, vp,
+                                                  sz, vp, ctypes.c_int]
+        lib.pa_paged_attention_masked.restype = ctypes.c_int
         lib.pa_append_kv.argtypes = [sp, vp, vp, vp, vp, i32p, i32p, vp, sz, vp]
         lib.pa_append_kv.restype = ctypes.c_int
         lib.pa_status_str.argtypes = [ctypes.c_int]
@@ -205,6 +209,16 @@ def pa_gather_debug(shape, key_pages, value_pages, block_table, context_lens, ma
         _stream(stream))
 
 
+def pa_paged_attention_masked(shape, query, key_pages, value_pages, block_table, context_lens,
+                              scale, causal, mask, mask_S, out, workspace, workspace_bytes,
+                              stream=None, schedule=PA_SCHED_AUTO) -> int:
+    """mask: fp32 device tensor [B * H_q, L, mask_S] added to the scaled scores."""
+    return load().pa_paged_attention_masked(
+        ctypes.byref(shape), _ptr(query), _ptr(key_pages), _ptr(value_pages), _ptr(block_table),
+        _ptr(context_lens), float(scale), int(bool(causal)), _ptr(mask), int(mask_S), _ptr(out),
+        _ptr(workspace), int(workspace_bytes), _stream(stream), int(schedule))
+
+
 def pa_append_kv(shape, k_new, v_new, key_pages, value_pages, block_table, context_lens,
                  workspace, workspace_bytes, stream=None) -> int:
     return load().pa_append_kv(
@@ -245,10 +259,12 @@ def new_workspace(shape: pa_shape, device=None):
 
 
 def paged_attention(query, key_pages, value_pages, block_table, context_lens, page_size,
-                    scale=None, causal=True, *, out=None, workspace=None,
+                    scale=None, causal=True, *, mask=None, out=None, workspace=None,
                     schedule=PA_SCHED_AUTO, stream=None):
-    """out[B, H_q, L, D] = softmax(scale * q.K^T over visible keys) . V, with
-    K/V read from the paged pool through block_table."""
+    """out[B, H_q, L, D] = softmax(scale * q.K^T + mask over visible keys) . V,
+    with K/V read from the paged pool through block_table.  mask: optional
+    fp32 CUDA tensor [B * H_q, L, S_mask] (S_mask >= the table's capacity, a
+    multiple of 4) added to the scaled scores."""
     import torch
     shape = shape_of(query, key_pages, block_table)
     if shape.page_size != int(page_size):
@@ -265,9 +281,18 @@ def paged_attention(query, key_pages, value_pages, block_table, context_lens, pa
         out = torch.empty_like(query)
     if workspace is None:
         workspace = new_workspace(shape, query.device)
-    st = pa_paged_attention_sched(shape, query, key_pages, value_pages, block_table,
-                                  context_lens, scale, causal, out, workspace,
-                                  workspace.numel(), stream, schedule)
+    if mask is None:
+        st = pa_paged_attention_sched(shape, query, key_pages, value_pages, block_table,
+                                      context_lens, scale, causal, out, workspace,
+                                      workspace.numel(), stream, schedule)
+    else:
+        if mask.dtype != torch.float32 or not mask.is_cuda or not mask.is_contiguous():
+            raise ValueError("mask must be a contiguous fp32 CUDA tensor")
+        if mask.dim() != 3 or mask.shape[0] != shape.B * shape.H_q or mask.shape[1] != shape.L:
+            raise ValueError("mask must be [B * H_q, L, S_mask]")
+        st = pa_paged_attention_masked(shape, query, key_pages, value_pages, block_table,
+                                       context_lens, scale, causal, mask, mask.shape[2], out,
+                                       workspace, workspace.numel(), stream, schedule)
     if st != PA_OK:
         raise PagedAttentionError(st, "pa_paged_attention")
     return out

@@ -81,7 +81,7 @@ pa_status run(const pa_shape* shape, const void* query, const void* key_pages,
               const void* value_pages, const int32_t* block_table, const int32_t* context_lens,
               float scale, int causal, void* out, void* workspace, size_t workspace_bytes,
               void* cuda_stream, int schedule, void* ev_before = nullptr,
-              void* ev_after = nullptr) {
+              void* ev_after = nullptr, const float* mask = nullptr, long long mask_S = 0) {
     pa_status st = check_shape(shape);
     if (st != PA_OK) return st;
     if (!query || !key_pages || !value_pages || !block_table || !context_lens || !out)
@@ -110,6 +110,8 @@ pa_status run(const pa_shape* shape, const void* query, const void* key_pages,
     c.stream = static_cast<cudaStream_t>(cuda_stream);
     c.ev_before = static_cast<cudaEvent_t>(ev_before);
     c.ev_after = static_cast<cudaEvent_t>(ev_after);
+    c.mask = mask;
+    c.mask_S = mask_S;
     st = current_device_info(&c.dev);
     if (st != PA_OK) return st;
     if (c.dev.cc_major != 10 || c.dev.cc_minor != 3) return PA_ERR_UNSUPPORTED;
@@ -157,6 +159,22 @@ pa_status pa_paged_attention_profiled(const pa_shape* shape, const void* query,
                                       void* event_before, void* event_after) {
     return run(shape, query, key_pages, value_pages, block_table, context_lens, scale, causal,
                out, workspace, workspace_bytes, cuda_stream, schedule, event_before, event_after);
+}
+
+pa_status pa_paged_attention_masked(const pa_shape* shape, const void* query,
+                                    const void* key_pages, const void* value_pages,
+                                    const int32_t* block_table, const int32_t* context_lens,
+                                    float scale, int causal, const float* mask,
+                                    long long mask_S, void* out, void* workspace,
+                                    size_t workspace_bytes, void* cuda_stream, int schedule) {
+    pa_status st = check_shape(shape);
+    if (st != PA_OK) return st;
+    if (!mask || !aligned(mask, 16)) return PA_ERR_INVALID_ARG;
+    const long long cap = static_cast<long long>(shape->max_pages_per_seq) * shape->page_size;
+    if (mask_S < cap || mask_S % 4 != 0) return PA_ERR_INVALID_ARG;
+    return run(shape, query, key_pages, value_pages, block_table, context_lens, scale, causal,
+               out, workspace, workspace_bytes, cuda_stream, schedule, nullptr, nullptr, mask,
+               mask_S);
 }
 
 pa_status pa_gather_debug(const pa_shape* shape, const void* key_pages, const void* value_pages,

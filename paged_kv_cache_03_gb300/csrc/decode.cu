@@ -69,6 +69,8 @@ struct DecodeParams {
     long long max_S;
     float scale_log2;
     int tk_pages, tk_slots;  // a full tile of TK keys spans TK / ps pages + TK % ps slots
+    const float* mask;       // optional additive mask [B * H_q, L, mask_S], or null
+    long long mask_S;
 };
 
 template <typename T, int RB_, int P_, int TK_, int NCW_, int NST_, int MINB_ = 1, int GRAN_ = 0>
@@ -482,6 +484,17 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB) decode_split_kernel(const
                 if (any_bad) atomicOr(p.flag, PA_FLAG_BAD_PAGE);
             }
 
+            // the explicit mask's rows of this tile go to L2 now, NST stages
+            // before the consumers read them: [key0, key0 + nvalid) widened to
+            // whole 16-byte words, inside the row (mask_S % 4 == 0, >= S)
+            if (p.mask && lane < nrows && nvalid > 0) {
+                const int rg = row0 + lane, gq = rg / p.L, lq = rg - gq * p.L;
+                const int lo = w.key0 & ~3, hi = (w.key0 + nvalid + 3) & ~3;
+                bulk_prefetch_l2(p.mask + ((static_cast<long long>(w.b) * p.H_q +
+                                            w.kvh * p.G + gq) * p.L + lq) * p.mask_S + lo,
+                                 static_cast<uint32_t>(hi - lo) * 4u);
+            }
+
             const int stage = i % C::NST;
             const uint32_t fb = full0 + 8 * stage, eb = empty0 + 8 * stage;
             if (i >= C::NST &&
@@ -647,6 +660,22 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB) decode_split_kernel(const
         if (h.nvalid > kw0) {
             const uint8_t* const Ks = st + C::HDR + C::QBYTES;
             const uint8_t* const Vs = Ks + C::KBYTES;
+            // An explicit additive mask joins the score of (key, row) in log2
+            // units before the max; its loads go out before the dot products.
+            float mv[C::IT];
+            if (p.mask) {
+                const int rg = h.chunk * C::RB + rho;  // row of the (b, kv head) block
+                const bool rok = rg < p.G * p.L;
+                const int gq = rg / p.L, lq = rg - gq * p.L;
+                const float* mrow = p.mask + ((static_cast<long long>(h.b) * p.H_q +
+                                               h.kvh * p.G + gq) * p.L + lq) * p.mask_S +
+                                    h.key0;
+#pragma unroll
+                for (int it = 0; it < C::IT; ++it) {
+                    const int kl = kw0 + it * C::KPI + grp;
+                    mv[it] = rok && kl < h.nvalid ? __ldcs(mrow + kl) : 0.f;
+                }
+            }
             float sc[C::IT];  // score of (this group's key of iteration it, row rho)
 #pragma unroll
             for (int it = 0; it < C::IT; ++it) {
@@ -662,6 +691,10 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB) decode_split_kernel(const
                     d[r] = acc.x + acc.y;
                 }
                 sc[it] = transpose_reduce<C::RB, C::P>(d, li);
+            }
+            if (p.mask) {
+#pragma unroll
+                for (int it = 0; it < C::IT; ++it) sc[it] += mv[it] * 1.4426950408889634f;
             }
             // Score mask (the separate "second mask" of a masked load): keys
             // past the context or past a row's causal frontier get -inf.
@@ -940,6 +973,8 @@ pa_status launch_cfg(const Call& c) {
     p.causal = c.causal ? 1 : 0;
     p.max_S = static_cast<long long>(sh.max_pages_per_seq) * sh.page_size;
     p.scale_log2 = c.scale * 1.4426950408889634f;
+    p.mask = c.mask;
+    p.mask_S = c.mask_S;
     p.tk_pages = C::TK / sh.page_size;
     p.tk_slots = C::TK % sh.page_size;
 

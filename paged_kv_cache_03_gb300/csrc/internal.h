@@ -42,6 +42,10 @@ struct Call {
     cudaStream_t stream;
     cudaEvent_t ev_before = nullptr;  // recorded around the dominant kernel
     cudaEvent_t ev_after = nullptr;
+    // optional additive mask [B * H_q, L, mask_S] (fp32), mask_S >= the table's
+    // capacity and a multiple of 4
+    const float* mask = nullptr;
+    long long mask_S = 0;
     DeviceInfo dev;
 };
 

@@ -88,6 +88,8 @@ struct PrefillParams {
     int B, H_q, H_kv, L, G, Lt, nM, nPairs, num_pages, ps, max_npg, box_rows, causal;
     long long max_S;
     float scale_log2;
+    const float* mask;  // optional additive mask [B * H_q, L, mask_S], or null
+    long long mask_S;   // >= the table's capacity, a multiple of 4
 };
 
 __device__ __forceinline__ float neg_inf() { return __int_as_float(0xff800000); }
@@ -160,6 +162,9 @@ __device__ __forceinline__ void exp_pack(const float (&x)[4][32], float2 c2, flo
     }
 }
 
+// kMask: an explicit additive mask is read (a separate instantiation, so the
+// unmasked kernel carries none of its code or registers).
+template <bool kMask>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tile_kernel(const __grid_constant__ CUtensorMap tm_q,
                         const __grid_constant__ CUtensorMap tm_k,
@@ -370,10 +375,31 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int lim = min(p.causal ? l + S - p.L : S - 1, S - 1);
         const int nkt = nk_t[t];
         const float c = p.scale_log2;
+        // with an explicit mask the scores are taken to log2 units (and the
+        // mask added) right after the load, so the rest scales by 1
+        const float cs = kMask ? 1.f : c;
+        const float* const mask_row =
+            kMask && row_valid
+                ? p.mask + ((static_cast<long long>(b) * p.H_q + h) * p.L + l) * p.mask_S
+                : nullptr;
+        // the lines holding this row's visible mask entries of key tile jj go
+        // to L2 ahead of use: keys [jj * BN, min(jj * BN + BN, lim + 1)), all
+        // inside the row (lim < S <= mask_S)
+        auto prefetch_mask = [&](int jj) {
+            if (!kMask || !mask_row || jj >= nkt) return;
+            const int k0 = jj * BN;
+            if (k0 > lim) return;
+            const int k1 = min(k0 + BN, lim + 1) - 1;  // last visible key of the tile
+#pragma unroll
+            for (int e = 0; e < 4; ++e) prefetch_l2(mask_row + min(k0 + 32 * e, k1));
+            prefetch_l2(mask_row + k1);
+        };
+        prefetch_mask(0);
         float mrow = neg_inf();
         float2 lsum2 = make_float2(0.f, 0.f);
         bool ok = true;
         for (int j = 0; j < nkt; ++j) {
+            prefetch_mask(j + 1);
             ok = warp_wait(bar(kSFull + t), j & 1);
             if (!ok || aborted(abort_flag)) break;
             tc::fence_after_sync();
@@ -381,6 +407,21 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int cc = 0; cc < 4; ++cc) tc::ld32(trow + col_s(t) + cc * 32, x[cc]);
             tc::wait_ld();
+            if constexpr (kMask) {  // s * scale * log2 e + mask * log2 e
+                // only the words holding a visible key (k0 + 4q <= lim < mask_S)
+                const int k0 = j * BN;
+#pragma unroll
+                for (int q = 0; q < 32; ++q) {
+                    float4 mv = make_float4(0.f, 0.f, 0.f, 0.f);
+                    if (mask_row && k0 + 4 * q <= lim)
+                        mv = __ldg(reinterpret_cast<const float4*>(mask_row + k0) + q);
+                    const int cc = q >> 3, e = (q & 7) * 4;
+                    x[cc][e + 0] = fmaf(x[cc][e + 0], c, mv.x * 1.4426950408889634f);
+                    x[cc][e + 1] = fmaf(x[cc][e + 1], c, mv.y * 1.4426950408889634f);
+                    x[cc][e + 2] = fmaf(x[cc][e + 2], c, mv.z * 1.4426950408889634f);
+                    x[cc][e + 3] = fmaf(x[cc][e + 3], c, mv.w * 1.4426950408889634f);
+                }
+            }
             // causal / length mask (frontier tiles only), row max of raw scores
             const bool masking = j * BN + BN - 1 > lim_min_t[t];  // uniform over the CTA
             if (masking) {
@@ -400,7 +441,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mq[cc] = fmaxf(mq[cc], x[cc][31]);
             }
             float mt = fmax3(mq[0], mq[1], fmaxf(mq[2], mq[3]));
-            mt *= c;
+            mt *= cs;
             const bool grow = mt > mrow + kLazyRescaleLog2;
             const bool any_grow = __any_sync(0xffffffffu, grow);
             const float mn = grow ? mt : mrow;
@@ -408,7 +449,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mrow = mn;
             // P = 2^(s*c - m) packed to bf16 pairs in registers, before any wait
             const float mu = (mrow == neg_inf()) ? 0.f : mrow;
-            const float2 c2 = make_float2(c, c), nm2 = make_float2(-mu, -mu);
+            const float2 c2 = make_float2(cs, cs), nm2 = make_float2(-mu, -mu);
             float2 ts = make_float2(0.f, 0.f);
             uint32_t pw[64];
             exp_pack(x, c2, nm2, pw, ts);
@@ -579,7 +620,11 @@ pa_status prefill_launch(const Call& c) {
 
     static int attr_done[64] = {0};
     if (c.dev.device >= 0 && c.dev.device < 64 && !attr_done[c.dev.device]) {
-        if (cudaFuncSetAttribute(prefill_tile_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        if (cudaFuncSetAttribute(prefill_tile_kernel<false>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kSmemBytes) != cudaSuccess ||
+            cudaFuncSetAttribute(prefill_tile_kernel<true>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  kSmemBytes) != cudaSuccess)
             return PA_ERR_CUDA;
         attr_done[c.dev.device] = 1;
@@ -604,9 +649,14 @@ pa_status prefill_launch(const Call& c) {
     p.causal = c.causal ? 1 : 0;
     p.max_S = static_cast<long long>(sh.max_pages_per_seq) * sh.page_size;
     p.scale_log2 = c.scale * 1.4426950408889634f;
+    p.mask = c.mask;
+    p.mask_S = c.mask_S;
     const unsigned grid = static_cast<unsigned>(static_cast<long long>(p.nPairs) * sh.H_kv * sh.B);
     if (c.ev_before && cudaEventRecord(c.ev_before, c.stream) != cudaSuccess) return PA_ERR_CUDA;
-    prefill_tile_kernel<<<grid, kThreads, kSmemBytes, c.stream>>>(tq, tk, tv, p);
+    if (c.mask)
+        prefill_tile_kernel<true><<<grid, kThreads, kSmemBytes, c.stream>>>(tq, tk, tv, p);
+    else
+        prefill_tile_kernel<false><<<grid, kThreads, kSmemBytes, c.stream>>>(tq, tk, tv, p);
     if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
     if (c.ev_after && cudaEventRecord(c.ev_after, c.stream) != cudaSuccess) return PA_ERR_CUDA;
     return PA_OK;

@@ -93,6 +93,17 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
         : "memory");
 }
 
+// Bulk prefetch of global memory into L2 (no completion to wait for).
+// src and bytes must be multiples of 16.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
+// Prefetch of the global-memory line holding addr into L2 (LSU path).
+__device__ __forceinline__ void prefetch_l2(const void* addr) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(addr));
+}
+
 // Programmatic dependent launch: let the next kernel in the stream start its
 // prologue / make this kernel wait for the previous one's memory.
 __device__ __forceinline__ void pdl_launch_dependents() {

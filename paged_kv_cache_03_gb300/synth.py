@@ -157,3 +157,24 @@ def new_kv(B: int, H_kv: int, L: int, D: int, seed: int, dtype: str = "bf16"):
     each (bf16 bit patterns or fp32), for the K/V append."""
     rng = np.random.default_rng(seed)
     return _normal(rng, (B, H_kv, L, D), dtype), _normal(rng, (B, H_kv, L, D), dtype)
+
+
+def additive_mask(rows: int, L: int, S_mask: int, seed: int, removed: float = 1.0 / 3.0):
+    """Seeded fp32 additive mask [rows, L, S_mask] (rows = B * H_q): N(0,1)
+    biases, a `removed` fraction of the positions at -inf."""
+    rng = np.random.default_rng(seed)
+    m = rng.standard_normal((rows, L, S_mask), dtype=np.float32)
+    m[rng.random(m.shape) < removed] = -np.inf
+    return m
+
+
+def additive_mask_device(rows: int, L: int, S_mask: int, seed: int, device,
+                         removed: float = 1.0 / 3.0):
+    """additive_mask's recipe (N(0,1) biases, a `removed` fraction at -inf)
+    drawn on a CUDA device with torch's seeded generator, for the gigabyte
+    masks of the full-size workloads; the values differ from additive_mask's."""
+    import torch
+    g = torch.Generator(device=device).manual_seed(seed)
+    m = torch.randn((rows, L, S_mask), generator=g, device=device, dtype=torch.float32)
+    drop = torch.rand((rows, L, S_mask), generator=g, device=device) < removed
+    return m.masked_fill_(drop, float("-inf"))

@@ -96,6 +96,10 @@ class OracleLib:
             sp, vp, vp, vp, ip, ip, ctypes.c_double, ctypes.c_int, fp, ctypes.c_int, dp,
             ctypes.c_int]
         self.lib.oracle_paged_attention_masked.restype = ctypes.c_int
+        self.lib.oracle_paged_attention_varlen.argtypes = [
+            sp, vp, vp, vp, ip, ip, ip, ctypes.c_int, ctypes.c_double, ctypes.c_int, dp,
+            ctypes.c_int]
+        self.lib.oracle_paged_attention_varlen.restype = ctypes.c_int
         self.lib.oracle_append_kv.argtypes = [sp, vp, vp, vp, vp, ip, ip]
         self.lib.oracle_append_kv.restype = ctypes.c_int
 
@@ -182,6 +186,37 @@ class OracleLib:
             raise OracleError(st)
         return k, v
 
+
+    def paged_attention_varlen(self, query, key_pages, value_pages, block_table, context_lens,
+                               cu_q, scale: float, causal: bool, max_L: int | None = None,
+                               num_threads: int = 0) -> np.ndarray:
+        """Ragged batch: query [total_q, H_q, D] packed by token, cu_q [B + 1]
+        query offsets (sequence b owns tokens cu_q[b] .. cu_q[b+1]-1, the
+        last positions of its context); returns [total_q, H_q, D] float64."""
+        cu_q = np.ascontiguousarray(cu_q, dtype=np.int32)
+        self._check_arrays(query, key_pages, value_pages, block_table, context_lens)
+        P, H_kv, ps, D = key_pages.shape
+        T, Hq, Dq = query.shape
+        assert Dq == D
+        B = block_table.shape[0]
+        assert cu_q.shape == (B + 1,) and context_lens.shape == (B,)
+        lens = np.diff(cu_q)
+        if max_L is None:
+            max_L = max(1, int(lens.max()) if B else 1)
+        sh = _Shape(B=B, H_q=Hq, H_kv=H_kv, L=int(max_L), D=D, num_pages=P, page_size=ps,
+                    max_pages_per_seq=block_table.shape[1],
+                    dtype=0 if key_pages.dtype == np.uint16 else 1)
+        out = np.zeros(query.shape, dtype=np.float64)
+        st = self.lib.oracle_paged_attention_varlen(
+            ctypes.byref(sh), _ptr(query), _ptr(key_pages), _ptr(value_pages),
+            block_table.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),
+            context_lens.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),
+            cu_q.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)), int(T), float(scale),
+            int(bool(causal)), out.ctypes.data_as(ctypes.POINTER(ctypes.c_double)),
+            int(num_threads))
+        if st != ORACLE_OK:
+            raise OracleError(st)
+        return out
 
     def append_kv(self, k_new, v_new, key_pages, value_pages, block_table, context_lens):
         """Copies of the pools after writing the new tokens' K/V rows

@@ -22,6 +22,13 @@
  *                    "Week 3 Day 5", Task 2.  Natural exp in double; the max
  *                    is subtracted before exponentiating (stable softmax).
  *
+ *   oracle_paged_attention_varlen() -- a ragged batch (per-sequence query
+ *                    counts, tokens packed): each sequence's rows are those of
+ *                    a batch of that sequence alone ("Day 22: the fused
+ *                    paged-attention kernel": decode steps, causal prefills
+ *                    and partial continuations are all the same fold; "Week 3
+ *                    Day 5", Task 2: the causal offset is that sequence's
+ *                    context length minus its own query count).
  *   oracle_append_kv() -- the step before the path: the new tokens' K/V rows
  *                    are stored in their pages.  The pages introduce physical
  *                    pages and block tables as the prerequisite of "Week 3 Day
@@ -73,18 +80,24 @@ static int check_shape(const oracle_shape* sh) {
 
 /* Validates what the method will read for sequence b: its context length and
  * the block-table entries of its ceil(S / page_size) logical pages. */
-static int check_sequence(const oracle_shape* sh, const int32_t* block_table,
-                          const int32_t* context_lens, int b, int causal) {
+static int check_sequence_lq(const oracle_shape* sh, const int32_t* block_table,
+                             const int32_t* context_lens, int b, int causal, int L) {
     const int S = context_lens[b];
     if (S < 1 || (int64_t)S > (int64_t)sh->max_pages_per_seq * sh->page_size)
         return ORACLE_ERR_INVALID_ARG;
-    if (causal && sh->L > S) return ORACLE_ERR_INVALID_ARG;
+    if (causal && L > S) return ORACLE_ERR_INVALID_ARG;
     const int npg = (S + sh->page_size - 1) / sh->page_size;
     for (int lp = 0; lp < npg; ++lp) {
         const int32_t pp = block_table[(int64_t)b * sh->max_pages_per_seq + lp];
         if (pp < 0 || pp >= sh->num_pages) return ORACLE_ERR_BAD_BLOCK_TABLE;
     }
     return ORACLE_OK;
+}
+
+/* The same for sequences with sh->L query positions each. */
+static int check_sequence(const oracle_shape* sh, const int32_t* block_table,
+                          const int32_t* context_lens, int b, int causal) {
+    return check_sequence_lq(sh, block_table, context_lens, b, causal, sh->L);
 }
 
 static int kv_head_of(const oracle_shape* sh, int h) {
@@ -128,11 +141,12 @@ static void gather_one(const oracle_shape* sh, const void* key_pages, const void
  * scaled score before the softmax ("Week 2 Day 5: Fused Decode Attention",
  * Task 1, step 3: the score is scaled, then masked, then the causal rule applies).  A row whose every visible
  * score is -inf has no softmax; its output is 0. */
-static void attend_row(const oracle_shape* sh, const void* query, int b, int h, int l, int S,
-                       const double* K, const double* V, double scale, int causal,
+static void attend_row(const oracle_shape* sh, const void* query, int64_t qbase, int l, int L,
+                       int S, const double* K, const double* V, double scale, int causal,
                        const float* mask_row, double* x, double* o) {
-    const int D = sh->D, L = sh->L;
-    const int64_t qbase = (((int64_t)b * sh->H_q + h) * L + l) * D;
+    /* qbase: index of the row's first query element; l: its position among
+     * the sequence's L query positions (the last L of its S keys) */
+    const int D = sh->D;
     /* last visible key: s <= l + S - L under causal, s <= S - 1 otherwise */
 #if ORACLE_MUTANT == 1
     int last = causal ? l + S - L - 1 : S - 1; /* planted: causal off by one */
@@ -247,7 +261,8 @@ int oracle_paged_attention_masked(const oracle_shape* sh, const void* query,
             for (int h = 0; h < sh->H_q; ++h) {
                 if (kv_head_of(sh, h) != kvh) continue;
                 for (int l = 0; l < sh->L; ++l)
-                    attend_row(sh, query, b, h, l, S, K, V, scale, causal,
+                    attend_row(sh, query, (((int64_t)b * sh->H_q + h) * sh->L + l) * D, l,
+                               sh->L, S, K, V, scale, causal,
                                mask ? mask + (((int64_t)b * sh->H_q + h) * sh->L + l) * mask_S
                                     : NULL,
                                x, out + (((int64_t)b * sh->H_q + h) * sh->L + l) * D);
@@ -293,7 +308,71 @@ int oracle_paged_attention_rows(const oracle_shape* sh, const void* query,
             failed = 1;
         } else {
             gather_one(sh, key_pages, value_pages, block_table, b, kvh, S, K, V);
-            attend_row(sh, query, b, h, l, S, K, V, scale, causal, NULL, x, out + (int64_t)i * D);
+            attend_row(sh, query, (((int64_t)b * sh->H_q + h) * sh->L + l) * D, l, sh->L, S, K,
+                       V, scale, causal, NULL, x, out + (int64_t)i * D);
+        }
+        free(K);
+        free(V);
+        free(x);
+    }
+    return failed ? ORACLE_ERR_NOMEM : ORACLE_OK;
+}
+
+/* Ragged batch: sequence b has L_b = cu_q[b + 1] - cu_q[b] query positions,
+ * its last L_b of context_lens[b] keys (a decode step has L_b = 1, a prefill
+ * chunk L_b > 1, a sequence without new queries L_b = 0).  Queries and
+ * outputs are packed by token: row (b, h, l) is token cu_q[b] + l of
+ * [total_q, H_q, D].  Each row is the row of a batch of one sequence with L_b
+ * positions; rows of sequences with L_b = 0 do not exist and nothing of
+ * those sequences is read. */
+int oracle_paged_attention_varlen(const oracle_shape* sh, const void* query,
+                                  const void* key_pages, const void* value_pages,
+                                  const int32_t* block_table, const int32_t* context_lens,
+                                  const int32_t* cu_q, int total_q, double scale, int causal,
+                                  double* out, int num_threads) {
+    if (!query || !key_pages || !value_pages || !block_table || !context_lens || !cu_q || !out)
+        return ORACLE_ERR_INVALID_ARG;
+    int st = check_shape(sh);
+    if (st) return st;
+    if (cu_q[0] != 0 || cu_q[sh->B] != total_q) return ORACLE_ERR_INVALID_ARG;
+    for (int b = 0; b < sh->B; ++b) {
+        const int Lb = cu_q[b + 1] - cu_q[b];
+        if (Lb < 0 || Lb > sh->L) return ORACLE_ERR_INVALID_ARG;
+        if (Lb == 0) continue;
+        st = check_sequence_lq(sh, block_table, context_lens, b, causal, Lb);
+        if (st) return st;
+    }
+    const int D = sh->D;
+    const int n_items = sh->B * sh->H_kv;
+    int failed = 0;
+#ifdef _OPENMP
+    if (num_threads <= 0) num_threads = omp_get_max_threads();
+#pragma omp parallel for schedule(dynamic, 1) num_threads(num_threads)
+#endif
+    for (int item = 0; item < n_items; ++item) {
+        const int b = item / sh->H_kv, kvh = item % sh->H_kv;
+        const int Lb = cu_q[b + 1] - cu_q[b];
+        if (Lb == 0) continue;
+        const int S = context_lens[b];
+        double* K = (double*)malloc(sizeof(double) * (size_t)S * D);
+        double* V = (double*)malloc(sizeof(double) * (size_t)S * D);
+        double* x = (double*)malloc(sizeof(double) * (size_t)S);
+        if (!K || !V || !x) {
+            failed = 1;
+        } else {
+            gather_one(sh, key_pages, value_pages, block_table, b, kvh, S, K, V);
+            for (int h = 0; h < sh->H_q; ++h) {
+                if (kv_head_of(sh, h) != kvh) continue;
+                for (int l = 0; l < Lb; ++l) {
+                    const int64_t row = ((int64_t)(cu_q[b] + l) * sh->H_q + h) * D;
+#if ORACLE_MUTANT == 10
+                    const int Lq = sh->L; /* planted: the batch's longest query as offset */
+#else
+                    const int Lq = Lb;
+#endif
+                    attend_row(sh, query, row, l, Lq, S, K, V, scale, causal, NULL, x, out + row);
+                }
+            }
         }
         free(K);
         free(V);

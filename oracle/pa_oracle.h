@@ -83,6 +83,16 @@ int oracle_paged_attention_rows(const oracle_shape* sh, const void* query,
                                 double scale, int causal, const int32_t* rows, int n_rows,
                                 double* out, int num_threads);
 
+/* Ragged batch: sequence b has L_b = cu_q[b+1] - cu_q[b] query positions
+ * (0 <= L_b <= sh->L; cu_q[0] = 0, cu_q[B] = total_q), the last L_b of its
+ * context; query and out are packed [total_q, H_q, D] (row (b, h, l) is token
+ * cu_q[b] + l).  Sequences with L_b = 0 are skipped unread. */
+int oracle_paged_attention_varlen(const oracle_shape* sh, const void* query,
+                                  const void* key_pages, const void* value_pages,
+                                  const int32_t* block_table, const int32_t* context_lens,
+                                  const int32_t* cu_q, int total_q, double scale, int causal,
+                                  double* out, int num_threads);
+
 /* Append of new keys and values (the step before the path: the new tokens'
  * K/V stored in their pages).  Shape fields used: B, H_kv, L (new tokens per
  * sequence), D, num_pages, page_size, max_pages_per_seq, dtype.  The new

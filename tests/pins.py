@@ -527,9 +527,112 @@ def pin_mask_dominant_and_empty_rows(lib):
     assert np.array_equal(got[0][keep], ref[0][keep])
 
 
+# --------------------------------------------------------------------------
+# Ragged batches: per-sequence query counts, tokens packed [T, H_q, D]
+# --------------------------------------------------------------------------
+VARLEN_CASES = [
+    # (seed, H_q, H_kv, D, ps, L_b per sequence, context lengths, causal, dtype)
+    (81, 4, 2, 8, 3, [1, 7, 1, 3, 2], [9, 20, 1, 40, 2], True, "bf16"),
+    (82, 2, 2, 16, 16, [5, 1, 1], [5, 33, 17], True, "f32"),
+    (83, 6, 2, 8, 4, [2, 4, 1], [11, 6, 30], False, "bf16"),
+    (84, 4, 1, 128, 16, [1, 6], [13, 40], True, "bf16"),
+]
+
+
+def _varlen_case(seed, H_q, H_kv, D, ps, lens, ctx, causal, dtype):
+    """A ragged batch on the logical tensors of make_case: sequence b's
+    queries are the first L_b query rows drawn for it, packed by token."""
+    Lmax = max(lens)
+    c = make_case(seed, len(lens), H_q, H_kv, Lmax, D, ps, ctx, dtype=dtype, causal=causal)
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    T = int(cu[-1])
+    q_store = np.zeros((T, H_q, D), dtype=c.q_store.dtype)
+    q = np.zeros((T, H_q, D))
+    for b, Lb in enumerate(lens):
+        q_store[cu[b]:cu[b + 1]] = c.q_store[b, :, :Lb, :].transpose(1, 0, 2)
+        q[cu[b]:cu[b + 1]] = c.q[b, :, :Lb, :].transpose(1, 0, 2)
+    c.vq_store, c.vq, c.cu, c.lens = np.ascontiguousarray(q_store), q, cu, list(lens)
+    return c
+
+
+def _varlen_dense(c):
+    """Dense attention per sequence on the logical K/V: sequence b's L_b
+    queries are the last L_b of its S_b positions."""
+    G = c.H_q // c.H_kv
+    out = np.zeros(c.vq.shape)
+    for b, Lb in enumerate(c.lens):
+        if Lb == 0:
+            continue
+        S = int(c.ctx[b])
+        Kr = np.repeat(c.K[b, :, :S], G, axis=0)
+        Vr = np.repeat(c.V[b, :, :S], G, axis=0)
+        qb = c.vq[c.cu[b]:c.cu[b + 1]].transpose(1, 0, 2)  # [H_q, L_b, D]
+        scores = np.einsum("hld,hsd->hls", qb, Kr) * c.scale
+        scores = np.where(visible_mask(Lb, S, c.causal)[None], scores, -np.inf)
+        P = scipy.special.softmax(scores, axis=-1)
+        out[c.cu[b]:c.cu[b + 1]] = np.einsum("hls,hsd->hld", P, Vr).transpose(1, 0, 2)
+    return out
+
+
+def _run_varlen(lib, c, **kw):
+    return lib.paged_attention_varlen(c.vq_store, c.kp, c.vp, c.bt, c.ctx, c.cu, c.scale,
+                                      c.causal, **kw)
+
+
+def pin_varlen_bruteforce(lib):
+    for case in VARLEN_CASES:
+        c = _varlen_case(*case)
+        assert_close(_run_varlen(lib, c), _varlen_dense(c), what=f"varlen seed {case[0]}")
+
+
+def pin_varlen_equals_single_sequences(lib):
+    """Each sequence of a ragged batch gives exactly the rows of a batch of
+    that sequence alone with L = L_b (the uniform path, pinned above)."""
+    for case in VARLEN_CASES:
+        c = _varlen_case(*case)
+        got = _run_varlen(lib, c)
+        for b, Lb in enumerate(c.lens):
+            q1 = np.ascontiguousarray(c.vq_store[c.cu[b]:c.cu[b + 1]].transpose(1, 0, 2)[None])
+            one = lib.paged_attention(q1, c.kp, c.vp, np.ascontiguousarray(c.bt[b:b + 1]),
+                                      np.ascontiguousarray(c.ctx[b:b + 1]), c.scale, c.causal)
+            assert np.array_equal(got[c.cu[b]:c.cu[b + 1]], one[0].transpose(1, 0, 2)), \
+                f"varlen seed {case[0]}: sequence {b} differs from its single-sequence batch"
+
+
+def pin_varlen_empty_sequences_and_errors(lib):
+    """Sequences with no new queries are not read (their context length and
+    table row may be anything); a broken offset array or a query count above
+    the context (causal) is rejected."""
+    c = _varlen_case(85, 4, 2, 8, 3, [2, 3], [7, 12], True, "bf16")
+    ref = _run_varlen(lib, c)
+    # insert an empty sequence with junk metadata between the two
+    bt = np.concatenate([c.bt[:1], np.full((1, c.bt.shape[1]), 10 ** 6, np.int32), c.bt[1:]])
+    ctx = np.array([c.ctx[0], -5, c.ctx[1]], dtype=np.int32)
+    cu = np.array([0, 2, 2, 5], dtype=np.int32)
+    got = lib.paged_attention_varlen(c.vq_store, c.kp, c.vp, bt, ctx, cu, c.scale, True)
+    assert np.array_equal(got, ref), "an empty sequence changed the batch"
+    for cu_bad, what in (([1, 2, 5], "cu_q[0] != 0"), ([0, 4, 5], "L_b > max_L"),
+                         ([0, 3, 2], "decreasing offsets")):
+        try:
+            lib.paged_attention_varlen(c.vq_store, c.kp, c.vp, c.bt, c.ctx,
+                                       np.array(cu_bad, np.int32), c.scale, True, max_L=3)
+        except oracle_mod.OracleError as e:
+            assert e.code == oracle_mod.ORACLE_ERR_INVALID_ARG, what
+        else:
+            raise AssertionError(f"accepted {what}")
+    short = np.array([2, 2], dtype=np.int32)  # sequence 1: 3 queries, 2 keys
+    try:
+        lib.paged_attention_varlen(c.vq_store, c.kp, c.vp, c.bt, short, c.cu, c.scale, True)
+    except oracle_mod.OracleError as e:
+        assert e.code == oracle_mod.ORACLE_ERR_INVALID_ARG
+    else:
+        raise AssertionError("accepted L_b > context length under causal")
+
+
 ALL_PINS = [pin_bruteforce, pin_torch_sdpa, pin_page_permutation, pin_unused_table_entries,
             pin_tile_size_invariance, pin_single_page, pin_one_hot, pin_uniform_visible_mean,
             pin_gqa_equals_repeat, pin_gather, pin_errors, pin_rows_api,
             pin_append_dense_slice, pin_append_page_permutation, pin_append_touches_only_new_rows,
             pin_append_errors, pin_mask_bruteforce, pin_mask_zero_and_row_constant,
-            pin_mask_dominant_and_empty_rows]
+            pin_mask_dominant_and_empty_rows, pin_varlen_bruteforce,
+            pin_varlen_equals_single_sequences, pin_varlen_empty_sequences_and_errors]

@@ -5,14 +5,15 @@ ORACLE_MUTANT=n: (1) causal bound off by one, (2) wrong GQA head map, (3)
 block table ignored, (4) scale dropped, (5) K and V swapped, (6) a term
 dropped from the softmax denominator, (7) causal offset with its sign flipped,
 (8) the K/V append writing one slot too far, (9) an explicit mask subtracted
-instead of added.
+instead of added, (10) a ragged batch's causal offset taken from the longest
+query instead of the sequence's own.
 """
 import pytest
 
 import oracle
 import pins
 
-MUTANTS = [1, 2, 3, 4, 5, 6, 7, 8, 9]
+MUTANTS = [1, 2, 3, 4, 5, 6, 7, 8, 9, 10]
 
 
 @pytest.mark.parametrize("mutant", MUTANTS)

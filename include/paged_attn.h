@@ -85,7 +85,8 @@ typedef struct {
  * largest over the schedules).  The first 4 bytes are the flag word; the
  * caller must zero the workspace once before its first use (the flag is then
  * sticky across calls until cleared).  The rest holds the decode schedule's
- * per-split partial states (m, l, o[D] in fp32) and needs no initialisation.
+ * per-split partial states (m, l, o[D] in fp32) and, last, the tile plan of
+ * a ragged batch (B + 2 ints); it needs no initialisation.
  * Returns 0 for an invalid shape. */
 size_t pa_workspace_bytes(const pa_shape* shape);
 
@@ -136,6 +137,36 @@ pa_status pa_paged_attention_masked(const pa_shape* shape, const void* query,
                                     float scale, int causal, const float* mask,
                                     long long mask_S, void* out, void* workspace,
                                     size_t workspace_bytes, void* cuda_stream, int schedule);
+
+/* A ragged batch in one call: sequence b has L_b = cu_q[b + 1] - cu_q[b]
+ * new query positions, the last L_b of its context_lens[b] keys, so decode
+ * steps (L_b = 1), prefill chunks and continuations (L_b > 1) and sequences
+ * without new tokens (L_b = 0, not read) mix in one batch.  Every row is the
+ * row of a batch of that sequence alone: causal visibility s <= l +
+ * context_lens[b] - L_b ("Week 3 Day 5: Paged FlashAttention", Task 2; "Day
+ * 22: the fused paged-attention kernel" runs decode steps, causal prefills and
+ * partial continuations as one fold).
+ *
+ * query, out: [total_q, H_q, D] packed by token (row (b, h, l) is token
+ * cu_q[b] + l), 16-byte aligned.  cu_q: int32 device array [B + 1], cu_q[0]
+ * = 0, nondecreasing, cu_q[B] = total_q.  shape->L: an upper bound on every
+ * L_b; shape->B: the number of sequences.  Pool, block table and context
+ * lengths as for pa_paged_attention.  workspace: pa_workspace_bytes(shape).
+ *
+ * PA_SCHED_AUTO sends each sequence to a schedule on the device: at most 4
+ * query rows per kv head ((H_q / H_kv) * L_b <= 4) to the page walk, more to
+ * the tensor-core tiles (bf16, shapes the tiles take), both launched by this
+ * call; a forced schedule takes every sequence.  A sequence whose offsets are
+ * broken (cu_q[b] < 0, L_b < 0 or > shape->L, cu_q[b + 1] > total_q) sets
+ * PA_FLAG_BAD_CONTEXT and none of its rows is written; one whose context
+ * length breaks the contract sets it too and gets zero rows.  No explicit
+ * mask.  Returns as pa_paged_attention_sched; PA_OK at once for total_q = 0. */
+pa_status pa_paged_attention_varlen(const pa_shape* shape, const void* query,
+                                    const void* key_pages, const void* value_pages,
+                                    const int32_t* block_table, const int32_t* context_lens,
+                                    const int32_t* cu_q, int total_q, float scale, int causal,
+                                    void* out, void* workspace, size_t workspace_bytes,
+                                    void* cuda_stream, int schedule);
 
 /* Debug gather of "Week 3 Day 5", Task 1: writes the dense history of every
  * (b, kv_head) through the block table, k_dense/v_dense [B, H_kv, max_S, D]

@@ -102,6 +102,10 @@ def load(auto_build: bool = True):
                                                   ctypes.c_int, vp, ctypes.c_longlong, vp, vp,
                                                   sz, vp, ctypes.c_int]
         lib.pa_paged_attention_masked.restype = ctypes.c_int
+        lib.pa_paged_attention_varlen.argtypes = [sp, vp, vp, vp, i32p, i32p, i32p, ctypes.c_int,
+                                                  ctypes.c_float, ctypes.c_int, vp, vp, sz, vp,
+                                                  ctypes.c_int]
+        lib.pa_paged_attention_varlen.restype = ctypes.c_int
         lib.pa_append_kv.argtypes = [sp, vp, vp, vp, vp, i32p, i32p, vp, sz, vp]
         lib.pa_append_kv.restype = ctypes.c_int
         lib.pa_status_str.argtypes = [ctypes.c_int]
@@ -219,6 +223,17 @@ def pa_paged_attention_masked(shape, query, key_pages, value_pages, block_table,
         _ptr(workspace), int(workspace_bytes), _stream(stream), int(schedule))
 
 
+def pa_paged_attention_varlen(shape, query, key_pages, value_pages, block_table, context_lens,
+                              cu_q, total_q, scale, causal, out, workspace, workspace_bytes,
+                              stream=None, schedule=PA_SCHED_AUTO) -> int:
+    """Ragged batch: query/out [total_q, H_q, D] packed by token, cu_q int32
+    device tensor [B + 1]; shape.L bounds every sequence's query count."""
+    return load().pa_paged_attention_varlen(
+        ctypes.byref(shape), _ptr(query), _ptr(key_pages), _ptr(value_pages), _ptr(block_table),
+        _ptr(context_lens), _ptr(cu_q), int(total_q), float(scale), int(bool(causal)),
+        _ptr(out), _ptr(workspace), int(workspace_bytes), _stream(stream), int(schedule))
+
+
 def pa_append_kv(shape, k_new, v_new, key_pages, value_pages, block_table, context_lens,
                  workspace, workspace_bytes, stream=None) -> int:
     return load().pa_append_kv(
@@ -318,3 +333,53 @@ def append_kv(k_new, v_new, key_pages, value_pages, block_table, context_lens, *
     if st != PA_OK:
         raise PagedAttentionError(st, "pa_append_kv")
     return workspace
+
+
+def shape_of_varlen(query, key_pages, block_table, max_L) -> pa_shape:
+    """pa_shape of a ragged batch: query [total_q, H_q, D] packed by token,
+    B = block_table.shape[0] sequences, L = max_L (bounds every L_b)."""
+    import torch
+    T, H_q, D = query.shape
+    P, H_kv, ps, D2 = key_pages.shape
+    if D2 != D:
+        raise ValueError("query and pages disagree on head dim")
+    if query.dtype != key_pages.dtype:
+        raise ValueError("query and pages must share a dtype")
+    dt = {torch.bfloat16: PA_BF16, torch.float32: PA_F32}.get(query.dtype)
+    if dt is None:
+        raise ValueError(f"unsupported dtype {query.dtype}")
+    return make_shape(block_table.shape[0], H_q, H_kv, max(1, int(max_L)), D, P, ps,
+                      block_table.shape[1], dt)
+
+
+def paged_attention_varlen(query, key_pages, value_pages, block_table, context_lens, cu_q,
+                           max_L, page_size, scale=None, causal=True, *, out=None,
+                           workspace=None, schedule=PA_SCHED_AUTO, stream=None):
+    """Ragged batch: out[total_q, H_q, D]; sequence b's queries are tokens
+    cu_q[b] .. cu_q[b+1]-1 of `query` and the last positions of its context.
+    max_L bounds every cu_q[b+1] - cu_q[b]."""
+    import torch
+    shape = shape_of_varlen(query, key_pages, block_table, max_L)
+    if shape.page_size != int(page_size):
+        raise ValueError("page_size disagrees with key_pages.shape[2]")
+    for name, t in (("query", query), ("key_pages", key_pages), ("value_pages", value_pages),
+                    ("block_table", block_table), ("context_lens", context_lens), ("cu_q", cu_q)):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    if block_table.dtype != torch.int32 or context_lens.dtype != torch.int32 or \
+            cu_q.dtype != torch.int32:
+        raise ValueError("block_table, context_lens and cu_q must be int32")
+    if cu_q.numel() != shape.B + 1 or context_lens.numel() != shape.B:
+        raise ValueError("cu_q must hold B + 1 offsets and context_lens B lengths")
+    if scale is None:
+        scale = 1.0 / math.sqrt(query.shape[-1])
+    if out is None:
+        out = torch.empty_like(query)
+    if workspace is None:
+        workspace = new_workspace(shape, query.device)
+    st = pa_paged_attention_varlen(shape, query, key_pages, value_pages, block_table,
+                                   context_lens, cu_q, query.shape[0], scale, causal, out,
+                                   workspace, workspace.numel(), stream, schedule)
+    if st != PA_OK:
+        raise PagedAttentionError(st, "pa_paged_attention_varlen")
+    return out

@@ -71,7 +71,7 @@ int choose(const pa_shape& s) {
     // rows, 2-10x beyond); with at most 4 rows the page walk on CUDA cores
     // wins, except on calls so small that the tile schedule's lower fixed
     // cost decides (B * H_kv * context capacity up to 64K token rows).
-    if (rows > 4) return PA_SCHED_PREFILL;
+    if (rows > kMixedDecodeRows) return PA_SCHED_PREFILL;
     const long long work =
         static_cast<long long>(s.B) * s.H_kv * s.max_pages_per_seq * s.page_size;
     return work <= 65536 ? PA_SCHED_PREFILL : PA_SCHED_DECODE;
@@ -130,8 +130,7 @@ size_t pa_workspace_bytes(const pa_shape* shape) {
     if (check_shape(shape) != PA_OK) return 0;
     DeviceInfo dev;
     if (current_device_info(&dev) != PA_OK) return 0;
-    size_t need = decode_workspace_bytes(*shape, dev.sm_count);
-    return need > kFlagBytes ? need : kFlagBytes;
+    return workspace_bytes_total(*shape, dev.sm_count);
 }
 
 pa_status pa_paged_attention(const pa_shape* shape, const void* query, const void* key_pages,
@@ -175,6 +174,81 @@ pa_status pa_paged_attention_masked(const pa_shape* shape, const void* query,
     return run(shape, query, key_pages, value_pages, block_table, context_lens, scale, causal,
                out, workspace, workspace_bytes, cuda_stream, schedule, nullptr, nullptr, mask,
                mask_S);
+}
+
+pa_status pa_paged_attention_varlen(const pa_shape* shape, const void* query,
+                                    const void* key_pages, const void* value_pages,
+                                    const int32_t* block_table, const int32_t* context_lens,
+                                    const int32_t* cu_q, int total_q, float scale, int causal,
+                                    void* out, void* workspace, size_t workspace_bytes,
+                                    void* cuda_stream, int schedule) {
+    pa_status st = check_shape(shape);
+    if (st != PA_OK) return st;
+    const pa_shape& sh = *shape;
+    if (!query || !key_pages || !value_pages || !block_table || !context_lens || !cu_q || !out)
+        return PA_ERR_INVALID_ARG;
+    if (!aligned(query, 16) || !aligned(key_pages, 16) || !aligned(value_pages, 16) ||
+        !aligned(out, 16) || !aligned(block_table, 4) || !aligned(context_lens, 4) ||
+        !aligned(cu_q, 4))
+        return PA_ERR_INVALID_ARG;
+    if (total_q < 0 || !(scale == scale)) return PA_ERR_INVALID_ARG;
+    if (static_cast<long long>(total_q) * sh.H_q >= (1ll << 31)) return PA_ERR_UNSUPPORTED;
+    if (!workspace || !aligned(workspace, 256)) return PA_ERR_WORKSPACE;
+    if (schedule != PA_SCHED_AUTO && schedule != PA_SCHED_DECODE && schedule != PA_SCHED_PREFILL)
+        return PA_ERR_INVALID_ARG;
+
+    Call c;
+    c.sh = sh;
+    c.q = query;
+    c.kp = key_pages;
+    c.vp = value_pages;
+    c.bt = block_table;
+    c.ctx = context_lens;
+    c.scale = scale;
+    c.causal = causal ? 1 : 0;
+    c.out = out;
+    c.ws = workspace;
+    c.ws_bytes = workspace_bytes;
+    c.stream = static_cast<cudaStream_t>(cuda_stream);
+    c.cu_q = cu_q;
+    c.total_q = total_q;
+    st = current_device_info(&c.dev);
+    if (st != PA_OK) return st;
+    if (c.dev.cc_major != 10 || c.dev.cc_minor != 3) return PA_ERR_UNSUPPORTED;
+    c.plan_off = varlen_plan_offset(sh, c.dev.sm_count);
+    if (workspace_bytes < workspace_bytes_total(sh, c.dev.sm_count)) return PA_ERR_WORKSPACE;
+    if (total_q == 0) return PA_OK;  // no query rows
+
+    // Which sequences each schedule takes: a forced schedule takes all; AUTO
+    // gives sequences with at most kMixedDecodeRows query rows per kv head to
+    // the page walk and the rest to the tensor-core tiles, both in this call.
+    const int G = sh.H_q / sh.H_kv;
+    const bool tiles_ok = sh.dtype == PA_BF16 && prefill_supported(sh);
+    bool run_decode = false, run_tiles = false;
+    int dec_L = sh.L;
+    if (schedule == PA_SCHED_DECODE || (schedule == PA_SCHED_AUTO && !tiles_ok)) {
+        run_decode = true;
+    } else if (schedule == PA_SCHED_PREFILL) {
+        if (!tiles_ok) return PA_ERR_UNSUPPORTED;
+        run_tiles = true;
+        c.tiles_min_L = 0;
+    } else {  // AUTO, mixed
+        dec_L = kMixedDecodeRows / G < sh.L ? kMixedDecodeRows / G : sh.L;
+        run_decode = dec_L > 0;
+        run_tiles = dec_L < sh.L;
+        c.tiles_min_L = dec_L;
+        c.route_mixed = run_tiles ? 1 : 0;
+    }
+    if (run_tiles) {
+        st = prefill_launch(c);
+        if (st != PA_OK) return st;
+    }
+    if (run_decode) {
+        Call d = c;
+        d.sh.L = dec_L;  // the largest L_b the page walk takes
+        st = decode_launch(d);
+    }
+    return st;
 }
 
 pa_status pa_gather_debug(const pa_shape* shape, const void* key_pages, const void* value_pages,

@@ -71,6 +71,11 @@ struct DecodeParams {
     int tk_pages, tk_slots;  // a full tile of TK keys spans TK / ps pages + TK % ps slots
     const float* mask;       // optional additive mask [B * H_q, L, mask_S], or null
     long long mask_S;
+    // ragged batch: query rows packed by token [total_q, H_q, D], sequence b
+    // owns tokens cu_q[b] .. cu_q[b + 1] - 1; null for the [B, H_q, L, D] layout
+    const int32_t* cu_q;
+    int total_q;
+    int route_mixed;  // 1: sequences with more than L query positions belong to the tiles
 };
 
 template <typename T, int RB_, int P_, int TK_, int NCW_, int NST_, int MINB_ = 1, int GRAN_ = 0>
@@ -114,7 +119,7 @@ struct Cfg {
 };
 
 struct alignas(16) StageHdr {
-    int seg_id, b, kvh, chunk, key0, nvalid, S, flags, slot, pad0, pad1, pad2;
+    int seg_id, b, kvh, chunk, key0, nvalid, S, flags, slot, Lb, q0, pad2;
 };
 enum : int { kStart = 1, kEnd = 2, kFinal = 4, kLast = 8 };
 
@@ -134,16 +139,58 @@ __device__ __forceinline__ void finish_chunk_counters(const DecodeParams& p, int
     }
 }
 
-// The context length the kernels use for sequence b: 0 (no work, rows
-// written as zeros) when it breaks the contract.
-__device__ __forceinline__ int checked_len(const DecodeParams& p, int b, bool report) {
-    const int S = __ldg(p.ctx + b);
-    const bool bad = S < 1 || static_cast<long long>(S) > p.max_S || (p.causal && S < p.L);
-    if (bad) {
-        if (report) atomicOr(p.flag, PA_FLAG_BAD_CONTEXT);
-        return 0;
+// The work of sequence b in this launch.  Lb: its query positions (p.L in
+// the [B, H_q, L, D] layout); q0: its first token (ragged batch).  nch = 0:
+// the sequence is not this launch's (no new queries, or more than p.L of
+// them in a mixed batch, which the tile schedule takes), or its offsets are
+// broken (flagged; nothing of it is written).  S = 0 with nch > 0: its context
+// length breaks the contract (flagged; its rows are written as zeros).
+struct SeqWork {
+    int S, nch, Lb, q0;
+};
+
+// From the raw values S_raw = context_lens[b], q0 = cu_q[b], q1 = cu_q[b + 1].
+template <int RB>
+__device__ __forceinline__ SeqWork seq_work_raw(const DecodeParams& p, int S_raw, int q0, int q1,
+                                                bool report) {
+    SeqWork w;
+    w.Lb = p.L;
+    w.q0 = 0;
+    if (p.cu_q) {
+        w.q0 = q0;
+        w.Lb = q1 - w.q0;
+        const bool broken = w.q0 < 0 || w.Lb < 0 || q1 > p.total_q || (!p.route_mixed && w.Lb > p.L);
+        if (broken || w.Lb == 0 || w.Lb > p.L) {
+            if (broken && report) atomicOr(p.flag, PA_FLAG_BAD_CONTEXT);
+            w.S = 0;
+            w.nch = 0;
+            return w;
+        }
     }
-    return S;
+    w.nch = (p.G * w.Lb + RB - 1) / RB;
+    const int S = S_raw;
+    const bool bad = S < 1 || static_cast<long long>(S) > p.max_S || (p.causal && S < w.Lb);
+    if (bad && report) atomicOr(p.flag, PA_FLAG_BAD_CONTEXT);
+    w.S = bad ? 0 : S;
+    return w;
+}
+
+template <int RB>
+__device__ __forceinline__ SeqWork seq_work(const DecodeParams& p, int b, bool report) {
+    const int q0 = p.cu_q ? __ldg(p.cu_q + b) : 0;
+    const int q1 = p.cu_q ? __ldg(p.cu_q + b + 1) : 0;
+    return seq_work_raw<RB>(p, __ldg(p.ctx + b), q0, q1, report);
+}
+
+// Row index (in units of D elements) of row rr = g * Lb + l of the (b, kv
+// head) block in the query / output layout.
+__device__ __forceinline__ long long out_row(const DecodeParams& p, int b, int kvh, int Lb, int q0,
+                                             int rr) {
+    if (p.cu_q) {
+        const int g = rr / Lb, l = rr - g * Lb;
+        return static_cast<long long>(q0 + l) * p.H_q + static_cast<long long>(kvh) * p.G + g;
+    }
+    return (static_cast<long long>(b) * p.H_q + static_cast<long long>(kvh) * p.G) * p.L + rr;
 }
 
 __device__ __forceinline__ int warp_sum(int v) {
@@ -212,17 +259,15 @@ struct Walker {
     int chunk, next, cu0, cu1;  // current chunk, the one claimed after it, its units
     int u;                      // first unit of the next tile
     int b, bpref, S, ng;        // sequence, its first unit, length, units per segment
+    int nch, Lb, q0;            // its row chunks, query positions, first token
     int sib, g;                 // segment within the sequence, unit within the segment
     int kvh, chunk_r;           // kv head and row chunk of the segment
     int key0, lp, slot;         // first key of the next tile, its page and slot
     int S_ahead;                // context length of sequence b + 1 (requested early)
+    int qn, qn_ahead;           // cu_q[b + 1], cu_q[b + 2] (ragged batch, requested early)
     int wb, win0, win1;         // page-id windows of sequence b
     int nb_win;                 // pages 0..31 of sequence b + 1
 };
-
-__device__ __forceinline__ int sanitized_len(const DecodeParams& p, int S) {
-    return (S < 1 || static_cast<long long>(S) > p.max_S || (p.causal && S < p.L)) ? 0 : S;
-}
 
 // Block-table entry (b, lp), or -1 past the row.  The page windows may fetch
 // entries past a sequence's last page; those values are never used.
@@ -237,20 +282,37 @@ __device__ __forceinline__ void load_windows(const DecodeParams& p, int lane, Wa
 }
 
 // Position the walker at unit w.u (a chunk start); sequences at or after w.b.
+// Enters sequence w.b: its length, units per segment and row chunks.
 template <class C>
-__device__ void walker_seek(const DecodeParams& p, int lane, int segs_per_b, Walker<C>& w) {
-    while (w.u >= w.bpref + segs_per_b * w.ng) {
-        w.bpref += segs_per_b * w.ng;
+__device__ __forceinline__ void walker_set(const DecodeParams& p, Walker<C>& w, const SeqWork& sw) {
+    w.S = sw.S;
+    w.nch = sw.nch;
+    w.Lb = sw.Lb;
+    w.q0 = sw.q0;
+    w.ng = sw.nch > 0 ? (sw.S + C::GRAN - 1) / C::GRAN : 0;
+}
+
+// Requests the raw metadata of sequence w.b + 1 for the next walker_set.
+template <class C>
+__device__ __forceinline__ void walker_look_ahead(const DecodeParams& p, Walker<C>& w) {
+    w.S_ahead = w.b + 1 < p.B ? __ldg(p.ctx + w.b + 1) : 0;
+    w.qn_ahead = p.cu_q && w.b + 1 < p.B ? __ldg(p.cu_q + w.b + 2) : 0;
+}
+
+template <class C>
+__device__ void walker_seek(const DecodeParams& p, int lane, Walker<C>& w) {
+    while (w.u >= w.bpref + p.H_kv * w.nch * w.ng) {
+        w.bpref += p.H_kv * w.nch * w.ng;
         ++w.b;
-        w.S = sanitized_len(p, w.S_ahead);
-        w.ng = (w.S + C::GRAN - 1) / C::GRAN;
-        w.S_ahead = w.b + 1 < p.B ? __ldg(p.ctx + w.b + 1) : 0;
+        walker_set<C>(p, w, seq_work<C::RB>(p, w.b, false));
     }
+    w.qn = p.cu_q ? __ldg(p.cu_q + w.b + 1) : 0;
+    walker_look_ahead<C>(p, w);
     const int loc = w.u - w.bpref;
     w.sib = loc / w.ng;
     w.g = loc - w.sib * w.ng;
-    w.kvh = w.sib / p.nchunk;
-    w.chunk_r = w.sib - w.kvh * p.nchunk;
+    w.kvh = w.sib / w.nch;
+    w.chunk_r = w.sib - w.kvh * w.nch;
     w.key0 = w.g * C::GRAN;
     w.lp = w.key0 / p.ps;
     w.slot = w.key0 - w.lp * p.ps;
@@ -373,10 +435,13 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB) decode_split_kernel(const
     // kChunksPerCta equal chunks per CTA.  CTA c starts with chunk c and then
     // claims further chunks from a counter, so SMs that stream faster take
     // more of them.
-    const int segs_per_b = p.H_kv * p.nchunk;
+    // units of sequence b: its segments (kv heads x row chunks) x key units
+    auto units_of = [&](int b, bool report) {
+        const SeqWork sw = seq_work<C::RB>(p, b, report);
+        return p.H_kv * sw.nch * ((sw.S + C::GRAN - 1) / C::GRAN);
+    };
     int mine = 0;
-    for (int b = tid; b < p.B; b += C::THREADS)
-        mine += segs_per_b * ((checked_len(p, b, blockIdx.x == 0) + C::GRAN - 1) / C::GRAN);
+    for (int b = tid; b < p.B; b += C::THREADS) mine += units_of(b, blockIdx.x == 0);
     int total;
     block_incl_scan<C::THREADS>(mine, s_scan, &total);
     const int grid = static_cast<int>(gridDim.x);
@@ -386,7 +451,7 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB) decode_split_kernel(const
     int carry = 0;
     for (int base = 0; base < p.B; base += C::THREADS) {
         const int b = base + tid;
-        const int v = b < p.B ? segs_per_b * ((checked_len(p, b, false) + C::GRAN - 1) / C::GRAN) : 0;
+        const int v = b < p.B ? units_of(b, false) : 0;
         int tot;
         const int incl = block_incl_scan<C::THREADS>(v, s_scan, &tot);
         const int excl = carry + incl - v;
@@ -426,10 +491,8 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB) decode_split_kernel(const
         w.u = w.cu0;
         w.b = s_start_b;
         w.bpref = s_start_pref;
-        w.S = sanitized_len(p, __ldg(p.ctx + w.b));
-        w.ng = (w.S + C::GRAN - 1) / C::GRAN;
-        w.S_ahead = w.b + 1 < p.B ? __ldg(p.ctx + w.b + 1) : 0;
-        walker_seek<C>(p, lane, segs_per_b, w);
+        walker_set<C>(p, w, seq_work<C::RB>(p, w.b, false));
+        walker_seek<C>(p, lane, w);
         int issued = 0;
         for (int i = 0;; ++i) {
             // ---- this tile: keys [key0, key0 + nvalid) of segment (b, sib) ----
@@ -447,7 +510,7 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB) decode_split_kernel(const
             // page pieces: piece j covers page lp + j (lane j + 32 k handles it);
             // a tile spans at most TK / ps + 2 pages, one lane each unless ps < 4
             const int row0 = w.chunk_r * C::RB;
-            const int nrows = min(C::RB, p.G * p.L - row0);
+            const int nrows = min(C::RB, p.G * w.Lb - row0);
             int pid[C::PIECE_ITERS], klo[C::PIECE_ITERS], kn[C::PIECE_ITERS];
             bool any_bad = false;
 #pragma unroll
@@ -488,10 +551,10 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB) decode_split_kernel(const
             // before the consumers read them: [key0, key0 + nvalid) widened to
             // whole 16-byte words, inside the row (mask_S % 4 == 0, >= S)
             if (p.mask && lane < nrows && nvalid > 0) {
-                const int rg = row0 + lane, gq = rg / p.L, lq = rg - gq * p.L;
+                const int rg = row0 + lane, gq = rg / w.Lb, lq = rg - gq * w.Lb;
                 const int lo = w.key0 & ~3, hi = (w.key0 + nvalid + 3) & ~3;
                 bulk_prefetch_l2(p.mask + ((static_cast<long long>(w.b) * p.H_q +
-                                            w.kvh * p.G + gq) * p.L + lq) * p.mask_S + lo,
+                                            w.kvh * p.G + gq) * w.Lb + lq) * p.mask_S + lo,
                                  static_cast<uint32_t>(hi - lo) * 4u);
             }
 
@@ -510,7 +573,7 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB) decode_split_kernel(const
                 uint4* h = reinterpret_cast<uint4*>(st);
                 h[0] = make_uint4(seg_id, w.b, w.kvh, w.chunk_r);
                 h[1] = make_uint4(w.key0, nvalid, w.S, flags);
-                h[2] = make_uint4(seg_id + w.chunk, 0, 0, 0);
+                h[2] = make_uint4(seg_id + w.chunk, w.Lb, w.q0, 0);
                 mbar_arrive_expect_tx(fb, bytes);
             }
             __syncwarp();
@@ -526,11 +589,17 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB) decode_split_kernel(const
                 bulk_g2s(kdst + off, kp + row * C::ROW, nb, fb, pol);
                 bulk_g2s(kdst + C::KBYTES + off, vp + row * C::ROW, nb, fb, pol);
             }
-            if (lane == 0 && start) {
-                const long long qrow = (static_cast<long long>(w.b) * p.H_q +
-                                        static_cast<long long>(w.kvh) * p.G) * p.L + row0;
-                bulk_g2s(smem_u32(st) + C::HDR, qp + qrow * C::ROW,
-                         static_cast<uint32_t>(nrows) * C::ROW, fb, pol);
+            if (start) {
+                if (!p.cu_q) {  // the segment's rows are contiguous
+                    if (lane == 0)
+                        bulk_g2s(smem_u32(st) + C::HDR,
+                                 qp + out_row(p, w.b, w.kvh, w.Lb, 0, row0) * C::ROW,
+                                 static_cast<uint32_t>(nrows) * C::ROW, fb, pol);
+                } else if (lane < nrows) {  // one token-major row per lane
+                    bulk_g2s(smem_u32(st) + C::HDR + lane * C::ROW,
+                             qp + out_row(p, w.b, w.kvh, w.Lb, w.q0, row0 + lane) * C::ROW,
+                             C::ROW, fb, pol);
+                }
             }
             issued = i + 1;
 
@@ -544,7 +613,7 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB) decode_split_kernel(const
                 w.cu0 = w.chunk * cu;
                 w.cu1 = min(w.cu0 + cu, total);
                 w.u = w.cu0;
-                walker_seek<C>(p, lane, segs_per_b, w);
+                walker_seek<C>(p, lane, w);
             } else if (w.u >= seg_u1) {
                 // next segment: same sequence (next row chunk / kv head) or the next one
                 w.g = 0;
@@ -552,18 +621,19 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB) decode_split_kernel(const
                 w.lp = 0;
                 w.slot = 0;
                 ++w.sib;
-                if (++w.chunk_r == p.nchunk) {
+                if (++w.chunk_r == w.nch) {
                     w.chunk_r = 0;
                     ++w.kvh;
                 }
-                if (w.sib == segs_per_b) {
+                if (w.sib == p.H_kv * w.nch) {
                     // next sequence with work (sequences with no keys are skipped)
                     do {
-                        w.bpref += segs_per_b * w.ng;
+                        w.bpref += p.H_kv * w.nch * w.ng;
                         ++w.b;
-                        w.S = sanitized_len(p, w.S_ahead);
-                        w.ng = (w.S + C::GRAN - 1) / C::GRAN;
-                        w.S_ahead = w.b + 1 < p.B ? __ldg(p.ctx + w.b + 1) : 0;
+                        walker_set<C>(p, w, seq_work_raw<C::RB>(p, w.S_ahead, w.qn, w.qn_ahead,
+                                                                 false));
+                        w.qn = w.qn_ahead;
+                        walker_look_ahead<C>(p, w);
                         w.win0 = w.nb_win;
                         w.nb_win = w.b + 1 < p.B ? bt_entry(p, w.b + 1, lane) : -1;
                     } while (w.ng == 0);
@@ -638,7 +708,7 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB) decode_split_kernel(const
         const StageHdr h = *reinterpret_cast<const StageHdr*>(st);
 
         if (h.flags & kStart) {
-            const int rows = p.G * p.L - h.chunk * C::RB;
+            const int rows = p.G * h.Lb - h.chunk * C::RB;
             lmin = INT_MAX;
 #pragma unroll
             for (int r = 0; r < C::RB; ++r) {
@@ -649,9 +719,9 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB) decode_split_kernel(const
                     q2[r][e].y *= p.scale_log2;
                 }
                 o4[r][0] = o4[r][1] = make_float2(0.f, 0.f);
-                lmin = min(lmin, r < rows ? (h.chunk * C::RB + r) % p.L : p.L - 1);
+                lmin = min(lmin, r < rows ? (h.chunk * C::RB + r) % h.Lb : h.Lb - 1);
             }
-            lrow_mine = rho < rows ? (h.chunk * C::RB + rho) % p.L : p.L - 1;
+            lrow_mine = rho < rows ? (h.chunk * C::RB + rho) % h.Lb : h.Lb - 1;
             m_mine = neg_inf();
             l_mine = 0.f;
         }
@@ -665,10 +735,10 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB) decode_split_kernel(const
             float mv[C::IT];
             if (p.mask) {
                 const int rg = h.chunk * C::RB + rho;  // row of the (b, kv head) block
-                const bool rok = rg < p.G * p.L;
-                const int gq = rg / p.L, lq = rg - gq * p.L;
+                const bool rok = rg < p.G * h.Lb;
+                const int gq = rg / h.Lb, lq = rg - gq * h.Lb;
                 const float* mrow = p.mask + ((static_cast<long long>(h.b) * p.H_q +
-                                               h.kvh * p.G + gq) * p.L + lq) * p.mask_S +
+                                               h.kvh * p.G + gq) * h.Lb + lq) * p.mask_S +
                                     h.key0;
 #pragma unroll
                 for (int it = 0; it < C::IT; ++it) {
@@ -700,13 +770,13 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB) decode_split_kernel(const
             // past the context or past a row's causal frontier get -inf.
             const int last_key = h.key0 + kw0 + C::KPW - 1;
             const bool tail = h.nvalid < kw0 + C::KPW;
-            if (tail || (p.causal && last_key > lmin + h.S - p.L)) {
+            if (tail || (p.causal && last_key > lmin + h.S - h.Lb)) {
 #pragma unroll
                 for (int it = 0; it < C::IT; ++it) {
                     const int kl = kw0 + it * C::KPI + grp;
                     const int kg = h.key0 + kl;
                     const bool vis =
-                        kl < h.nvalid && (!p.causal || kg <= lrow_mine + h.S - p.L);
+                        kl < h.nvalid && (!p.causal || kg <= lrow_mine + h.S - h.Lb);
                     if (!vis) sc[it] = neg_inf();
                 }
             }
@@ -786,10 +856,7 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB) decode_split_kernel(const
                 s_abort = 1;
                 break;
             }
-            const int rows_valid = min(C::RB, p.G * p.L - h.chunk * C::RB);
-            const long long base_row =
-                (static_cast<long long>(h.b) * p.H_q + static_cast<long long>(h.kvh) * p.G) * p.L +
-                static_cast<long long>(h.chunk) * C::RB;
+            const int rows_valid = min(C::RB, p.G * h.Lb - h.chunk * C::RB);
             const long long slot = h.slot;
             // warp r merges row r (and r + NCW, ...), four dims per lane
             for (int r = warp; r < rows_valid; r += C::NCW) {
@@ -814,7 +881,8 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB) decode_split_kernel(const
                 }
                 if (h.flags & kFinal) {
                     const float inv = den > 0.f ? 1.f / den : 0.f;
-                    store4<T>(out, (base_row + r) * kD + 4 * lane,
+                    store4<T>(out, out_row(p, h.b, h.kvh, h.Lb, h.q0, h.chunk * C::RB + r) * kD +
+                                       4 * lane,
                               make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv));
                 } else {
                     *reinterpret_cast<float4*>(p.part_o + (slot * C::RB + r) * kD + 4 * lane) = acc;
@@ -842,24 +910,25 @@ template <class C>
 __global__ void __launch_bounds__(128) decode_combine_kernel(const DecodeParams p) {
     using T = typename C::Elem;
     pdl_wait_primary();
+    // segment ids number (b, kv head, row chunk) with p.nchunk chunks per kv
+    // head; sequence b has sw.nch <= p.nchunk of them
     const int seg = blockIdx.x;
-    const int segs_per_b = p.H_kv * p.nchunk;
-    const int b = seg / segs_per_b, sib = seg - b * segs_per_b;
-    const int kvh = sib / p.nchunk, chunk = sib - kvh * p.nchunk;
-    const int S = checked_len(p, b, false);
-    const int ng = (S + C::GRAN - 1) / C::GRAN;
-    const int rows_valid = min(C::RB, p.G * p.L - chunk * C::RB);
-    const long long base_row =
-        (static_cast<long long>(b) * p.H_q + static_cast<long long>(kvh) * p.G) * p.L +
-        static_cast<long long>(chunk) * C::RB;
+    const int b = seg / (p.H_kv * p.nchunk), kc = seg - b * (p.H_kv * p.nchunk);
+    const int kvh = kc / p.nchunk, chunk = kc - kvh * p.nchunk;
+    const SeqWork sw = seq_work<C::RB>(p, b, false);
+    if (chunk >= sw.nch) return;  // not this launch's rows
+    const int ng = (sw.S + C::GRAN - 1) / C::GRAN;
+    const int rows_valid = min(C::RB, p.G * sw.Lb - chunk * C::RB);
     T* const out = static_cast<T*>(p.out);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int d0 = lane * 4;
+    auto orow = [&](int r) { return out_row(p, b, kvh, sw.Lb, sw.q0, chunk * C::RB + r); };
     if (ng == 0) {
         for (int r = warp; r < rows_valid; r += 4)
-            store4<T>(out, (base_row + r) * kD + d0, make_float4(0.f, 0.f, 0.f, 0.f));
+            store4<T>(out, orow(r) * kD + d0, make_float4(0.f, 0.f, 0.f, 0.f));
         return;
     }
+    const int sib = kvh * sw.nch + chunk;  // the walker's segment order within b
     const int per = p.prefix[p.B + 1];
     const int first = p.prefix[b] + sib * ng;
     const int c0 = first / per, c1 = (first + ng - 1) / per;
@@ -898,7 +967,7 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(const DecodeParams 
             for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
         }
         const float inv = den > 0.f ? 1.f / den : 0.f;
-        store4<T>(out, (base_row + r) * kD + d0,
+        store4<T>(out, orow(r) * kD + d0,
                   make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv));
     }
 }
@@ -975,6 +1044,9 @@ pa_status launch_cfg(const Call& c) {
     p.scale_log2 = c.scale * 1.4426950408889634f;
     p.mask = c.mask;
     p.mask_S = c.mask_S;
+    p.cu_q = c.cu_q;
+    p.total_q = c.total_q;
+    p.route_mixed = c.route_mixed;
     p.tk_pages = C::TK / sh.page_size;
     p.tk_slots = C::TK % sh.page_size;
 
@@ -1012,6 +1084,15 @@ int decode_grid(const pa_shape& /*sh*/, int sm_count) { return sm_count > 0 ? sm
 
 size_t decode_workspace_bytes(const pa_shape& sh, int sm_count) {
     return ws_layout(sh, decode_grid(sh, sm_count), decode_rows_per_chunk(sh)).total;
+}
+
+size_t varlen_plan_offset(const pa_shape& sh, int sm_count) {
+    const size_t d = decode_workspace_bytes(sh, sm_count);
+    return align_up(d > kFlagBytes ? d : kFlagBytes, 256);
+}
+
+size_t workspace_bytes_total(const pa_shape& sh, int sm_count) {
+    return varlen_plan_offset(sh, sm_count) + 4 * (static_cast<size_t>(sh.B) + 2);
 }
 
 pa_status decode_launch(const Call& c) {

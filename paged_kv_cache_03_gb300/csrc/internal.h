@@ -46,6 +46,14 @@ struct Call {
     // capacity and a multiple of 4
     const float* mask = nullptr;
     long long mask_S = 0;
+    // ragged batch: query / output packed by token [total_q, H_q, D], sequence
+    // b owns tokens cu_q[b] .. cu_q[b + 1] - 1 (null: [B, H_q, L, D]); sh.L
+    // bounds every L_b
+    const int32_t* cu_q = nullptr;
+    int total_q = 0;
+    int route_mixed = 0;   // decode: sequences with L_b > sh.L belong to the tiles
+    int tiles_min_L = 0;   // tiles: only sequences with L_b > tiles_min_L
+    size_t plan_off = 0;   // workspace offset of the tile schedule's pair plan
     DeviceInfo dev;
 };
 
@@ -55,6 +63,13 @@ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 // Rows of one (b, kv_head) handled together by one pass over its keys.
 int decode_rows_per_chunk(const pa_shape& sh);
 size_t decode_workspace_bytes(const pa_shape& sh, int sm_count);
+// Ragged batches: the tile schedule's pair plan (B + 1 ints) follows the
+// decode schedule's workspace.
+size_t varlen_plan_offset(const pa_shape& sh, int sm_count);
+size_t workspace_bytes_total(const pa_shape& sh, int sm_count);
+// In a mixed ragged batch the page walk takes the sequences with at most this
+// many query rows per kv head (G * L_b), the tiles the rest.
+constexpr int kMixedDecodeRows = 4;
 int decode_grid(const pa_shape& sh, int sm_count);
 pa_status decode_launch(const Call& c);
 

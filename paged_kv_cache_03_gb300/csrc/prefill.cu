@@ -36,6 +36,7 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "internal.h"
@@ -77,7 +78,8 @@ enum Bar {
 };
 constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
 constexpr int kOffAbort = kOffTmemSlot + 8;
-constexpr int kSmemUsed = kOffAbort + 8;
+constexpr int kOffRows = kOffAbort + 8;  // output row (b, h, l) = base + h * sh + l * sl
+constexpr int kSmemUsed = kOffRows + 16;
 constexpr int kSmemBytes = kSmemUsed + 1024;  // slack to align the base
 
 struct PrefillParams {
@@ -90,9 +92,23 @@ struct PrefillParams {
     float scale_log2;
     const float* mask;  // optional additive mask [B * H_q, L, mask_S], or null
     long long mask_S;   // >= the table's capacity, a multiple of 4
+    // ragged batch (null cu_q: the [B, H_q, L, D] layout): rows packed by
+    // token [total_q, H_q, D]; sequence b owns tokens cu_q[b] .. cu_q[b+1]-1;
+    // pair_prefix[b] = query-tile pairs of sequences before b, [B] = all
+    const int32_t* cu_q;
+    const int* pair_prefix;
+    int total_q;
 };
 
 __device__ __forceinline__ float neg_inf() { return __int_as_float(0xff800000); }
+
+// Output rows of one CTA's sequence, in units of D elements: row (b, h, l)
+// is base + h * sh + l * sl ([B, H_q, L, D], or [tokens, H_q, D] from token
+// q0 on).  Kept in shared memory between the set-up and the epilogue.
+struct alignas(16) OutRows {
+    long long base;
+    int sh, sl;
+};
 
 // All 32 lanes wait; the warp agrees on the outcome (a lane that timed out
 // makes the whole warp give up, so warp-collective instructions stay uniform).
@@ -162,9 +178,10 @@ __device__ __forceinline__ void exp_pack(const float (&x)[4][32], float2 c2, flo
     }
 }
 
-// kMask: an explicit additive mask is read (a separate instantiation, so the
-// unmasked kernel carries none of its code or registers).
-template <bool kMask>
+// kMask: an explicit additive mask is read; kVarlen: a ragged batch (queries
+// packed by token, per-sequence query counts).  Separate instantiations, so
+// the plain kernel carries none of their code or registers.
+template <bool kMask, bool kVarlen>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tile_kernel(const __grid_constant__ CUtensorMap tm_q,
                         const __grid_constant__ CUtensorMap tm_k,
@@ -177,30 +194,52 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto bar = [&](int i) { return bar0 + 8u * static_cast<uint32_t>(i); };
     volatile int* const abort_flag = reinterpret_cast<volatile int*>(sbase + kOffAbort);
     uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(sbase + kOffTmemSlot);
+    OutRows* const out_rows = reinterpret_cast<OutRows*>(sbase + kOffRows);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
     // ---- which tiles ----------------------------------------------------------
-    const int per_m = p.H_kv * p.B;
-    const int mp = p.nPairs - 1 - static_cast<int>(blockIdx.x) / per_m;  // heavy pairs first
-    const int rest = static_cast<int>(blockIdx.x) % per_m;
-    const int b = rest / p.H_kv, kvh = rest % p.H_kv;
+    // (b, kv head, pair mp of 128-row query tiles); Lb query positions of
+    // sequence b, the first at token q0 (ragged batch)
+    int b, kvh, mp, Lb = p.L, q0 = 0, nM = p.nM;
+    if constexpr (kVarlen) {
+        const int i = static_cast<int>(blockIdx.x) / p.H_kv;
+        kvh = static_cast<int>(blockIdx.x) % p.H_kv;
+        if (i >= p.pair_prefix[p.B]) return;  // past the batch's pairs: before any set-up
+        int lo = 0, hi = p.B - 1;  // the last sequence whose pairs start at or before i
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (p.pair_prefix[mid] <= i) lo = mid;
+            else hi = mid - 1;
+        }
+        b = lo;
+        q0 = p.cu_q[b];
+        Lb = p.cu_q[b + 1] - q0;
+        nM = (Lb + p.Lt - 1) / p.Lt;
+        mp = (nM + 1) / 2 - 1 - (i - p.pair_prefix[b]);  // heavy pairs of a sequence first
+    } else {
+        const int per_m = p.H_kv * p.B;
+        mp = p.nPairs - 1 - static_cast<int>(blockIdx.x) / per_m;  // heavy pairs first
+        const int rest = static_cast<int>(blockIdx.x) % per_m;
+        b = rest / p.H_kv;
+        kvh = rest % p.H_kv;
+    }
     const int S = p.ctx[b];
     const bool valid_seq =
-        S >= 1 && static_cast<long long>(S) <= p.max_S && !(p.causal && S < p.L);
+        S >= 1 && static_cast<long long>(S) <= p.max_S && !(p.causal && S < Lb);
     int nk_t[2], lim_min_t[2], l0_t[2];
 #pragma unroll
     for (int t = 0; t < 2; ++t) {
         const int m = 2 * mp + t;
         l0_t[t] = m * p.Lt;
-        const bool exists = m < p.nM && valid_seq;
-        const int l_last = min(l0_t[t] + p.Lt, p.L) - 1;
-        const int lim_max = p.causal ? l_last + S - p.L : S - 1;  // last key any row sees
-        lim_min_t[t] = p.causal ? l0_t[t] + S - p.L : S - 1;      // last key row l0 sees
+        const bool exists = m < nM && valid_seq;
+        const int l_last = min(l0_t[t] + p.Lt, Lb) - 1;
+        const int lim_max = p.causal ? l_last + S - Lb : S - 1;  // last key any row sees
+        lim_min_t[t] = p.causal ? l0_t[t] + S - Lb : S - 1;      // last key row l0 sees
         nk_t[t] = exists ? lim_max / BN + 1 : 0;
     }
     const int nk = max(nk_t[0], nk_t[1]);
-    const int ntiles = (2 * mp + 1 < p.nM) ? 2 : 1;
+    const int ntiles = (2 * mp + 1 < nM) ? 2 : 1;
 
     // ---- set-up: barriers, V zeroed, TMEM --------------------------------------
     if (tid == 0) {
@@ -218,6 +257,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mbar_init(bar(kMmaDone), 1);
         *abort_flag = 0;
+        if constexpr (kVarlen) {
+            out_rows->base = static_cast<long long>(q0) * p.H_q;
+            out_rows->sh = 1;
+            out_rows->sl = p.H_q;
+        } else {
+            out_rows->base = static_cast<long long>(b) * p.H_q * p.L;
+            out_rows->sh = p.L;
+            out_rows->sl = 1;
+        }
         fence_mbar_init();
     }
     // key rows that are never loaded must hold finite values (their weight is
@@ -249,10 +297,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                                   static_cast<uint32_t>(ntiles * p.G * p.Lt * 128 * 2));
             for (int t = 0; t < ntiles; ++t)
                 for (int g = 0; g < p.G; ++g) {
-                    const int row = ((b * p.H_q) + kvh * p.G + g) * p.L + l0_t[t];
-                    for (int h = 0; h < 2; ++h)
-                        tc::tma_load_2d(base + kOffQ + t * kTile + h * kHalf + g * p.Lt * 128,
-                                        &tm_q, h * 64, row, bar(kQFull), pol_q);
+                    const uint32_t dst = base + kOffQ + t * kTile + g * p.Lt * 128;
+                    if constexpr (kVarlen) {  // map (D, H_q, tokens): Lt tokens of head kvh*G + g
+                        for (int h = 0; h < 2; ++h)
+                            tc::tma_load_3d(dst + h * kHalf, &tm_q, h * 64, kvh * p.G + g,
+                                            q0 + l0_t[t], bar(kQFull), pol_q);
+                    } else {
+                        const int row = ((b * p.H_q) + kvh * p.G + g) * p.L + l0_t[t];
+                        for (int h = 0; h < 2; ++h)
+                            tc::tma_load_2d(dst + h * kHalf, &tm_q, h * 64, row, bar(kQFull),
+                                            pol_q);
+                    }
                 }
         }
         __syncwarp();
@@ -370,9 +425,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int r = q4 * 32 + lane;       // query row of this thread
         const uint32_t trow = tmem + (static_cast<uint32_t>(q4 * 32) << 16);
         const int g = r / p.Lt, l = l0_t[t] + (r - g * p.Lt);
-        const bool row_valid = t < ntiles && g < p.G && l < p.L;
+        const bool row_valid = t < ntiles && g < p.G && l < Lb;
         const int h = kvh * p.G + g;
-        const int lim = min(p.causal ? l + S - p.L : S - 1, S - 1);
+        const int lim = min(p.causal ? l + S - Lb : S - 1, S - 1);
         const int nkt = nk_t[t];
         const float c = p.scale_log2;
         // with an explicit mask the scores are taken to log2 units (and the
@@ -508,7 +563,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc::fence_after_sync();
             const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
             uint16_t* const orow = static_cast<uint16_t*>(p.out) +
-                                   ((static_cast<long long>(b) * p.H_q + h) * p.L + l) * kD;
+                                   (out_rows->base + static_cast<long long>(h) * out_rows->sh +
+                                    static_cast<long long>(l) * out_rows->sl) * kD;
 #pragma unroll 1
             for (int cc = 0; cc < 4; ++cc) {
                 float o[32];
@@ -532,7 +588,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!valid_seq && row_valid) {
             uint4* orow = reinterpret_cast<uint4*>(
                 static_cast<uint16_t*>(p.out) +
-                ((static_cast<long long>(b) * p.H_q + h) * p.L + l) * kD);
+                (out_rows->base + static_cast<long long>(h) * out_rows->sh +
+                 static_cast<long long>(l) * out_rows->sl) * kD);
             for (int q = 0; q < kD / 8; ++q) orow[q] = make_uint4(0u, 0u, 0u, 0u);
         }
     }
@@ -544,6 +601,56 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::fence_after_sync();
         tc::tmem_dealloc(tmem, kTmemCols);
     }
+}
+
+// Ragged batch: pair_prefix[b] = query-tile pairs of the sequences before b
+// that the tile schedule takes (L_b > min_L), [B] = all.  A sequence whose
+// offsets are broken (cu_q[b] < 0, L_b < 0 or > max_L, cu_q[b+1] > total_q)
+// gets none and sets PA_FLAG_BAD_CONTEXT.  One CTA, a block scan per 1024
+// sequences.
+__global__ void __launch_bounds__(1024) pair_plan_kernel(const int32_t* cu_q, int B, int total_q,
+                                                         int Lt, int min_L, int max_L,
+                                                         uint32_t* flag, int* pair_prefix) {
+    __shared__ int warp_sums[32];
+    __shared__ int carry_s;
+    const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+    if (tid == 0) carry_s = 0;
+    __syncthreads();
+    for (int base = 0; base < B; base += 1024) {
+        const int b = base + tid;
+        int v = 0;
+        if (b < B) {
+            const int q0 = cu_q[b], q1 = cu_q[b + 1], Lb = q1 - q0;
+            const bool broken = q0 < 0 || Lb < 0 || Lb > max_L || q1 > total_q;
+            if (broken) atomicOr(flag, PA_FLAG_BAD_CONTEXT);
+            else if (Lb > min_L) v = ((Lb + Lt - 1) / Lt + 1) / 2;
+        }
+        int x = v;  // inclusive scan: warps, then warp totals
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, x, o);
+            if (lane >= o) x += y;
+        }
+        if (lane == 31) warp_sums[w] = x;
+        __syncthreads();
+        if (w == 0) {
+            int t = warp_sums[lane];
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, t, o);
+                if (lane >= o) t += y;
+            }
+            warp_sums[lane] = t;
+        }
+        __syncthreads();
+        const int incl = x + (w > 0 ? warp_sums[w - 1] : 0);
+        const int carry = carry_s;
+        if (b < B) pair_prefix[b] = carry + incl - v;
+        __syncthreads();
+        if (tid == 1023) carry_s = carry + incl;
+        __syncthreads();
+    }
+    if (tid == 0) pair_prefix[B] = carry_s;
 }
 
 // ---------------------------------------------------------------------------
@@ -575,6 +682,22 @@ bool make_map(CUtensorMap* map, const void* ptr, long long rows, int box_rows) {
     cuuint32_t box[2] = {64u, static_cast<cuuint32_t>(box_rows)};
     cuuint32_t estr[2] = {1u, 1u};
     return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Token-major query map (D, H_q, tokens): one box = box_rows tokens of one
+// head, laid out in shared memory exactly like a box of the 2-D map.
+bool make_map_tokens(CUtensorMap* map, const void* ptr, int H_q, long long tokens, int box_rows) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(H_q),
+                          static_cast<cuuint64_t>(tokens)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(kD) * 2,
+                             static_cast<cuuint64_t>(H_q) * kD * 2};
+    cuuint32_t box[3] = {64u, 1u, static_cast<cuuint32_t>(box_rows)};
+    cuuint32_t estr[3] = {1u, 1u, 1u};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box,
               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -614,16 +737,21 @@ pa_status prefill_launch(const Call& c) {
     const int box_rows = gcd_int(sh.page_size, BN);
     CUtensorMap tq, tk, tv;
     const long long pool_rows = static_cast<long long>(sh.num_pages) * sh.H_kv * sh.page_size;
-    if (!make_map(&tq, c.q, static_cast<long long>(sh.B) * sh.H_q * sh.L, Lt) ||
-        !make_map(&tk, c.kp, pool_rows, box_rows) || !make_map(&tv, c.vp, pool_rows, box_rows))
+    const bool q_ok = c.cu_q ? make_map_tokens(&tq, c.q, sh.H_q, c.total_q, Lt)
+                             : make_map(&tq, c.q, static_cast<long long>(sh.B) * sh.H_q * sh.L, Lt);
+    if (!q_ok || !make_map(&tk, c.kp, pool_rows, box_rows) ||
+        !make_map(&tv, c.vp, pool_rows, box_rows))
         return PA_ERR_CUDA;
 
     static int attr_done[64] = {0};
     if (c.dev.device >= 0 && c.dev.device < 64 && !attr_done[c.dev.device]) {
-        if (cudaFuncSetAttribute(prefill_tile_kernel<false>,
+        if (cudaFuncSetAttribute(prefill_tile_kernel<false, false>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  kSmemBytes) != cudaSuccess ||
-            cudaFuncSetAttribute(prefill_tile_kernel<true>,
+            cudaFuncSetAttribute(prefill_tile_kernel<true, false>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kSmemBytes) != cudaSuccess ||
+            cudaFuncSetAttribute(prefill_tile_kernel<false, true>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  kSmemBytes) != cudaSuccess)
             return PA_ERR_CUDA;
@@ -651,12 +779,31 @@ pa_status prefill_launch(const Call& c) {
     p.scale_log2 = c.scale * 1.4426950408889634f;
     p.mask = c.mask;
     p.mask_S = c.mask_S;
-    const unsigned grid = static_cast<unsigned>(static_cast<long long>(p.nPairs) * sh.H_kv * sh.B);
+    p.cu_q = c.cu_q;
+    p.total_q = c.total_q;
+    p.pair_prefix = nullptr;
+    long long pairs = static_cast<long long>(p.nPairs) * sh.B;
+    if (c.cu_q) {
+        // the pairs of all sequences are at most ceil(L_b / (2 Lt)) each, so at
+        // most (total_q + B (2 Lt - 1)) / (2 Lt) together; CTAs past the
+        // planned pairs return at once
+        pairs = std::min(pairs, (static_cast<long long>(c.total_q) +
+                                 static_cast<long long>(sh.B) * (2 * Lt - 1)) / (2 * Lt));
+        int* plan = reinterpret_cast<int*>(static_cast<uint8_t*>(c.ws) + c.plan_off);
+        p.pair_prefix = plan;
+        pair_plan_kernel<<<1, 1024, 0, c.stream>>>(c.cu_q, sh.B, c.total_q, Lt, c.tiles_min_L,
+                                                   sh.L, p.flag, plan);
+        if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
+        if (pairs == 0) return PA_OK;
+    }
+    const unsigned grid = static_cast<unsigned>(pairs * sh.H_kv);
     if (c.ev_before && cudaEventRecord(c.ev_before, c.stream) != cudaSuccess) return PA_ERR_CUDA;
-    if (c.mask)
-        prefill_tile_kernel<true><<<grid, kThreads, kSmemBytes, c.stream>>>(tq, tk, tv, p);
+    if (c.cu_q)  // (a ragged batch takes no explicit mask)
+        prefill_tile_kernel<false, true><<<grid, kThreads, kSmemBytes, c.stream>>>(tq, tk, tv, p);
+    else if (c.mask)
+        prefill_tile_kernel<true, false><<<grid, kThreads, kSmemBytes, c.stream>>>(tq, tk, tv, p);
     else
-        prefill_tile_kernel<false><<<grid, kThreads, kSmemBytes, c.stream>>>(tq, tk, tv, p);
+        prefill_tile_kernel<false, false><<<grid, kThreads, kSmemBytes, c.stream>>>(tq, tk, tv, p);
     if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
     if (c.ev_after && cudaEventRecord(c.ev_after, c.stream) != cudaSuccess) return PA_ERR_CUDA;
     return PA_OK;

@@ -178,3 +178,80 @@ def additive_mask_device(rows: int, L: int, S_mask: int, seed: int, device,
     m = torch.randn((rows, L, S_mask), generator=g, device=device, dtype=torch.float32)
     drop = torch.rand((rows, L, S_mask), generator=g, device=device) < removed
     return m.masked_fill_(drop, float("-inf"))
+
+
+@dataclasses.dataclass
+class RaggedInputs:
+    query: np.ndarray          # [T, H_q, D] packed by token (bf16 bits or float32)
+    key_pages: np.ndarray      # [P, H_kv, ps, D]
+    value_pages: np.ndarray
+    block_table: np.ndarray    # [B, max_pages_per_seq] int32
+    context_lens: np.ndarray   # [B] int32
+    cu_q: np.ndarray           # [B + 1] int32 query offsets
+    page_size: int
+    scale: float
+    causal: bool
+    dtype: str
+    name: str = ""
+
+    @property
+    def B(self):
+        return int(self.block_table.shape[0])
+
+    @property
+    def H_q(self):
+        return int(self.query.shape[1])
+
+    @property
+    def H_kv(self):
+        return int(self.key_pages.shape[1])
+
+    @property
+    def D(self):
+        return int(self.query.shape[2])
+
+    @property
+    def num_pages(self):
+        return int(self.key_pages.shape[0])
+
+    @property
+    def q_lens(self):
+        return np.diff(self.cu_q)
+
+    @property
+    def max_L(self):
+        return max(1, int(self.q_lens.max()))
+
+
+def generate_ragged(H_q, H_kv, D, page_size, q_lens, context_lens, seed=0, dtype="bf16",
+                    num_pages=None, max_pages_per_seq=None, k_scale=1.0, causal=True,
+                    scale=None, name="") -> RaggedInputs:
+    """A ragged batch: sequence b has q_lens[b] new queries (its last
+    positions) and context_lens[b] keys; pools and block table as in
+    generate(), queries packed by token."""
+    q_lens = np.asarray(q_lens, dtype=np.int64)
+    B = len(q_lens)
+    base = generate(B, H_q, H_kv, 1, D, page_size, context_lens=context_lens,
+                    num_pages=num_pages, max_pages_per_seq=max_pages_per_seq, seed=seed,
+                    dtype=dtype, k_scale=k_scale, causal=causal, scale=scale, name=name)
+    rng = np.random.default_rng(seed + 7919)
+    T = int(q_lens.sum())
+    query = _normal(rng, (T, H_q, D), dtype)
+    cu_q = np.concatenate([[0], np.cumsum(q_lens)]).astype(np.int32)
+    return RaggedInputs(query, base.key_pages, base.value_pages, base.block_table,
+                        base.context_lens, cu_q, page_size, base.scale, bool(causal), dtype, name)
+
+
+# A continuous-batching step (Qwen3-4B heads): 56 single-token decodes over
+# contexts U{128..4096} and 8 prefill chunks of 128 tokens (the serving
+# trace's prefill step) over contexts U{128..2048}, in one batch.
+def mixed_workload(seed=6, dtype="bf16") -> RaggedInputs:
+    rng = np.random.default_rng(seed)
+    n_dec, n_pre, chunk = 56, 8, 128
+    ctx_dec = rng.integers(128, 4096 + 1, size=n_dec)
+    ctx_pre = rng.integers(chunk, 2048 + 1, size=n_pre)
+    order = rng.permutation(n_dec + n_pre)  # decodes and chunks interleaved
+    q_lens = np.concatenate([np.ones(n_dec, np.int64), np.full(n_pre, chunk)])[order]
+    ctx = np.concatenate([ctx_dec, ctx_pre])[order]
+    return generate_ragged(32, 8, 128, 128, q_lens, ctx, seed=seed, dtype=dtype,
+                           max_pages_per_seq=4096 // 128, name="mixed")

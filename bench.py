@@ -8,6 +8,7 @@ Prints ONE JSON line.
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                   [--workload decode|prefill|tails|long_decode|tiny] [--op attention|append]
                   [--no-causal] [--mask]
+  python bench.py --workload mixed   (a ragged continuous-batching step)
 
 Default workload: batched decode, B=64, L=1, H_q=32, H_kv=8, D=128,
 page_size=128, context lengths U{128..4096}, scattered pages (seeded).
@@ -55,7 +56,8 @@ L2_FLUSH_BYTES = 256 << 20
 
 # Which quantity each workload is measured in.
 WORKLOAD_BOUND = {"decode": "hbm", "long_decode": "hbm", "tiny": "hbm", "prefill": "tensor",
-                  "tails": "tensor"}
+                  "tails": "tensor", "mixed": "hbm"}
+METRIC_MIXED = "paged-attn ragged batch (decode steps + prefill chunks), HBM GB/s (bf16, d128)"
 
 
 # ---------------------------------------------------------------------------
@@ -88,6 +90,29 @@ def algorithmic_flops(inp) -> int:
     """4 * H_q * D * visible pairs: a multiply-add per element of Q.K^T and
     of P.V."""
     return 4 * inp.H_q * inp.D * visible_pairs(inp)
+
+
+def ragged_bytes(r) -> int:
+    """Minimum bytes of one ragged-batch call: every visible K and V row of
+    each sequence with queries once, queries in and outputs out once, the
+    used block-table entries, context lengths and offsets."""
+    es = 2 if r.dtype == "bf16" else 4
+    lens = r.q_lens
+    ctx = r.context_lens.astype(np.int64)
+    live = lens > 0
+    kv = 2 * r.H_kv * r.D * es * int(ctx[live].sum())
+    qo = 2 * r.query.size * es
+    pages = int(sum((int(s) + r.page_size - 1) // r.page_size for s in ctx[live]))
+    return kv + qo + 4 * pages + 4 * r.B + 4 * (r.B + 1)
+
+
+def ragged_flops(r) -> int:
+    """4 * H_q * D per visible (query row, key) pair."""
+    tot = 0
+    for Lb, S in zip(r.q_lens, r.context_lens):
+        Lb, S = int(Lb), int(S)
+        tot += (Lb * (S - Lb) + Lb * (Lb + 1) // 2) if r.causal else Lb * S
+    return 4 * r.H_q * r.D * tot
 
 
 def mask_bytes(inp) -> int:
@@ -357,7 +382,8 @@ def run_ours(args):
     ctx = dev_tensor(inp.context_lens)
     out = torch.empty_like(q)
     shape = B.shape_of(q, kp, bt)
-    sched = B.pa_choose_schedule(shape)
+    sched = {"auto": B.pa_choose_schedule(shape), "decode": B.PA_SCHED_DECODE,
+             "prefill": B.PA_SCHED_PREFILL}[args.schedule]
     launches = B.pa_launch_count(shape, sched)
     ws = B.new_workspace(shape, device)
     stream = torch.cuda.current_stream(device)
@@ -536,6 +562,180 @@ def run_ours(args):
         v, secs, desc, cores = time_oracle(inp, args.cpu_seconds, unit_fn, mask_fn)
         line["cpu_baseline"] = {"value": round(v, 6), "unit": value_unit, "cores": cores,
                                 "kind": "oracle", "sample": desc, "seconds": round(secs, 3)}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    return line
+
+
+def ragged_sub_batch(r, n):
+    """The first n sequences of a ragged batch (same pool)."""
+    cu = r.cu_q[:n + 1]
+    return synth.RaggedInputs(np.ascontiguousarray(r.query[:int(cu[-1])]), r.key_pages,
+                              r.value_pages, np.ascontiguousarray(r.block_table[:n]),
+                              np.ascontiguousarray(r.context_lens[:n]), np.ascontiguousarray(cu),
+                              r.page_size, r.scale, r.causal, r.dtype, r.name)
+
+
+def ragged_desc(r) -> str:
+    lens = r.q_lens
+    n_dec = int((lens == 1).sum())
+    chunks = sorted(set(int(x) for x in lens if x > 1))
+    return (f"mixed: B={r.B} ({n_dec} decodes L=1 ctx~U[128,4096], {r.B - n_dec} prefill chunks "
+            f"L={chunks} ctx~U[128,2048]) total_q={int(r.cu_q[-1])} H_q={r.H_q} H_kv={r.H_kv} "
+            f"D={r.D} page_size={r.page_size} pool={r.num_pages} pages, causal, seed=6")
+
+
+def run_mixed(args):
+    """One step = one pa_paged_attention_varlen call over the continuous-
+    batching step (the device routes decodes to the page walk and chunks to
+    the tensor-core tiles)."""
+    import torch
+    from paged_kv_cache_03_gb300 import binding as B
+    world, rank, local = dist_env()
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist_init("nccl")
+    device = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(device)
+    B.load()
+    r = synth.mixed_workload()
+    bytes_step, flops_step = ragged_bytes(r), ragged_flops(r)
+
+    def dev_tensor(a, dt=None):
+        t = torch.from_numpy(np.ascontiguousarray(a))
+        return (t.view(dt) if dt is not None else t).to(device)
+
+    q = dev_tensor(r.query, torch.bfloat16)
+    kp, vp = dev_tensor(r.key_pages, torch.bfloat16), dev_tensor(r.value_pages, torch.bfloat16)
+    bt, ctx, cu = dev_tensor(r.block_table), dev_tensor(r.context_lens), dev_tensor(r.cu_q)
+    out = torch.empty_like(q)
+    shape = B.shape_of_varlen(q, kp, bt, r.max_L)
+    ws = B.new_workspace(shape, device)
+    stream = torch.cuda.current_stream(device)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+    T = int(r.cu_q[-1])
+    sched = {"auto": B.PA_SCHED_AUTO, "decode": B.PA_SCHED_DECODE,
+             "prefill": B.PA_SCHED_PREFILL}[args.schedule]
+
+    def call():
+        st = B.pa_paged_attention_varlen(shape, q, kp, vp, bt, ctx, cu, T, r.scale, r.causal, out,
+                                         ws, ws.numel(), stream, sched)
+        if st != B.PA_OK:
+            raise RuntimeError(f"pa_paged_attention_varlen: {B.status_str(st)}")
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        call()
+    torch.cuda.synchronize(device)
+    _, flag = B.pa_check_device_flag(ws, stream=stream)
+    if flag:
+        raise RuntimeError(f"device flag {flag:#x} after warm-up")
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
+    for e in ev:
+        for x in e:
+            x.record(stream)
+    torch.cuda.synchronize(device)
+    sampler = ClockSampler(device.index)
+    if rank == 0:
+        sampler.start()
+    barrier(device)
+    torch.cuda.synchronize(device)
+    for k in range(K):
+        flush.zero_()
+        ev[k][0].record(stream)
+        call()
+        ev[k][1].record(stream)
+    torch.cuda.synchronize(device)
+    barrier(device)
+    clocks = sampler.stop() if rank == 0 else None
+    step_ms = np.array([e[0].elapsed_time(e[1]) for e in ev])
+    _, flag = B.pa_check_device_flag(ws, stream=stream)
+    if flag:
+        raise RuntimeError(f"device flag {flag:#x} after timed steps")
+    value, t_max = aggregate(bytes_step, K, float(step_ms.sum()), world, device)
+    peaks, peaks_src = load_peaks()
+    achieved = bytes_step / (float(step_ms.mean()) * 1e-3) / 1e9
+    peak = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
+    # pair plan + tile kernel, page walk + combine, or both pairs
+    launches = {"auto": 4, "decode": 2, "prefill": 2}[args.schedule]
+    roofline = {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 4), "traffic": None,
+                "kernel": {"auto": "whole call (pair_plan + prefill_tile + decode_split + "
+                                   "decode_combine)",
+                           "decode": "whole call (decode_split + decode_combine)",
+                           "prefill": "whole call (pair_plan + prefill_tile)"}[args.schedule],
+                "kernel_ms_avg": round(float(step_ms.mean()), 5),
+                "kernel_ms_median": round(float(np.median(step_ms)), 5),
+                "peak_source": f"{peaks_src} (MEASURED_PEAKS.json)" if peaks_src == "measured"
+                else "fallback", "algorithmic_bytes": bytes_step,
+                "algorithmic_flops": flops_step,
+                "tensor_floor_ms": round(flops_step / (peaks.get(
+                    "bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]) * 1e12) * 1e3, 5)}
+    e2e = None
+    if not args.no_e2e:
+        host = {n: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
+                for n, a in (("q", r.query), ("kp", r.key_pages), ("vp", r.value_pages),
+                             ("bt", r.block_table), ("ctx", r.context_lens), ("cu", r.cu_q))}
+        dst = {"q": q, "kp": kp, "vp": vp, "bt": bt, "ctx": ctx, "cu": cu}
+        out_host = torch.empty(out.shape, dtype=torch.bfloat16).pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in host.values())
+        d2h = out.numel() * out.element_size()
+        Ke = max(3, min(args.e2e_steps, K))
+
+        def e2e_step():
+            for n, t in host.items():
+                dst[n].view(torch.uint8).view(-1).copy_(t.view(torch.uint8).view(-1),
+                                                        non_blocking=True)
+            call()
+            out_host.copy_(out, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize(device)
+        a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(Ke):
+            e2e_step()
+        b_.record(stream)
+        torch.cuda.synchronize(device)
+        e2e_ms = reduce_max(a.elapsed_time(b_), device)
+        e2e = {"value": round(bytes_step * Ke * world / (e2e_ms * 1e-3) / 1e9, 3), "unit": "GB/s",
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": Ke,
+               "ms_per_step": round(e2e_ms / Ke, 4),
+               "note": "pinned host query, pools, block table, context lengths and offsets "
+                       "copied to HBM, one call, output copied back, every step"}
+    line = {
+        "metric": METRIC_MIXED, "value": round(value / 1e9, 3), "unit": "GB/s", "n_gpus": world,
+        "steps": K, "warmup": args.warmup, "ms_per_step": round(t_max / K, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": r.dtype,
+        "data": "synthetic (seeded N(0,1) bf16, scattered pages)",
+        "config": {"workload": ragged_desc(r), "schedule": args.schedule,
+                   "l2": "flushed: 256 MiB write between timed steps (outside step events)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
+                   "algorithmic_bytes_per_step": bytes_step,
+                   "algorithmic_flops_per_step": flops_step},
+        "clocks": clocks, "e2e": e2e, "gpu_launches": K * launches, "roofline": roofline,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        import oracle
+        lib = oracle.load()
+        cores = oracle.host_cores()
+        n, dt = 1, 0.0
+        while True:
+            sub = ragged_sub_batch(r, n)
+            t0 = time.perf_counter()
+            lib.paged_attention_varlen(sub.query, sub.key_pages, sub.value_pages, sub.block_table,
+                                       sub.context_lens, sub.cu_q, sub.scale, sub.causal,
+                                       num_threads=cores)
+            dt = time.perf_counter() - t0
+            if dt >= args.cpu_seconds or n >= r.B:
+                break
+            n = min(r.B, max(n + 1, int(n * args.cpu_seconds / max(dt, 1e-3) * 0.9)))
+        line["cpu_baseline"] = {"value": round(ragged_bytes(sub) / dt / 1e9, 6), "unit": "GB/s",
+                                "cores": cores, "kind": "oracle",
+                                "sample": f"first {n} of {r.B} sequences, one oracle call",
+                                "seconds": round(dt, 3)}
     if rank == 0:
         print(json.dumps(line), flush=True)
     return line
@@ -732,15 +932,70 @@ def run_reference(args):
     return line
 
 
+def run_mixed_reference(args):
+    """--impl reference for the ragged step: the oracle on the host cores, a
+    bounded leading sub-batch per step."""
+    world, rank, _ = dist_env()
+    if world > 1 and rank != 0:
+        return None
+    import oracle
+    lib = oracle.load()
+    cores = oracle.host_cores()
+    r = synth.mixed_workload()
+    per_step = max(0.05, min(3.0, args.ref_budget / max(1, args.steps + args.warmup)))
+    n = 1
+    while n < r.B:
+        sub = ragged_sub_batch(r, n)
+        t0 = time.perf_counter()
+        lib.paged_attention_varlen(sub.query, sub.key_pages, sub.value_pages, sub.block_table,
+                                   sub.context_lens, sub.cu_q, sub.scale, sub.causal,
+                                   num_threads=cores)
+        dt = time.perf_counter() - t0
+        if dt >= per_step:
+            break
+        n = min(r.B, max(n + 1, int(n * per_step / max(dt, 1e-4) * 0.9)))
+    sub = ragged_sub_batch(r, n)
+
+    def step():
+        lib.paged_attention_varlen(sub.query, sub.key_pages, sub.value_pages, sub.block_table,
+                                   sub.context_lens, sub.cu_q, sub.scale, sub.causal,
+                                   num_threads=cores)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = time.perf_counter() - t0
+    v = ragged_bytes(sub) / 1e9 * args.steps / dt
+    desc = f"first {n} of {r.B} sequences per step, one full oracle call"
+    line = {"impl": "reference", "metric": METRIC_MIXED, "value": round(v, 6), "unit": "GB/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(dt / args.steps * 1e3, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded N(0,1) bf16, scattered pages)",
+            "config": {"workload": ragged_desc(r), "sample": desc},
+            "cpu_baseline": {"value": round(v, 6), "unit": "GB/s", "cores": cores,
+                             "kind": "oracle", "sample": desc},
+            "e2e": {"value": round(v, 6), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+    print(json.dumps(line), flush=True)
+    return line
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=sorted(synth.WORKLOADS), default="decode")
+    ap.add_argument("--workload", choices=sorted(synth.WORKLOADS) + ["mixed"], default="decode",
+                    help="mixed: a ragged continuous-batching step (decodes + prefill chunks)")
     ap.add_argument("--op", choices=["attention", "append"], default="attention",
                     help="the path (paged attention) or the K/V append before it")
+    ap.add_argument("--schedule", choices=["auto", "decode", "prefill"], default="auto",
+                    help="force a schedule (auto: the library's choice)")
     ap.add_argument("--no-causal", action="store_true",
                     help="every key of the context visible (mask=None) instead of causal")
     ap.add_argument("--mask", action="store_true",
@@ -760,6 +1015,10 @@ def main(argv=None):
                               "the append's reference arm is its oracle: see cpu_baseline"}))
             return None
         return run_append(args)
+    if args.workload == "mixed":
+        if args.op != "attention" or args.mask or args.no_causal:
+            ap.error("--workload mixed takes neither --op append, --mask nor --no-causal")
+        return run_mixed_reference(args) if args.impl == "reference" else run_mixed(args)
     if args.impl == "reference":
         if args.mask:
             print(json.dumps({"impl": "reference", "unavailable":

@@ -246,6 +246,7 @@ pa_status pa_paged_attention_varlen(const pa_shape* shape, const void* query,
     if (run_decode) {
         Call d = c;
         d.sh.L = dec_L;  // the largest L_b the page walk takes
+        d.overlap_prev = run_tiles;  // the two touch disjoint rows: run side by side
         st = decode_launch(d);
     }
     return st;

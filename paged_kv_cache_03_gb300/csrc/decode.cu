@@ -470,8 +470,13 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB) decode_split_kernel(const
     }
     __syncthreads();
     pdl_launch_dependents();
+    // Launched beside the tile kernel of a mixed ragged batch (as its
+    // programmatic dependent), this grid must not finish before that one:
+    // every exit waits for it, so stream order still covers both kernels.
+    // (Without a preceding programmatic launch the wait returns at once.)
     if (static_cast<int>(blockIdx.x) >= nchunks) {
         if (tid == 0) finish_chunk_counters(p, grid);
+        pdl_wait_primary();
         return;
     }
 
@@ -668,6 +673,7 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB) decode_split_kernel(const
             if (!mbar_wait(full0 + 8 * (k % C::NST), (k / C::NST) & 1))
                 atomicOr(p.flag, PA_FLAG_TIMEOUT);
         if (lane == 0) finish_chunk_counters(p, grid);
+        pdl_wait_primary();
         return;
     }
 
@@ -900,6 +906,7 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB) decode_split_kernel(const
         }
         if (h.flags & kLast) break;
     }
+    pdl_wait_primary();
 }
 
 // Merges the pieces of every segment that was split across CTAs (one CTA per
@@ -1051,8 +1058,22 @@ pa_status launch_cfg(const Call& c) {
     p.tk_slots = C::TK % sh.page_size;
 
     if (c.ev_before && cudaEventRecord(c.ev_before, c.stream) != cudaSuccess) return PA_ERR_CUDA;
-    decode_split_kernel<C><<<grid, C::THREADS, C::SMEM, c.stream>>>(p);
-    if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
+    if (c.overlap_prev) {  // may start while the preceding tile kernel runs
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(static_cast<unsigned>(grid));
+        cfg.blockDim = dim3(C::THREADS);
+        cfg.dynamicSmemBytes = C::SMEM;
+        cfg.stream = c.stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (cudaLaunchKernelEx(&cfg, decode_split_kernel<C>, p) != cudaSuccess) return PA_ERR_CUDA;
+    } else {
+        decode_split_kernel<C><<<grid, C::THREADS, C::SMEM, c.stream>>>(p);
+        if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
+    }
     if (c.ev_after && cudaEventRecord(c.ev_after, c.stream) != cudaSuccess) return PA_ERR_CUDA;
 
     cudaLaunchConfig_t cfg = {};

@@ -54,6 +54,7 @@ struct Call {
     int route_mixed = 0;   // decode: sequences with L_b > sh.L belong to the tiles
     int tiles_min_L = 0;   // tiles: only sequences with L_b > tiles_min_L
     size_t plan_off = 0;   // workspace offset of the tile schedule's pair plan
+    bool overlap_prev = false;  // decode: launch as the tile kernel's programmatic dependent
     DeviceInfo dev;
 };
 

@@ -203,6 +203,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // sequence b, the first at token q0 (ragged batch)
     int b, kvh, mp, Lb = p.L, q0 = 0, nM = p.nM;
     if constexpr (kVarlen) {
+        // a page walk over the batch's other sequences may start beside us
+        pdl_launch_dependents();
         const int i = static_cast<int>(blockIdx.x) / p.H_kv;
         kvh = static_cast<int>(blockIdx.x) % p.H_kv;
         if (i >= p.pair_prefix[p.B]) return;  // past the batch's pairs: before any set-up

@@ -150,13 +150,13 @@ struct SeqWork {
 };
 
 // From the raw values S_raw = context_lens[b], q0 = cu_q[b], q1 = cu_q[b + 1].
-template <int RB>
+template <int RB, bool kVar>
 __device__ __forceinline__ SeqWork seq_work_raw(const DecodeParams& p, int S_raw, int q0, int q1,
                                                 bool report) {
     SeqWork w;
     w.Lb = p.L;
     w.q0 = 0;
-    if (p.cu_q) {
+    if constexpr (kVar) {
         w.q0 = q0;
         w.Lb = q1 - w.q0;
         const bool broken = w.q0 < 0 || w.Lb < 0 || q1 > p.total_q || (!p.route_mixed && w.Lb > p.L);
@@ -167,7 +167,7 @@ __device__ __forceinline__ SeqWork seq_work_raw(const DecodeParams& p, int S_raw
             return w;
         }
     }
-    w.nch = (p.G * w.Lb + RB - 1) / RB;
+    w.nch = kVar ? (p.G * w.Lb + RB - 1) / RB : p.nchunk;
     const int S = S_raw;
     const bool bad = S < 1 || static_cast<long long>(S) > p.max_S || (p.causal && S < w.Lb);
     if (bad && report) atomicOr(p.flag, PA_FLAG_BAD_CONTEXT);
@@ -175,18 +175,19 @@ __device__ __forceinline__ SeqWork seq_work_raw(const DecodeParams& p, int S_raw
     return w;
 }
 
-template <int RB>
+template <int RB, bool kVar>
 __device__ __forceinline__ SeqWork seq_work(const DecodeParams& p, int b, bool report) {
-    const int q0 = p.cu_q ? __ldg(p.cu_q + b) : 0;
-    const int q1 = p.cu_q ? __ldg(p.cu_q + b + 1) : 0;
-    return seq_work_raw<RB>(p, __ldg(p.ctx + b), q0, q1, report);
+    const int q0 = kVar ? __ldg(p.cu_q + b) : 0;
+    const int q1 = kVar ? __ldg(p.cu_q + b + 1) : 0;
+    return seq_work_raw<RB, kVar>(p, __ldg(p.ctx + b), q0, q1, report);
 }
 
 // Row index (in units of D elements) of row rr = g * Lb + l of the (b, kv
 // head) block in the query / output layout.
+template <bool kVar>
 __device__ __forceinline__ long long out_row(const DecodeParams& p, int b, int kvh, int Lb, int q0,
                                              int rr) {
-    if (p.cu_q) {
+    if constexpr (kVar) {
         const int g = rr / Lb, l = rr - g * Lb;
         return static_cast<long long>(q0 + l) * p.H_q + static_cast<long long>(kvh) * p.G + g;
     }
@@ -293,26 +294,28 @@ __device__ __forceinline__ void walker_set(const DecodeParams& p, Walker<C>& w, 
 }
 
 // Requests the raw metadata of sequence w.b + 1 for the next walker_set.
-template <class C>
+template <class C, bool kVar>
 __device__ __forceinline__ void walker_look_ahead(const DecodeParams& p, Walker<C>& w) {
     w.S_ahead = w.b + 1 < p.B ? __ldg(p.ctx + w.b + 1) : 0;
-    w.qn_ahead = p.cu_q && w.b + 1 < p.B ? __ldg(p.cu_q + w.b + 2) : 0;
+    if constexpr (kVar) w.qn_ahead = w.b + 1 < p.B ? __ldg(p.cu_q + w.b + 2) : 0;
 }
 
-template <class C>
+template <class C, bool kVar>
 __device__ void walker_seek(const DecodeParams& p, int lane, Walker<C>& w) {
-    while (w.u >= w.bpref + p.H_kv * w.nch * w.ng) {
-        w.bpref += p.H_kv * w.nch * w.ng;
+    const int segs_plain = p.H_kv * p.nchunk;
+    while (w.u >= w.bpref + (kVar ? p.H_kv * w.nch : segs_plain) * w.ng) {
+        w.bpref += (kVar ? p.H_kv * w.nch : segs_plain) * w.ng;
         ++w.b;
-        walker_set<C>(p, w, seq_work<C::RB>(p, w.b, false));
+        walker_set<C>(p, w, seq_work<C::RB, kVar>(p, w.b, false));
     }
-    w.qn = p.cu_q ? __ldg(p.cu_q + w.b + 1) : 0;
-    walker_look_ahead<C>(p, w);
+    if constexpr (kVar) w.qn = __ldg(p.cu_q + w.b + 1);
+    walker_look_ahead<C, kVar>(p, w);
     const int loc = w.u - w.bpref;
     w.sib = loc / w.ng;
     w.g = loc - w.sib * w.ng;
-    w.kvh = w.sib / w.nch;
-    w.chunk_r = w.sib - w.kvh * w.nch;
+    const int nch = kVar ? w.nch : p.nchunk;
+    w.kvh = w.sib / nch;
+    w.chunk_r = w.sib - w.kvh * nch;
     w.key0 = w.g * C::GRAN;
     w.lp = w.key0 / p.ps;
     w.slot = w.key0 - w.lp * p.ps;
@@ -394,9 +397,12 @@ __device__ __forceinline__ void store4<float>(float* base, long long idx, float4
     *reinterpret_cast<float4*>(base + idx) = v;
 }
 
-template <class C>
+// F: 0 plain, 1 with an explicit mask, 2 a ragged batch.  Separate
+// instantiations, so the plain kernel carries none of the others' code.
+template <class C, int F>
 __global__ void __launch_bounds__(C::THREADS, C::MINB) decode_split_kernel(const DecodeParams p) {
     using T = typename C::Elem;
+    constexpr bool kMask = F == 1, kVar = F == 2;
     extern __shared__ __align__(128) uint8_t smem[];
     uint8_t* const stage0 = smem;
     float* const merge = reinterpret_cast<float*>(smem + C::NST * C::STAGE);
@@ -436,8 +442,9 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB) decode_split_kernel(const
     // claims further chunks from a counter, so SMs that stream faster take
     // more of them.
     // units of sequence b: its segments (kv heads x row chunks) x key units
+    const int segs_per_b = p.H_kv * p.nchunk;  // (the [B, H_q, L, D] layout)
     auto units_of = [&](int b, bool report) {
-        const SeqWork sw = seq_work<C::RB>(p, b, report);
+        const SeqWork sw = seq_work<C::RB, kVar>(p, b, report);
         return p.H_kv * sw.nch * ((sw.S + C::GRAN - 1) / C::GRAN);
     };
     int mine = 0;
@@ -496,8 +503,8 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB) decode_split_kernel(const
         w.u = w.cu0;
         w.b = s_start_b;
         w.bpref = s_start_pref;
-        walker_set<C>(p, w, seq_work<C::RB>(p, w.b, false));
-        walker_seek<C>(p, lane, w);
+        walker_set<C>(p, w, seq_work<C::RB, kVar>(p, w.b, false));
+        walker_seek<C, kVar>(p, lane, w);
         int issued = 0;
         for (int i = 0;; ++i) {
             // ---- this tile: keys [key0, key0 + nvalid) of segment (b, sib) ----
@@ -515,7 +522,7 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB) decode_split_kernel(const
             // page pieces: piece j covers page lp + j (lane j + 32 k handles it);
             // a tile spans at most TK / ps + 2 pages, one lane each unless ps < 4
             const int row0 = w.chunk_r * C::RB;
-            const int nrows = min(C::RB, p.G * w.Lb - row0);
+            const int nrows = min(C::RB, p.G * (kVar ? w.Lb : p.L) - row0);
             int pid[C::PIECE_ITERS], klo[C::PIECE_ITERS], kn[C::PIECE_ITERS];
             bool any_bad = false;
 #pragma unroll
@@ -555,7 +562,7 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB) decode_split_kernel(const
             // the explicit mask's rows of this tile go to L2 now, NST stages
             // before the consumers read them: [key0, key0 + nvalid) widened to
             // whole 16-byte words, inside the row (mask_S % 4 == 0, >= S)
-            if (p.mask && lane < nrows && nvalid > 0) {
+            if (kMask && lane < nrows && nvalid > 0) {
                 const int rg = row0 + lane, gq = rg / w.Lb, lq = rg - gq * w.Lb;
                 const int lo = w.key0 & ~3, hi = (w.key0 + nvalid + 3) & ~3;
                 bulk_prefetch_l2(p.mask + ((static_cast<long long>(w.b) * p.H_q +
@@ -595,14 +602,14 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB) decode_split_kernel(const
                 bulk_g2s(kdst + C::KBYTES + off, vp + row * C::ROW, nb, fb, pol);
             }
             if (start) {
-                if (!p.cu_q) {  // the segment's rows are contiguous
+                if constexpr (!kVar) {  // the segment's rows are contiguous
                     if (lane == 0)
                         bulk_g2s(smem_u32(st) + C::HDR,
-                                 qp + out_row(p, w.b, w.kvh, w.Lb, 0, row0) * C::ROW,
+                                 qp + out_row<false>(p, w.b, w.kvh, p.L, 0, row0) * C::ROW,
                                  static_cast<uint32_t>(nrows) * C::ROW, fb, pol);
                 } else if (lane < nrows) {  // one token-major row per lane
                     bulk_g2s(smem_u32(st) + C::HDR + lane * C::ROW,
-                             qp + out_row(p, w.b, w.kvh, w.Lb, w.q0, row0 + lane) * C::ROW,
+                             qp + out_row<true>(p, w.b, w.kvh, w.Lb, w.q0, row0 + lane) * C::ROW,
                              C::ROW, fb, pol);
                 }
             }
@@ -618,7 +625,7 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB) decode_split_kernel(const
                 w.cu0 = w.chunk * cu;
                 w.cu1 = min(w.cu0 + cu, total);
                 w.u = w.cu0;
-                walker_seek<C>(p, lane, w);
+                walker_seek<C, kVar>(p, lane, w);
             } else if (w.u >= seg_u1) {
                 // next segment: same sequence (next row chunk / kv head) or the next one
                 w.g = 0;
@@ -626,19 +633,19 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB) decode_split_kernel(const
                 w.lp = 0;
                 w.slot = 0;
                 ++w.sib;
-                if (++w.chunk_r == w.nch) {
+                if (++w.chunk_r == (kVar ? w.nch : p.nchunk)) {
                     w.chunk_r = 0;
                     ++w.kvh;
                 }
-                if (w.sib == p.H_kv * w.nch) {
+                if (w.sib == (kVar ? p.H_kv * w.nch : segs_per_b)) {
                     // next sequence with work (sequences with no keys are skipped)
                     do {
-                        w.bpref += p.H_kv * w.nch * w.ng;
+                        w.bpref += (kVar ? p.H_kv * w.nch : segs_per_b) * w.ng;
                         ++w.b;
-                        walker_set<C>(p, w, seq_work_raw<C::RB>(p, w.S_ahead, w.qn, w.qn_ahead,
-                                                                 false));
+                        walker_set<C>(p, w, seq_work_raw<C::RB, kVar>(p, w.S_ahead, w.qn,
+                                                                       w.qn_ahead, false));
                         w.qn = w.qn_ahead;
-                        walker_look_ahead<C>(p, w);
+                        walker_look_ahead<C, kVar>(p, w);
                         w.win0 = w.nb_win;
                         w.nb_win = w.b + 1 < p.B ? bt_entry(p, w.b + 1, lane) : -1;
                     } while (w.ng == 0);
@@ -712,9 +719,10 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB) decode_split_kernel(const
         if ((i & 7) == 0 && __any_sync(0xffffffffu, s_abort != 0)) break;
         const uint8_t* const st = stage0 + stage * C::STAGE;
         const StageHdr h = *reinterpret_cast<const StageHdr*>(st);
+        const int hLb = kVar ? h.Lb : p.L;  // the segment's query positions
 
         if (h.flags & kStart) {
-            const int rows = p.G * h.Lb - h.chunk * C::RB;
+            const int rows = p.G * hLb - h.chunk * C::RB;
             lmin = INT_MAX;
 #pragma unroll
             for (int r = 0; r < C::RB; ++r) {
@@ -725,9 +733,9 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB) decode_split_kernel(const
                     q2[r][e].y *= p.scale_log2;
                 }
                 o4[r][0] = o4[r][1] = make_float2(0.f, 0.f);
-                lmin = min(lmin, r < rows ? (h.chunk * C::RB + r) % h.Lb : h.Lb - 1);
+                lmin = min(lmin, r < rows ? (h.chunk * C::RB + r) % hLb : hLb - 1);
             }
-            lrow_mine = rho < rows ? (h.chunk * C::RB + rho) % h.Lb : h.Lb - 1;
+            lrow_mine = rho < rows ? (h.chunk * C::RB + rho) % hLb : hLb - 1;
             m_mine = neg_inf();
             l_mine = 0.f;
         }
@@ -739,12 +747,12 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB) decode_split_kernel(const
             // An explicit additive mask joins the score of (key, row) in log2
             // units before the max; its loads go out before the dot products.
             float mv[C::IT];
-            if (p.mask) {
+            if constexpr (kMask) {
                 const int rg = h.chunk * C::RB + rho;  // row of the (b, kv head) block
-                const bool rok = rg < p.G * h.Lb;
-                const int gq = rg / h.Lb, lq = rg - gq * h.Lb;
+                const bool rok = rg < p.G * hLb;
+                const int gq = rg / hLb, lq = rg - gq * hLb;
                 const float* mrow = p.mask + ((static_cast<long long>(h.b) * p.H_q +
-                                               h.kvh * p.G + gq) * h.Lb + lq) * p.mask_S +
+                                               h.kvh * p.G + gq) * hLb + lq) * p.mask_S +
                                     h.key0;
 #pragma unroll
                 for (int it = 0; it < C::IT; ++it) {
@@ -768,7 +776,7 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB) decode_split_kernel(const
                 }
                 sc[it] = transpose_reduce<C::RB, C::P>(d, li);
             }
-            if (p.mask) {
+            if constexpr (kMask) {
 #pragma unroll
                 for (int it = 0; it < C::IT; ++it) sc[it] += mv[it] * 1.4426950408889634f;
             }
@@ -776,13 +784,13 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB) decode_split_kernel(const
             // past the context or past a row's causal frontier get -inf.
             const int last_key = h.key0 + kw0 + C::KPW - 1;
             const bool tail = h.nvalid < kw0 + C::KPW;
-            if (tail || (p.causal && last_key > lmin + h.S - h.Lb)) {
+            if (tail || (p.causal && last_key > lmin + h.S - hLb)) {
 #pragma unroll
                 for (int it = 0; it < C::IT; ++it) {
                     const int kl = kw0 + it * C::KPI + grp;
                     const int kg = h.key0 + kl;
                     const bool vis =
-                        kl < h.nvalid && (!p.causal || kg <= lrow_mine + h.S - h.Lb);
+                        kl < h.nvalid && (!p.causal || kg <= lrow_mine + h.S - hLb);
                     if (!vis) sc[it] = neg_inf();
                 }
             }
@@ -862,7 +870,7 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB) decode_split_kernel(const
                 s_abort = 1;
                 break;
             }
-            const int rows_valid = min(C::RB, p.G * h.Lb - h.chunk * C::RB);
+            const int rows_valid = min(C::RB, p.G * hLb - h.chunk * C::RB);
             const long long slot = h.slot;
             // warp r merges row r (and r + NCW, ...), four dims per lane
             for (int r = warp; r < rows_valid; r += C::NCW) {
@@ -887,8 +895,9 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB) decode_split_kernel(const
                 }
                 if (h.flags & kFinal) {
                     const float inv = den > 0.f ? 1.f / den : 0.f;
-                    store4<T>(out, out_row(p, h.b, h.kvh, h.Lb, h.q0, h.chunk * C::RB + r) * kD +
-                                       4 * lane,
+                    store4<T>(out,
+                              out_row<kVar>(p, h.b, h.kvh, hLb, h.q0, h.chunk * C::RB + r) * kD +
+                                  4 * lane,
                               make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv));
                 } else {
                     *reinterpret_cast<float4*>(p.part_o + (slot * C::RB + r) * kD + 4 * lane) = acc;
@@ -913,7 +922,7 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB) decode_split_kernel(const
 // segment, one warp per row, four dims per lane; the pieces' (m, l) are read
 // by the lanes in parallel), and writes zeros for sequences whose context
 // length broke the contract.
-template <class C>
+template <class C, bool kVar>
 __global__ void __launch_bounds__(128) decode_combine_kernel(const DecodeParams p) {
     using T = typename C::Elem;
     pdl_wait_primary();
@@ -922,14 +931,14 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(const DecodeParams 
     const int seg = blockIdx.x;
     const int b = seg / (p.H_kv * p.nchunk), kc = seg - b * (p.H_kv * p.nchunk);
     const int kvh = kc / p.nchunk, chunk = kc - kvh * p.nchunk;
-    const SeqWork sw = seq_work<C::RB>(p, b, false);
+    const SeqWork sw = seq_work<C::RB, kVar>(p, b, false);
     if (chunk >= sw.nch) return;  // not this launch's rows
     const int ng = (sw.S + C::GRAN - 1) / C::GRAN;
     const int rows_valid = min(C::RB, p.G * sw.Lb - chunk * C::RB);
     T* const out = static_cast<T*>(p.out);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int d0 = lane * 4;
-    auto orow = [&](int r) { return out_row(p, b, kvh, sw.Lb, sw.q0, chunk * C::RB + r); };
+    auto orow = [&](int r) { return out_row<kVar>(p, b, kvh, sw.Lb, sw.q0, chunk * C::RB + r); };
     if (ng == 0) {
         for (int r = warp; r < rows_valid; r += 4)
             store4<T>(out, orow(r) * kD + d0, make_float4(0.f, 0.f, 0.f, 0.f));
@@ -1004,6 +1013,51 @@ WsLayout ws_layout(const pa_shape& sh, int grid, int RB) {
     return w;
 }
 
+template <class C, int F>
+pa_status launch_split_combine(const Call& c, const DecodeParams& p, int grid, long long nseg) {
+    static int attr_done[64] = {0};
+    if (c.dev.device >= 0 && c.dev.device < 64 && !attr_done[c.dev.device]) {
+        if (cudaFuncSetAttribute(decode_split_kernel<C, F>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 C::SMEM) != cudaSuccess)
+            return PA_ERR_CUDA;
+        attr_done[c.dev.device] = 1;
+    }
+    if (c.ev_before && cudaEventRecord(c.ev_before, c.stream) != cudaSuccess) return PA_ERR_CUDA;
+    if (c.overlap_prev) {  // may start while the preceding tile kernel runs
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(static_cast<unsigned>(grid));
+        cfg.blockDim = dim3(C::THREADS);
+        cfg.dynamicSmemBytes = C::SMEM;
+        cfg.stream = c.stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (cudaLaunchKernelEx(&cfg, decode_split_kernel<C, F>, p) != cudaSuccess)
+            return PA_ERR_CUDA;
+    } else {
+        decode_split_kernel<C, F><<<grid, C::THREADS, C::SMEM, c.stream>>>(p);
+        if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
+    }
+    if (c.ev_after && cudaEventRecord(c.ev_after, c.stream) != cudaSuccess) return PA_ERR_CUDA;
+
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(nseg));
+    cfg.blockDim = dim3(128);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = c.stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, decode_combine_kernel<C, F == 2>, p) != cudaSuccess)
+        return PA_ERR_CUDA;
+    return PA_OK;
+}
+
 template <class C>
 pa_status launch_cfg(const Call& c) {
     const pa_shape& sh = c.sh;
@@ -1016,13 +1070,6 @@ pa_status launch_cfg(const Call& c) {
                                                sh.page_size + C::GRAN - 1) / C::GRAN);
     if (max_units >= INT_MAX / 2) return PA_ERR_UNSUPPORTED;
 
-    static int attr_done[64] = {0};
-    if (c.dev.device >= 0 && c.dev.device < 64 && !attr_done[c.dev.device]) {
-        if (cudaFuncSetAttribute(decode_split_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 C::SMEM) != cudaSuccess)
-            return PA_ERR_CUDA;
-        attr_done[c.dev.device] = 1;
-    }
     uint8_t* ws = static_cast<uint8_t*>(c.ws);
     DecodeParams p;
     p.q = c.q;
@@ -1057,37 +1104,9 @@ pa_status launch_cfg(const Call& c) {
     p.tk_pages = C::TK / sh.page_size;
     p.tk_slots = C::TK % sh.page_size;
 
-    if (c.ev_before && cudaEventRecord(c.ev_before, c.stream) != cudaSuccess) return PA_ERR_CUDA;
-    if (c.overlap_prev) {  // may start while the preceding tile kernel runs
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(static_cast<unsigned>(grid));
-        cfg.blockDim = dim3(C::THREADS);
-        cfg.dynamicSmemBytes = C::SMEM;
-        cfg.stream = c.stream;
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        attr[0].val.programmaticStreamSerializationAllowed = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        if (cudaLaunchKernelEx(&cfg, decode_split_kernel<C>, p) != cudaSuccess) return PA_ERR_CUDA;
-    } else {
-        decode_split_kernel<C><<<grid, C::THREADS, C::SMEM, c.stream>>>(p);
-        if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
-    }
-    if (c.ev_after && cudaEventRecord(c.ev_after, c.stream) != cudaSuccess) return PA_ERR_CUDA;
-
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(w.nseg));
-    cfg.blockDim = dim3(128);
-    cfg.dynamicSmemBytes = 0;
-    cfg.stream = c.stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, decode_combine_kernel<C>, p) != cudaSuccess) return PA_ERR_CUDA;
-    return PA_OK;
+    if (c.cu_q) return launch_split_combine<C, 2>(c, p, grid, w.nseg);
+    if (c.mask) return launch_split_combine<C, 1>(c, p, grid, w.nseg);
+    return launch_split_combine<C, 0>(c, p, grid, w.nseg);
 }
 
 }  // namespace

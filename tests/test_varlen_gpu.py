@@ -213,3 +213,20 @@ def test_varlen_argument_checks():
     assert call(o=None) == B.PA_ERR_INVALID_ARG
     assert call(total_q=0) == B.PA_OK
     torch.cuda.synchronize()
+
+
+def test_varlen_many_sequences(oracle_lib):
+    """1500 sequences (more than one 1024-wide scan block in the tile plan and
+    several in the page walk's prologue): decode steps, empty sequences and
+    a 40-token chunk every 50th sequence."""
+    rng = np.random.default_rng(460)
+    B = 1500
+    q_lens = np.ones(B, dtype=np.int64)
+    q_lens[::50] = 40
+    q_lens[7::97] = 0
+    ctx = rng.integers(40, 401, size=B)
+    inp = synth.generate_ragged(8, 2, 128, 16, q_lens, ctx, seed=461, name="many")
+    ref = oracle_varlen(oracle_lib, inp)
+    for sched in SCHEDULES:
+        got = gu.out_to_f64(run_varlen(inp, sched)[0])
+        gu.assert_parity(got, ref, "bf16", f"1500 sequences sched {sched}")

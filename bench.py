@@ -443,12 +443,19 @@ def run_ours(args):
     barrier(device)
     torch.cuda.synchronize(device)
     wall0 = time.perf_counter()
+    # Pass 1, the step: the call exactly as a user makes it.  (Events recorded
+    # inside the call would sit between its kernels and stop the combine from
+    # starting early: 7 us of a 125 us decode step.)
     for k in range(K):
         flush.zero_()  # L2 flush between timed steps (outside the step's events)
         e = ev[k]
         e[0].record(stream)
-        call(e[1], e[2])
+        call()
         e[3].record(stream)
+    # Pass 2, the dominant kernel: the same K calls with events around it.
+    for k in range(K):
+        flush.zero_()
+        call(ev[k][1], ev[k][2])
     torch.cuda.synchronize(device)
     barrier(device)
     wall = time.perf_counter() - wall0
@@ -558,7 +565,9 @@ def run_ours(args):
                    **({"mask": f"fp32 [B*H_q, L, {mask.shape[2]}], N(0,1) biases, 1/3 -inf, "
                                f"seed 4343 (device draw); {mask_bytes(inp)} visible bytes"}
                       if mask is not None else {})},
-        "clocks": clocks, "e2e": e2e, "gpu_launches": K * launches, "roofline": roofline,
+        "clocks": clocks, "e2e": e2e, "gpu_launches": 2 * K * launches, "roofline": roofline,
+        "timing": "steps: K calls as a user makes them; kernel: a second pass of K calls "
+                  "with events around the dominant kernel, same timed region",
         "step_ms_median": round(float(np.median(step_ms)), 5),
         "wall_s_timed_region": round(wall, 3),
     }

@@ -139,8 +139,9 @@ static void gather_one(const oracle_shape* sh, const void* key_pages, const void
  * x is scratch for S scores, o receives D outputs.  mask_row, when not NULL,
  * is the row's additive mask over logical key positions: it is added to the
  * scaled score before the softmax ("Week 2 Day 5: Fused Decode Attention",
- * Task 1, step 3: the score is scaled, then masked, then the causal rule applies).  A row whose every visible
- * score is -inf has no softmax; its output is 0. */
+ * Task 1, step 3: the score is scaled, then masked, then the causal rule
+ * applies).  A row whose every visible score is -inf has no softmax; its
+ * output is 0. */
 static void attend_row(const oracle_shape* sh, const void* query, int64_t qbase, int l, int L,
                        int S, const double* K, const double* V, double scale, int causal,
                        const float* mask_row, double* x, double* o) {

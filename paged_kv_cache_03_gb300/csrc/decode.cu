@@ -159,7 +159,8 @@ __device__ __forceinline__ SeqWork seq_work_raw(const DecodeParams& p, int S_raw
     if constexpr (kVar) {
         w.q0 = q0;
         w.Lb = q1 - w.q0;
-        const bool broken = w.q0 < 0 || w.Lb < 0 || q1 > p.total_q || (!p.route_mixed && w.Lb > p.L);
+        const bool broken =
+            w.q0 < 0 || w.Lb < 0 || q1 > p.total_q || (!p.route_mixed && w.Lb > p.L);
         if (broken || w.Lb == 0 || w.Lb > p.L) {
             if (broken && report) atomicOr(p.flag, PA_FLAG_BAD_CONTEXT);
             w.S = 0;

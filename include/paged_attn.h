@@ -168,6 +168,17 @@ pa_status pa_paged_attention_varlen(const pa_shape* shape, const void* query,
                                     void* out, void* workspace, size_t workspace_bytes,
                                     void* cuda_stream, int schedule);
 
+/* Self-test of the failure path of the kernels' bounded on-chip waits (every
+ * mbarrier wait gives up after 2 s instead of hanging): one warp waits, with the
+ * same wait, on a barrier phase that nothing completes.  After timeout_us
+ * (at most 2,000,000) the wait gives up, PA_FLAG_TIMEOUT is recorded in the
+ * workspace's flag word and the kernel returns, leaving the context usable.
+ * No fault, no trap.  Asynchronous on cuda_stream.  Returns PA_ERR_WORKSPACE
+ * for a missing or misaligned workspace, PA_ERR_INVALID_ARG for a longer
+ * timeout. */
+pa_status pa_selftest_wait_timeout(void* workspace, size_t workspace_bytes,
+                                   unsigned timeout_us, void* cuda_stream);
+
 /* Debug gather of "Week 3 Day 5", Task 1: writes the dense history of every
  * (b, kv_head) through the block table, k_dense/v_dense [B, H_kv, max_S, D]
  * in the pool's dtype, zeros at s >= context_lens[b].  Page translation is

@@ -106,6 +106,8 @@ def load(auto_build: bool = True):
                                                   ctypes.c_float, ctypes.c_int, vp, vp, sz, vp,
                                                   ctypes.c_int]
         lib.pa_paged_attention_varlen.restype = ctypes.c_int
+        lib.pa_selftest_wait_timeout.argtypes = [vp, sz, ctypes.c_uint, vp]
+        lib.pa_selftest_wait_timeout.restype = ctypes.c_int
         lib.pa_append_kv.argtypes = [sp, vp, vp, vp, vp, i32p, i32p, vp, sz, vp]
         lib.pa_append_kv.restype = ctypes.c_int
         lib.pa_status_str.argtypes = [ctypes.c_int]
@@ -232,6 +234,11 @@ def pa_paged_attention_varlen(shape, query, key_pages, value_pages, block_table,
         ctypes.byref(shape), _ptr(query), _ptr(key_pages), _ptr(value_pages), _ptr(block_table),
         _ptr(context_lens), _ptr(cu_q), int(total_q), float(scale), int(bool(causal)),
         _ptr(out), _ptr(workspace), int(workspace_bytes), _stream(stream), int(schedule))
+
+
+def pa_selftest_wait_timeout(workspace, workspace_bytes, timeout_us, stream=None) -> int:
+    return load().pa_selftest_wait_timeout(_ptr(workspace), int(workspace_bytes),
+                                           int(timeout_us), _stream(stream))
 
 
 def pa_append_kv(shape, k_new, v_new, key_pages, value_pages, block_table, context_lens,

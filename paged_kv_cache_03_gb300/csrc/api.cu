@@ -7,6 +7,7 @@
 #include <vector>
 
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace pa {
 
@@ -250,6 +251,18 @@ pa_status pa_paged_attention_varlen(const pa_shape* shape, const void* query,
         st = decode_launch(d);
     }
     return st;
+}
+
+pa_status pa_selftest_wait_timeout(void* workspace, size_t workspace_bytes,
+                                   unsigned timeout_us, void* cuda_stream) {
+    if (!workspace || !aligned(workspace, 256) || workspace_bytes < kFlagBytes)
+        return PA_ERR_WORKSPACE;
+    if (timeout_us > kWaitTimeoutNs / 1000) return PA_ERR_INVALID_ARG;
+    DeviceInfo dev;
+    const pa_status st = current_device_info(&dev);
+    if (st != PA_OK) return st;
+    return wait_timeout_launch(static_cast<uint32_t*>(workspace), 1000ull * timeout_us,
+                               static_cast<cudaStream_t>(cuda_stream));
 }
 
 pa_status pa_gather_debug(const pa_shape* shape, const void* key_pages, const void* value_pages,

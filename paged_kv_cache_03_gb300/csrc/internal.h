@@ -83,6 +83,9 @@ pa_status append_launch(const pa_shape& sh, const void* k_new, const void* v_new
                         void* vp, const int32_t* bt, const int32_t* ctx, uint32_t* flag,
                         int sm_count, cudaStream_t stream);
 
+// ---- self-test of the bounded waits ---------------------------------------
+pa_status wait_timeout_launch(uint32_t* flag, unsigned long long limit_ns, cudaStream_t stream);
+
 // ---- debug gather ---------------------------------------------------------
 pa_status gather_launch(const pa_shape& sh, const void* kp, const void* vp, const int32_t* bt,
                         const int32_t* ctx, int max_S, void* kd, void* vd, uint32_t* flag,

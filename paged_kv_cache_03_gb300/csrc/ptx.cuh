@@ -58,16 +58,22 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Waits for the phase of `bar` with the given parity to complete; returns
-// false (never hangs) once kWaitTimeoutNs has passed.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+// false (never hangs) once limit_ns have passed.
+__device__ __forceinline__ bool mbar_wait_for(uint32_t bar, uint32_t parity,
+                                              unsigned long long limit_ns) {
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = globaltimer_ns();
     for (;;) {
 #pragma unroll 1
         for (int i = 0; i < 32; ++i)
             if (mbar_try_wait(bar, parity)) return true;
-        if (globaltimer_ns() - t0 > kWaitTimeoutNs) return false;
+        if (globaltimer_ns() - t0 > limit_ns) return false;
     }
+}
+
+// The kernels' wait: gives up after kWaitTimeoutNs.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+    return mbar_wait_for(bar, parity, kWaitTimeoutNs);
 }
 
 __device__ __forceinline__ uint64_t l2_policy_evict_first() {

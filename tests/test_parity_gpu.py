@@ -328,3 +328,27 @@ def test_paged_attention_wrapper(oracle_lib):
                             scale=inp.scale, causal=True)
     torch.cuda.synchronize()
     gu.assert_parity(gu.out_to_f64(out), gu.oracle_full(oracle_lib, inp), "bf16", "wrapper")
+
+
+def test_bounded_wait_gives_up_and_the_context_survives(oracle_lib):
+    """The kernels' mbarrier wait on a phase that nothing completes gives up
+    after its limit, records PA_FLAG_TIMEOUT and returns; the context stays
+    usable (a normal call right after matches the oracle)."""
+    import time
+    import torch
+    ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    assert B.pa_selftest_wait_timeout(ws, ws.numel(), 20000) == B.PA_OK
+    torch.cuda.synchronize()
+    waited = time.perf_counter() - t0
+    _, flag = B.pa_check_device_flag(ws)
+    assert flag & B.PA_FLAG_TIMEOUT
+    assert waited >= 0.02
+    assert B.pa_selftest_wait_timeout(ws, ws.numel(), 3_000_000) == B.PA_ERR_INVALID_ARG
+    assert B.pa_selftest_wait_timeout(None, 0, 1000) == B.PA_ERR_WORKSPACE
+    inp = synth.workload("tiny")
+    out, flag = gu.run(inp)
+    assert flag == 0
+    gu.assert_parity(gu.out_to_f64(out), gu.oracle_full(oracle_lib, inp), "bf16",
+                     "call after a timed-out wait")

@@ -82,6 +82,10 @@ CASES = [
     ("full-visibility", 8, 2, 16, [1, 7, 40, 1], [30, 7, 500, 2], False, 404),
     ("page128-long", 32, 8, 128, [1, 128, 1, 256], [4000, 1500, 129, 3000], True, 405),
     ("page8-tiles-edge", 8, 2, 8, [33, 1, 64], [33, 17, 200], True, 406),
+    # page sizes the tiles do not take: the page walk serves every sequence,
+    # a tile of keys spanning many page pieces
+    ("page3-walk-only", 8, 2, 3, [1, 0, 9, 2], [40, 5, 100, 7], True, 407),
+    ("page1-walk-only", 4, 4, 1, [3, 1], [50, 20], True, 408),
 ]
 
 

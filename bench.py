@@ -7,12 +7,19 @@ Prints ONE JSON line.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                   [--workload decode|prefill|tails|long_decode|tiny] [--op attention|append]
-                  [--no-causal] [--mask]
+                  [--schedule auto|decode|prefill] [--no-causal] [--mask]
   python bench.py --workload mixed   (a ragged continuous-batching step)
 
 Default workload: batched decode, B=64, L=1, H_q=32, H_kv=8, D=128,
 page_size=128, context lengths U{128..4096}, scattered pages (seeded).
-Metric: achieved HBM GB/s = algorithmic bytes / device time (bf16).
+Metric: achieved HBM GB/s = algorithmic bytes / device time (bf16), or TFLOP/s
+= 4 * H_q * D * visible (row, key) pairs / device time where the FLOP time at
+the measured bf16 rate exceeds the byte time at the measured copy bandwidth
+(the causal prefill).
+
+The timed region holds two passes of K steps: the call as a user makes it
+(value, ms_per_step) and the same calls with CUDA events around the dominant
+kernel (roofline.achieved); L2 is flushed between steps.
 
 --impl reference times the fp64 CPU oracle on the host cores over a bounded
 sample of the same workload (the method has no other reference program).

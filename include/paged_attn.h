@@ -229,6 +229,17 @@ pa_status pa_check_device_flag(void* workspace, uint32_t* flag_out, int clear, v
 pa_status pa_validate_metadata(const pa_shape* shape, const int32_t* block_table,
                                const int32_t* context_lens, int causal, void* cuda_stream);
 
+/* pa_validate_metadata for a ragged batch (copies cu_q, context_lens and
+ * block_table to the host, synchronising the stream): PA_ERR_INVALID_ARG for
+ * cu_q[0] != 0, cu_q[B] != total_q, an L_b outside [0, shape->L], or a
+ * sequence with queries whose context length is outside [max(1, causal ? L_b
+ * : 1), max_pages_per_seq * page_size]; PA_ERR_BAD_BLOCK_TABLE for an entry a
+ * sequence with queries reads outside [0, num_pages).  Sequences with L_b = 0
+ * are not checked (they are not read).  Meant for debugging. */
+pa_status pa_validate_metadata_varlen(const pa_shape* shape, const int32_t* block_table,
+                                      const int32_t* context_lens, const int32_t* cu_q,
+                                      int total_q, int causal, void* cuda_stream);
+
 /* The schedule pa_paged_attention would pick for this shape (PA_SCHED_*),
  * or -1 for an invalid shape. */
 int pa_choose_schedule(const pa_shape* shape);

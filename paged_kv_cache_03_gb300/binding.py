@@ -106,6 +106,9 @@ def load(auto_build: bool = True):
                                                   ctypes.c_float, ctypes.c_int, vp, vp, sz, vp,
                                                   ctypes.c_int]
         lib.pa_paged_attention_varlen.restype = ctypes.c_int
+        lib.pa_validate_metadata_varlen.argtypes = [sp, i32p, i32p, i32p, ctypes.c_int,
+                                                    ctypes.c_int, vp]
+        lib.pa_validate_metadata_varlen.restype = ctypes.c_int
         lib.pa_selftest_wait_timeout.argtypes = [vp, sz, ctypes.c_uint, vp]
         lib.pa_selftest_wait_timeout.restype = ctypes.c_int
         lib.pa_append_kv.argtypes = [sp, vp, vp, vp, vp, i32p, i32p, vp, sz, vp]
@@ -234,6 +237,13 @@ def pa_paged_attention_varlen(shape, query, key_pages, value_pages, block_table,
         ctypes.byref(shape), _ptr(query), _ptr(key_pages), _ptr(value_pages), _ptr(block_table),
         _ptr(context_lens), _ptr(cu_q), int(total_q), float(scale), int(bool(causal)),
         _ptr(out), _ptr(workspace), int(workspace_bytes), _stream(stream), int(schedule))
+
+
+def pa_validate_metadata_varlen(shape, block_table, context_lens, cu_q, total_q, causal,
+                                stream=None) -> int:
+    return load().pa_validate_metadata_varlen(
+        ctypes.byref(shape), _ptr(block_table), _ptr(context_lens), _ptr(cu_q), int(total_q),
+        int(bool(causal)), _stream(stream))
 
 
 def pa_selftest_wait_timeout(workspace, workspace_bytes, timeout_us, stream=None) -> int:

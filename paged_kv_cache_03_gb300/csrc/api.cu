@@ -356,6 +356,42 @@ pa_status pa_validate_metadata(const pa_shape* shape, const int32_t* block_table
     return PA_OK;
 }
 
+pa_status pa_validate_metadata_varlen(const pa_shape* shape, const int32_t* block_table,
+                                      const int32_t* context_lens, const int32_t* cu_q,
+                                      int total_q, int causal, void* cuda_stream) {
+    pa_status st = check_shape(shape);
+    if (st != PA_OK) return st;
+    if (!block_table || !context_lens || !cu_q || total_q < 0) return PA_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
+    std::vector<int32_t> ctx(shape->B), cu(static_cast<size_t>(shape->B) + 1);
+    std::vector<int32_t> bt(static_cast<size_t>(shape->B) * shape->max_pages_per_seq);
+    if (cudaMemcpyAsync(ctx.data(), context_lens, ctx.size() * 4, cudaMemcpyDeviceToHost, s) !=
+            cudaSuccess ||
+        cudaMemcpyAsync(cu.data(), cu_q, cu.size() * 4, cudaMemcpyDeviceToHost, s) !=
+            cudaSuccess ||
+        cudaMemcpyAsync(bt.data(), block_table, bt.size() * 4, cudaMemcpyDeviceToHost, s) !=
+            cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess) {
+        cudaGetLastError();
+        return PA_ERR_CUDA;
+    }
+    if (cu[0] != 0 || cu[shape->B] != total_q) return PA_ERR_INVALID_ARG;
+    const long long cap = static_cast<long long>(shape->max_pages_per_seq) * shape->page_size;
+    for (int b = 0; b < shape->B; ++b) {
+        const int Lb = cu[b + 1] - cu[b];
+        if (Lb < 0 || Lb > shape->L) return PA_ERR_INVALID_ARG;
+        if (Lb == 0) continue;  // not read
+        const int S = ctx[b];
+        if (S < 1 || S > cap || (causal && S < Lb)) return PA_ERR_INVALID_ARG;
+        const int npg = (S + shape->page_size - 1) / shape->page_size;
+        for (int i = 0; i < npg; ++i) {
+            const int32_t pp = bt[static_cast<size_t>(b) * shape->max_pages_per_seq + i];
+            if (pp < 0 || pp >= shape->num_pages) return PA_ERR_BAD_BLOCK_TABLE;
+        }
+    }
+    return PA_OK;
+}
+
 int pa_choose_schedule(const pa_shape* shape) {
     if (check_shape(shape) != PA_OK) return -1;
     return choose(*shape);

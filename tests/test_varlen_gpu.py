@@ -234,3 +234,31 @@ def test_varlen_many_sequences(oracle_lib):
     for sched in SCHEDULES:
         got = gu.out_to_f64(run_varlen(inp, sched)[0])
         gu.assert_parity(got, ref, "bf16", f"1500 sequences sched {sched}")
+
+
+def test_varlen_validate_metadata():
+    """The host-side check of a ragged batch's metadata accepts what the oracle
+    accepts and rejects the same broken offsets, lengths and table entries."""
+    import torch
+    inp = synth.generate_ragged(8, 2, 128, 16, [2, 0, 70, 1], [20, 5, 300, 9], seed=470)
+    dev = to_device(inp)
+    shape = B.shape_of_varlen(dev["query"], dev["key_pages"], dev["block_table"], inp.max_L)
+    T = int(inp.cu_q[-1])
+
+    def check(cu=None, ctx=None, bt=None, total=T, causal=True):
+        t = lambda a: torch.tensor(np.asarray(a), dtype=torch.int32, device="cuda")  # noqa: E731
+        return B.pa_validate_metadata_varlen(
+            shape, dev["block_table"] if bt is None else t(bt),
+            dev["context_lens"] if ctx is None else t(ctx),
+            dev["cu_q"] if cu is None else t(cu), total, causal)
+
+    assert check() == B.PA_OK
+    assert check(ctx=[20, -9, 300, 9]) == B.PA_OK  # the empty sequence is not read
+    assert check(cu=[1, 3, 3, 73, 74]) == B.PA_ERR_INVALID_ARG
+    assert check(cu=[0, 2, 1, 73, 74]) == B.PA_ERR_INVALID_ARG
+    assert check(total=T + 1) == B.PA_ERR_INVALID_ARG
+    assert check(ctx=[1, 5, 300, 9]) == B.PA_ERR_INVALID_ARG  # 2 queries, 1 key, causal
+    assert check(ctx=[1, 5, 300, 9], causal=False) == B.PA_OK
+    bt = inp.block_table.copy()
+    bt[2, 5] = inp.num_pages
+    assert check(bt=bt) == B.PA_ERR_BAD_BLOCK_TABLE

@@ -73,3 +73,22 @@ def test_algorithmic_counts_match_closed_forms():
     qo = 2 * inp.query.size * 2
     assert bench.algorithmic_bytes(inp) == kv + qo + 4 * (1 + 3) + 4 * 2
     assert np.int64(bench.visible_pairs(synth.workload("prefill"))) == 4 * 2048 * 2049 // 2
+
+
+def test_torchrun_two_ranks_print_one_line():
+    """The driver's N>1 launch (torch.distributed.run, 127.0.0.1) of the
+    reference arm: both ranks exit 0 and only rank 0 prints its JSON line."""
+    import json
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
+           "--master-addr", "127.0.0.1", "--master-port", str(_free_port()),
+           os.path.join(root, "bench.py"), "--gpus", "2", "--impl", "reference", "--workload",
+           "tiny", "--steps", "3", "--warmup", "3", "--ref-budget", "1"]
+    r = subprocess.run(cmd, capture_output=True, text=True, timeout=600, cwd=root)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    line = json.loads(lines[0])
+    assert line["impl"] == "reference" and line["n_gpus"] == 2 and line["value"] > 0

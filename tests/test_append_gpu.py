@@ -151,3 +151,75 @@ def test_append_then_attend(oracle_lib):
     out, _ = gu.run(appended, dev=dev)
     gu.assert_parity(gu.out_to_f64(out), gu.oracle_full(oracle_lib, appended), "bf16",
                      "append then attend")
+
+
+def test_prefill_then_decode_through_the_library(oracle_lib):
+    """The serving flow on one pool, every step through the library: append
+    the prompts' K/V and attend over them (causal prefill), then append one
+    token per sequence and attend again (decode), then a ragged step where one
+    sequence decodes and the other takes a prefill chunk.  Each output matches
+    the oracle over the oracle's own appended pools."""
+    import torch
+    H_q, H_kv, D, ps = 8, 2, 128, 16
+    B_, L0 = 2, 70                            # two prompts of 70 tokens
+    npg = 8                                   # pages per sequence: room for 128 tokens
+    rng = np.random.default_rng(480)
+    pool = synth.generate(B_, H_q, H_kv, 1, D, ps, context_lens=[npg * ps] * B_, seed=481)
+    kp_ref, vp_ref = pool.key_pages.copy(), pool.value_pages.copy()
+    bt = pool.block_table.copy()
+    kp_dev, vp_dev = _torch(kp_ref), _torch(vp_ref)
+    bt_dev = _torch(bt)
+    ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
+
+    def append(ctx, L, seed):
+        nonlocal kp_ref, vp_ref
+        kn, vn = synth.new_kv(B_, H_kv, L, D, seed)
+        kp_ref, vp_ref, st = oracle_lib.append_kv(kn, vn, kp_ref, vp_ref, bt, ctx)
+        assert st == 0
+        sh = B.make_shape(B_, H_kv, H_kv, L, D, kp_ref.shape[0], ps, bt.shape[1])
+        assert B.pa_append_kv(sh, _torch(kn), _torch(vn), kp_dev, vp_dev, bt_dev, _torch(ctx),
+                              ws, 256) == B.PA_OK
+
+    def attend(ctx, L, seed, what):
+        q = synth._normal(rng, (B_, H_q, L, D), "bf16")
+        inp = synth.PagedInputs(q, kp_ref, vp_ref, bt, ctx, ps, float(np.float32(D ** -0.5)),
+                                True, "bf16", what)
+        dev = dict(query=_torch(q), key_pages=kp_dev, value_pages=vp_dev, block_table=bt_dev,
+                   context_lens=_torch(ctx))
+        out, flag = gu.run(inp, dev=dev)
+        assert flag == 0
+        gu.assert_parity(gu.out_to_f64(out), gu.oracle_full(oracle_lib, inp), "bf16", what)
+
+    # prefill: both prompts' K/V appended, then causal attention over them
+    ctx = np.array([L0, L0], dtype=np.int32)
+    append(ctx, L0, 482)
+    attend(ctx, L0, 483, "prefill")
+    for step in range(3):                     # three decode steps
+        ctx = ctx + 1
+        append(ctx, 1, 484 + step)
+        attend(ctx, 1, 490 + step, f"decode step {step}")
+    # ragged step: sequence 0 decodes one token, sequence 1 takes 20 tokens
+    lens = np.array([1, 20])
+    kn_all, vn_all = [], []
+    new_ctx = ctx + lens.astype(np.int32)
+    for b in range(B_):
+        kn, vn = synth.new_kv(1, H_kv, int(lens[b]), D, 500 + b)
+        one = np.ascontiguousarray(bt[b:b + 1])
+        kp_ref, vp_ref, st = oracle_lib.append_kv(kn, vn, kp_ref, vp_ref, one, new_ctx[b:b + 1])
+        assert st == 0
+        sh = B.make_shape(1, H_kv, H_kv, int(lens[b]), D, kp_ref.shape[0], ps, bt.shape[1])
+        assert B.pa_append_kv(sh, _torch(kn), _torch(vn), kp_dev, vp_dev, _torch(one),
+                              _torch(new_ctx[b:b + 1]), ws, 256) == B.PA_OK
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    q = synth._normal(rng, (int(cu[-1]), H_q, D), "bf16")
+    r = synth.RaggedInputs(q, kp_ref, vp_ref, bt, new_ctx, cu, ps, float(np.float32(D ** -0.5)),
+                           True, "bf16", "ragged step")
+    ref = oracle_lib.paged_attention_varlen(q, kp_ref, vp_ref, bt, new_ctx, cu, r.scale, True)
+    shape = B.shape_of_varlen(_torch(q), kp_dev, bt_dev, int(lens.max()))
+    out = torch.zeros((int(cu[-1]), H_q, D), dtype=torch.bfloat16, device="cuda")
+    wsv = B.new_workspace(shape)
+    assert B.pa_paged_attention_varlen(shape, _torch(q), kp_dev, vp_dev, bt_dev, _torch(new_ctx),
+                                       _torch(cu), int(cu[-1]), r.scale, True, out, wsv,
+                                       wsv.numel()) == B.PA_OK
+    torch.cuda.synchronize()
+    gu.assert_parity(gu.out_to_f64(out), ref, "bf16", "ragged step after decode")

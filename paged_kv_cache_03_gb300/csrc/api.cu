@@ -67,15 +67,18 @@ int choose(const pa_shape& s) {
     if (s.dtype != PA_BF16 || !prefill_supported(s)) return PA_SCHED_DECODE;
     const long long rows = static_cast<long long>(s.H_q / s.H_kv) * s.L;
     // Measured crossover (operator sweep over G in {1, 4}, L in 1..128,
-    // contexts 64..16384, B in {8, 64}): with more than 4 query rows per kv
-    // head the tensor-core tiles win at every context length (1.3x at 8
-    // rows, 2-10x beyond); with at most 4 rows the page walk on CUDA cores
-    // wins, except on calls so small that the tile schedule's lower fixed
-    // cost decides (B * H_kv * context capacity up to 64K token rows).
+    // contexts 64..32768, B in {1, 4, 8, 64, 256}): with more than 4 query
+    // rows per kv head the tensor-core tiles win at almost every context
+    // length (1.3x at 8 rows, 2-10x beyond); with at most 4 rows the page walk
+    // on CUDA cores wins, except on calls so small that the tile schedule's
+    // lower fixed cost decides: B * H_kv * context capacity up to 64K token
+    // rows and a capacity of at most 1024 keys (beyond it one tile CTA per
+    // (sequence, kv head) walks too many key tiles in turn: at B = 1 and 4096
+    // keys the tiles take 62 us, the page walk 37 us).
     if (rows > kMixedDecodeRows) return PA_SCHED_PREFILL;
-    const long long work =
-        static_cast<long long>(s.B) * s.H_kv * s.max_pages_per_seq * s.page_size;
-    return work <= 65536 ? PA_SCHED_PREFILL : PA_SCHED_DECODE;
+    const long long cap = static_cast<long long>(s.max_pages_per_seq) * s.page_size;
+    const long long work = static_cast<long long>(s.B) * s.H_kv * cap;
+    return work <= 65536 && cap <= 1024 ? PA_SCHED_PREFILL : PA_SCHED_DECODE;
 }
 
 pa_status run(const pa_shape* shape, const void* query, const void* key_pages,

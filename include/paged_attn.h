@@ -29,6 +29,12 @@
  * never used and may hold anything (the kernels may load them, always inside
  * the [B, max_pages_per_seq] table, but no page is read through them).
  *
+ * Variants of the same operation: pa_paged_attention_masked adds an fp32
+ * additive mask [B * H_q, L, mask_S]; pa_paged_attention_varlen takes a ragged
+ * batch (queries and outputs packed by token [total_q, H_q, D], offsets
+ * cu_q[B + 1], each sequence its own query count).  pa_append_kv stores the
+ * new tokens' K/V rows in their pages, the step before the operation.
+ *
  * Ownership: the caller allocates and owns every buffer, including the
  * workspace.  The library allocates no device memory in any call.  Calls are
  * asynchronous on the given stream (cudaStream_t passed as void*, NULL = the
@@ -92,8 +98,11 @@ size_t pa_workspace_bytes(const pa_shape* shape);
 
 /* out = attention(query, paged K/V) for every (b, q_head, l).  `scale`
  * multiplies q.k before the softmax (1/sqrt(D) for standard attention).
- * The shape rule picks the decode schedule when the rows sharing one kv head
- * (H_q/H_kv * L) are few, or for fp32; the tensor-core prefill otherwise. */
+ * The shape rule (measured crossover) picks the decode schedule when the rows
+ * sharing one kv head (H_q/H_kv * L) are at most 4, or for fp32 and shapes the
+ * tiles do not take; the tensor-core tiles otherwise, and also for at most 4
+ * rows on calls with B * H_kv * capacity <= 65536 and a table capacity
+ * (max_pages_per_seq * page_size) of at most 1024 keys. */
 pa_status pa_paged_attention(const pa_shape* shape, const void* query, const void* key_pages,
                              const void* value_pages, const int32_t* block_table,
                              const int32_t* context_lens, float scale, int causal, void* out,
@@ -156,7 +165,8 @@ pa_status pa_paged_attention_masked(const pa_shape* shape, const void* query,
  * PA_SCHED_AUTO sends each sequence to a schedule on the device: at most 4
  * query rows per kv head ((H_q / H_kv) * L_b <= 4) to the page walk, more to
  * the tensor-core tiles (bf16, shapes the tiles take), both launched by this
- * call; a forced schedule takes every sequence.  A sequence whose offsets are
+ * call, the page walk as a programmatic dependent of the tile kernel so the two
+ * run side by side; a forced schedule takes every sequence.  A sequence whose offsets are
  * broken (cu_q[b] < 0, L_b < 0 or > shape->L, cu_q[b + 1] > total_q) sets
  * PA_FLAG_BAD_CONTEXT and none of its rows is written; one whose context
  * length breaks the contract sets it too and gets zero rows.  No explicit

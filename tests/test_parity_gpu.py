@@ -352,3 +352,25 @@ def test_bounded_wait_gives_up_and_the_context_survives(oracle_lib):
     assert flag == 0
     gu.assert_parity(gu.out_to_f64(out), gu.oracle_full(oracle_lib, inp), "bf16",
                      "call after a timed-out wait")
+
+
+def test_long_prefill_8192(oracle_lib):
+    """One causal prefill of 8192 tokens (tile kernel: 128 query-tile pairs
+    per kv head, up to 64 key tiles each), checked on sampled rows."""
+    inp = synth.generate(B=1, H_q=32, H_kv=8, L=8192, D=128, page_size=128,
+                         context_lens=[8192], k_scale=2.0, seed=701, name="prefill-8192")
+    out, _ = gu.run(inp)
+    rows = gu.sample_rows(inp, 96, seed=702)
+    got = gu.out_to_f64(out)[rows[:, 0], rows[:, 1], rows[:, 2]]
+    gu.assert_parity(got, gu.oracle_rows(oracle_lib, inp, rows), "bf16", "prefill 8192")
+
+
+def test_decode_1024_sequences(oracle_lib):
+    """1024 single-token decodes (the page walk's prologue scans 4 blocks of
+    sequences; many short segments), checked in full."""
+    inp = synth.generate(B=1024, H_q=32, H_kv=8, L=1, D=128, page_size=16,
+                         ctx_range=(16, 512), seed=703, name="decode-1024")
+    for sched in (B.PA_SCHED_AUTO, B.PA_SCHED_DECODE):
+        out, _ = gu.run(inp, sched)
+        gu.assert_parity(gu.out_to_f64(out), gu.oracle_full(oracle_lib, inp), "bf16",
+                         f"decode 1024 sched {sched}")

@@ -31,6 +31,11 @@
 //     memory for the P.V MMA (one buffer, written by A and B in turn), running
 //     sum in fp32; at the end O/l -> bf16 -> global.  Whole K/V tiles past a
 //     tile's last causal frontier are skipped.
+//   * Boxes are copied whole, so a sequence's last K/V tile can carry page
+//     rows past its context (unused slots, any contents).  Their scores are
+//     masked to -inf.  Their V rows would still meet a weight of exactly 0,
+//     and 0 * NaN is NaN, so the producer lands that V tile on a barrier of
+//     its own, zeroes those rows and only then releases the tile to the MMA.
 //   * All waits are bounded; on a timeout the CTA records PA_FLAG_TIMEOUT,
 //     lets its copies and MMAs finish, frees TMEM and exits.
 #include <cuda.h>
@@ -74,7 +79,8 @@ enum Bar {
     kPFull = 11,  // + tile
     kODone = 13,  // + tile
     kMmaDone = 15,
-    kNumBars = 16
+    kVTail = 16,  // the V tile that holds rows past the context
+    kNumBars = 18  // (even: what follows stays 16-byte aligned)
 };
 constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
 constexpr int kOffAbort = kOffTmemSlot + 8;
@@ -258,6 +264,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(bar(kVEmpty + s), 1);
         }
         mbar_init(bar(kMmaDone), 1);
+        mbar_init(bar(kVTail), 1);
         *abort_flag = 0;
         if constexpr (kVarlen) {
             out_rows->base = static_cast<long long>(q0) * p.H_q;
@@ -313,6 +320,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
         }
         __syncwarp();
+        // the K/V tile whose last box runs past the context (its V rows past
+        // the context are zeroed before the MMA may read the tile), or -1
+        const int tail_tile = (S % p.box_rows != 0) ? (S - 1) / BN : -1;
         int rows_cur[4], rows_next[4];
         uint32_t bytes_cur, bytes_next;
         tile_boxes(p, b, kvh, S, 0, lane, rows_cur, bytes_cur);
@@ -335,11 +345,30 @@ __global__ void __launch_bounds__(kThreads, 1)
                 issued = -(t + 1);  // K(t) issued, V(t) not
                 break;
             }
-            if (lane == 0) mbar_arrive_expect_tx(bar(kVFull + s), bytes_cur);
+            const bool vtail = t == tail_tile;
+            const uint32_t vbar = vtail ? bar(kVTail) : bar(kVFull + s);
+            if (lane == 0) mbar_arrive_expect_tx(vbar, bytes_cur);
             __syncwarp();
-            issue_boxes(&tm_v, base + kOffV + s * kTile, rows_cur, lane, p.box_rows,
-                        bar(kVFull + s), pol_kv);
+            issue_boxes(&tm_v, base + kOffV + s * kTile, rows_cur, lane, p.box_rows, vbar, pol_kv);
             issued = t + 1;
+            if (vtail) {  // the last tile this CTA loads: nothing waits behind it
+                if (!warp_wait(bar(kVTail), 0)) {
+                    if (lane == 0) give_up(p, abort_flag);
+                    break;
+                }
+                for (int r = S - t * BN + lane; r < BN; r += 32) {
+                    uint4* const vrow =
+                        reinterpret_cast<uint4*>(sbase + kOffV + s * kTile + r * 128);
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) {
+                        vrow[q] = make_uint4(0u, 0u, 0u, 0u);
+                        vrow[kHalf / 16 + q] = make_uint4(0u, 0u, 0u, 0u);
+                    }
+                }
+                fence_proxy_async_smem();  // the MMA reads them through the async proxy
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(kVFull + s));
+            }
 #pragma unroll
             for (int w = 0; w < 4; ++w) rows_cur[w] = rows_next[w];
             bytes_cur = bytes_next;
@@ -350,7 +379,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int t = max(0, kdone - 2); t < kdone; ++t)
             if (!mbar_wait(bar(kKFull + (t & 1)), (t >> 1) & 1)) give_up(p, abort_flag);
         for (int t = max(0, vdone - 2); t < vdone; ++t)
-            if (!mbar_wait(bar(kVFull + (t & 1)), (t >> 1) & 1)) give_up(p, abort_flag);
+            if (!(t == tail_tile ? mbar_wait(bar(kVTail), 0)
+                                 : mbar_wait(bar(kVFull + (t & 1)), (t >> 1) & 1)))
+                give_up(p, abort_flag);
     } else if (warp == 1 && nk > 0) {
         // ============================ MMA issuer =============================
         if (lane == 0) {

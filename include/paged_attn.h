@@ -28,6 +28,13 @@
  * Entries block_table[b, i] with i >= ceil(context_lens[b] / page_size) are
  * never used and may hold anything (the kernels may load them, always inside
  * the [B, max_pages_per_seq] table, but no page is read through them).
+ * Page slots past a sequence's context length, and pages no table entry
+ * names, may hold anything, NaN and Inf included: they never reach the
+ * output.  (The tensor-core schedule copies whole boxes of page rows and
+ * zeroes, on chip, the value rows past the context before using them.)
+ * Values inside a context are taken to be finite: a key a query row does
+ * not see is multiplied by an exact 0 weight, so an Inf there would reach
+ * that row as NaN.
  *
  * Variants of the same operation: pa_paged_attention_masked adds an fp32
  * additive mask [B * H_q, L, mask_S]; pa_paged_attention_varlen takes a ragged

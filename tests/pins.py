@@ -195,6 +195,26 @@ def pin_page_permutation(lib):
     assert_close(outs[0], dense_bruteforce(c), what="permutation case")
 
 
+def pin_shared_pages(lib):
+    """Several table rows may name one physical page (a common prefix held
+    once; the translation of "Week 3 Day 5", Task 1 only reads the pool):
+    the result is bitwise that of private copies, and the dense brute force."""
+    c = make_case(37, 3, 4, 2, 3, 16, 4, [13, 10, 9])
+    # give sequences 1 and 2 sequence 0's first two pages (8 positions)
+    K_store, K = c.K_store.copy(), c.K.copy()
+    V_store, V = c.V_store.copy(), c.V.copy()
+    for b in (1, 2):
+        K_store[b, :, :8], K[b, :, :8] = c.K_store[0, :, :8], c.K[0, :, :8]
+        V_store[b, :, :8], V[b, :, :8] = c.V_store[0, :, :8], c.V[0, :, :8]
+    c = make_case(37, 3, 4, 2, 3, 16, 4, [13, 10, 9], q=(c.q_store, c.q), K=(K_store, K),
+                  V=(V_store, V))
+    private = run_oracle(lib, c)
+    bt = c.bt.copy()
+    bt[1:, :2] = c.bt[0, :2]
+    assert np.array_equal(run_oracle(lib, c, bt), private), "page sharing changed the result"
+    assert_close(private, dense_bruteforce(c), what="shared-prefix case")
+
+
 def pin_unused_table_entries(lib):
     c = make_case(41, 2, 2, 1, 2, 16, 8, [17, 8])
     ref = run_oracle(lib, c)
@@ -629,7 +649,8 @@ def pin_varlen_empty_sequences_and_errors(lib):
         raise AssertionError("accepted L_b > context length under causal")
 
 
-ALL_PINS = [pin_bruteforce, pin_torch_sdpa, pin_page_permutation, pin_unused_table_entries,
+ALL_PINS = [pin_bruteforce, pin_torch_sdpa, pin_page_permutation, pin_shared_pages,
+            pin_unused_table_entries,
             pin_tile_size_invariance, pin_single_page, pin_one_hot, pin_uniform_visible_mean,
             pin_gqa_equals_repeat, pin_gather, pin_errors, pin_rows_api,
             pin_append_dense_slice, pin_append_page_permutation, pin_append_touches_only_new_rows,

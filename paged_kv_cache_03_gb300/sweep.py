@@ -13,6 +13,7 @@ The grid restates the Week 2 operator grid of "Week 2 Day 5" (contexts up to
 longer contexts and more query positions, where the schedules trade places.
 
   python -m paged_kv_cache_03_gb300.sweep [--reps 15] [--json out.jsonl]
+  python -m paged_kv_cache_03_gb300.sweep --prefill-scan
 
 Needs a GPU; prints a markdown table.
 """
@@ -113,6 +114,54 @@ def run(reps=15, json_path=None, groups=GROUPS, ls=LS, ss=SS, batches=(B,)):
     return rows_out
 
 
+# Causal prefills of equal total tokens, from many short sequences to one long
+# one (L = context length, GQA group 4): how the tile schedule's fixed cost per
+# CTA is amortised by more key tiles per CTA.
+SCAN = ((16, 512), (8, 1024), (4, 2048), (2, 4096), (1, 8192), (1, 16384))
+
+
+def _measured_bf16_tflops():
+    import os
+    path = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
+                        "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["bf16_tflops"])
+    except Exception:
+        return None
+
+
+def prefill_scan(reps=15, scan=SCAN):
+    """Times the tile schedule on causal prefills with L = context length;
+    algorithmic FLOP = 4 * H_q * D per visible (row, key) pair, L (L + 1) / 2
+    pairs per sequence and head."""
+    import torch
+    from paged_kv_cache_03_gb300 import binding as Bd
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    peak = _measured_bf16_tflops()
+    print("| B x L | tile schedule (us) | TFLOP/s | of measured bf16 peak |")
+    print("|---|---|---|---|")
+    G, seed = 4, 2000
+    for nb, L in scan:
+        seed += 1
+        q, kp, vp, bt, ctx = _inputs(G, L, L, seed, nb)
+        sh = Bd.shape_of(q, kp, bt)
+        ws = Bd.new_workspace(sh)
+        out = torch.empty_like(q)
+
+        def call():
+            st = Bd.pa_paged_attention_sched(sh, q, kp, vp, bt, ctx, D ** -0.5, True, out, ws,
+                                             ws.numel(), None, Bd.PA_SCHED_PREFILL)
+            if st != Bd.PA_OK:
+                raise Bd.PagedAttentionError(st, "pa_paged_attention_sched")
+        us = _time(call, reps, flush)
+        flops = 4.0 * nb * G * H_KV * D * L * (L + 1) / 2
+        tf = flops / (us * 1e-6) / 1e12
+        frac = f"{tf / peak:.3f}" if peak else "n/a"
+        print(f"| {nb} x {L} | {us:.1f} | {tf:.0f} | {frac} |", flush=True)
+        del q, kp, vp, bt, ctx, ws, out
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--reps", type=int, default=15)
@@ -122,8 +171,13 @@ def main(argv=None):
     ap.add_argument("--ls", type=ints, default=LS, help="query positions, e.g. 1,2,4")
     ap.add_argument("--ss", type=ints, default=SS, help="context lengths")
     ap.add_argument("--batches", type=ints, default=(B,), help="batch sizes")
+    ap.add_argument("--prefill-scan", action="store_true",
+                    help="time the tile schedule on causal prefills of equal total tokens")
     a = ap.parse_args(argv)
-    run(a.reps, a.json, a.groups, a.ls, a.ss, a.batches)
+    if a.prefill_scan:
+        prefill_scan(a.reps)
+    else:
+        run(a.reps, a.json, a.groups, a.ls, a.ss, a.batches)
 
 
 if __name__ == "__main__":

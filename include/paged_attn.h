@@ -104,7 +104,9 @@ typedef struct {
 size_t pa_workspace_bytes(const pa_shape* shape);
 
 /* out = attention(query, paged K/V) for every (b, q_head, l).  `scale`
- * multiplies q.k before the softmax (1/sqrt(D) for standard attention).
+ * multiplies q.k before the softmax (1/sqrt(D) for standard attention); it
+ * must be finite and >= 0 (PA_ERR_INVALID_ARG otherwise, in every entry
+ * point that takes it).
  * The shape rule (measured crossover) picks the decode schedule when the rows
  * sharing one kv head (H_q/H_kv * L) are at most 4, or for fp32 and shapes the
  * tiles do not take; the tensor-core tiles otherwise, and also for at most 4

@@ -1,6 +1,7 @@
 // api.cu -- the extern "C" entry points of paged_attn.h: argument checks on
 // the host, schedule choice (the shape dispatch that "Week 3 Day 5: Paged
 // FlashAttention" puts inside the extension), and the launches.
+#include <cfloat>
 #include <cstdio>
 #include <cstring>
 #include <mutex>
@@ -63,6 +64,12 @@ pa_status check_shape(const pa_shape* s) {
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+// `scale` is the softmax temperature 1/sqrt(D) of standard attention: finite
+// and >= 0.  (The tile kernel takes a row's max over the raw scores and scales
+// it once, which is the max of the scaled scores only for scale >= 0.)  NaN,
+// negative and infinite values are rejected.
+bool scale_ok(float scale) { return scale >= 0.f && scale <= FLT_MAX; }
+
 int choose(const pa_shape& s) {
     if (s.dtype != PA_BF16 || !prefill_supported(s)) return PA_SCHED_DECODE;
     const long long rows = static_cast<long long>(s.H_q / s.H_kv) * s.L;
@@ -93,7 +100,7 @@ pa_status run(const pa_shape* shape, const void* query, const void* key_pages,
     if (!aligned(query, 16) || !aligned(key_pages, 16) || !aligned(value_pages, 16) ||
         !aligned(out, 16) || !aligned(block_table, 4) || !aligned(context_lens, 4))
         return PA_ERR_INVALID_ARG;
-    if (!(scale == scale)) return PA_ERR_INVALID_ARG;  // NaN scale
+    if (!scale_ok(scale)) return PA_ERR_INVALID_ARG;
     if (!workspace || !aligned(workspace, 256)) return PA_ERR_WORKSPACE;
     if (schedule == PA_SCHED_AUTO) schedule = choose(*shape);
     if (schedule != PA_SCHED_DECODE && schedule != PA_SCHED_PREFILL) return PA_ERR_INVALID_ARG;
@@ -195,7 +202,7 @@ pa_status pa_paged_attention_varlen(const pa_shape* shape, const void* query,
         !aligned(out, 16) || !aligned(block_table, 4) || !aligned(context_lens, 4) ||
         !aligned(cu_q, 4))
         return PA_ERR_INVALID_ARG;
-    if (total_q < 0 || !(scale == scale)) return PA_ERR_INVALID_ARG;
+    if (total_q < 0 || !scale_ok(scale)) return PA_ERR_INVALID_ARG;
     if (static_cast<long long>(total_q) * sh.H_q >= (1ll << 31)) return PA_ERR_UNSUPPORTED;
     if (!workspace || !aligned(workspace, 256)) return PA_ERR_WORKSPACE;
     if (schedule != PA_SCHED_AUTO && schedule != PA_SCHED_DECODE && schedule != PA_SCHED_PREFILL)

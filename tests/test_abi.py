@@ -85,9 +85,18 @@ def test_missing_workspace_is_rejected():
     assert st == B.PA_ERR_WORKSPACE
 
 
-def test_nan_scale_is_rejected():
-    st = B.pa_paged_attention(good_shape(), FAKE, FAKE, FAKE, FAKE, FAKE, float("nan"), 1, FAKE,
+@pytest.mark.parametrize("scale", [float("nan"), -0.1, -1e-30, float("inf"), float("-inf")])
+def test_bad_scale_is_rejected(scale):
+    """scale is a softmax temperature: finite and >= 0 (checked on the host,
+    before anything is enqueued, in the uniform, masked and ragged calls)."""
+    st = B.pa_paged_attention(good_shape(), FAKE, FAKE, FAKE, FAKE, FAKE, scale, 1, FAKE,
                               FAKE, 1 << 20, 0)
+    assert st == B.PA_ERR_INVALID_ARG
+    st = B.pa_paged_attention_masked(good_shape(), FAKE, FAKE, FAKE, FAKE, FAKE, scale, 1, FAKE,
+                                     1 << 12, FAKE, FAKE, 1 << 20, 0, B.PA_SCHED_AUTO)
+    assert st == B.PA_ERR_INVALID_ARG
+    st = B.pa_paged_attention_varlen(good_shape(), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 8, scale,
+                                     1, FAKE, FAKE, 1 << 20, 0, B.PA_SCHED_AUTO)
     assert st == B.PA_ERR_INVALID_ARG
 
 

@@ -156,6 +156,7 @@ BRUTE_CASES = [
     (14, 2, 4, 4, 6, 8, 5, [6, 33], True, "f32"),
     (15, 2, 6, 2, 2, 8, 4, [17, 2], False, "bf16"),
     (16, 1, 4, 2, 1, 32, 16, [40], True, "f32"),
+    (17, 2, 4, 2, 5, 16, 4, [3, 17], False, "bf16"),  # no causal rule, L > context length
 ]
 
 

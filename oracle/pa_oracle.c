@@ -115,7 +115,11 @@ static void gather_one(const oracle_shape* sh, const void* key_pages, const void
     const int ps = sh->page_size, D = sh->D;
     for (int s = 0; s < S; ++s) {
         const int logical_page = s / ps;
+#if ORACLE_MUTANT == 12
+        const int slot = (s + 1) % ps; /* planted: slot off by one within its page */
+#else
         const int slot = s % ps;
+#endif
 #if ORACLE_MUTANT == 3
         const int64_t physical_page = logical_page; /* planted: block table ignored */
 #else
@@ -178,7 +182,11 @@ static void attend_row(const oracle_shape* sh, const void* query, int64_t qbase,
     for (int d = 0; d < D; ++d) o[d] = 0.0;
     if (M == -INFINITY) return; /* every visible key masked out */
     for (int s = 0; s <= last; ++s) {
+#if ORACLE_MUTANT == 11
+        const double w = exp(x[s]); /* planted: the max not subtracted */
+#else
         const double w = exp(x[s] - M);
+#endif
 #if ORACLE_MUTANT == 6
         if (s > 0) den += w; /* planted: a dropped term in the normaliser */
 #else
@@ -251,7 +259,11 @@ int oracle_paged_attention_masked(const oracle_shape* sh, const void* query,
 #endif
     for (int item = 0; item < n_items; ++item) {
         const int b = item / sh->H_kv, kvh = item % sh->H_kv;
+#if ORACLE_MUTANT == 13
+        const int S = context_lens[b] - 1; /* planted: the context's last key dropped */
+#else
         const int S = context_lens[b];
+#endif
         double* K = (double*)malloc(sizeof(double) * (size_t)S * D);
         double* V = (double*)malloc(sizeof(double) * (size_t)S * D);
         double* x = (double*)malloc(sizeof(double) * (size_t)S);

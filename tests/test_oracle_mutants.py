@@ -6,14 +6,17 @@ block table ignored, (4) scale dropped, (5) K and V swapped, (6) a term
 dropped from the softmax denominator, (7) causal offset with its sign flipped,
 (8) the K/V append writing one slot too far, (9) an explicit mask subtracted
 instead of added, (10) a ragged batch's causal offset taken from the longest
-query instead of the sequence's own.
+query instead of the sequence's own, (11) the softmax's max not subtracted
+(exact in real arithmetic, overflows on large scores), (12) the slot off by
+one within its page, (13) the last key of every context dropped.  Each keeps
+every index in bounds, so a mutant fails a pin instead of crashing the run.
 """
 import pytest
 
 import oracle
 import pins
 
-MUTANTS = [1, 2, 3, 4, 5, 6, 7, 8, 9, 10]
+MUTANTS = [1, 2, 3, 4, 5, 6, 7, 8, 9, 10, 11, 12, 13]
 
 
 @pytest.mark.parametrize("mutant", MUTANTS)

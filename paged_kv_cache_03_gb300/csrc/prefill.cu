@@ -170,17 +170,22 @@ __device__ __forceinline__ void issue_boxes(const CUtensorMap* map, uint32_t dst
     }
 }
 
-// p = 2^(s * c - m) for one 128-key row: packed to bf16 pairs in pw, summed
-// in fp32 into ts.
+// p = 2^(s * c - m) for one 128-key row: rounded to bf16 pairs in pw (the
+// P.V operand) and summed in fp32 into ts.  The row sum adds the rounded
+// weights, the same ones P.V applies to V, so the output stays a weighted
+// mean of value rows: o = sum bf16(p) v / sum bf16(p).  Summing the unrounded
+// p instead would scale a row dominated by one key by that key's rounding
+// error (up to 2^-9 relative), which on the causal prefill workload's peaky
+// rows reached 1.4e-2 absolute after the output's own rounding.
 __device__ __forceinline__ void exp_pack(const float (&x)[4][32], float2 c2, float2 nm2,
                                          uint32_t (&pw)[64], float2& ts) {
 #pragma unroll
     for (int k = 0; k < 64; ++k) {
         const int cc = k >> 4, e = (k & 15) * 2;
         const float2 y = __ffma2_rn(make_float2(x[cc][e], x[cc][e + 1]), c2, nm2);
-        const float2 pp = make_float2(fast_exp2(y.x), fast_exp2(y.y));
-        ts = __fadd2_rn(ts, pp);
-        pw[k] = pack_bf16x2(pp.x, pp.y);
+        const uint32_t w = pack_bf16x2(fast_exp2(y.x), fast_exp2(y.y));
+        ts = __fadd2_rn(ts, bf16x2_to_float2(w));
+        pw[k] = w;
     }
 }
 
@@ -248,6 +253,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     const int nk = max(nk_t[0], nk_t[1]);
     const int ntiles = (2 * mp + 1 < nM) ? 2 : 1;
+    // The producer's block-table lookup of K/V tile 0 goes out before the
+    // set-up below, so its latency overlaps the set-up instead of delaying
+    // the first copies.
+    int rows_cur[4] = {-1, -1, -1, -1};
+    uint32_t bytes_cur = 0;
+    if (warp == 0 && nk > 0) tile_boxes(p, b, kvh, S, 0, lane, rows_cur, bytes_cur);
 
     // ---- set-up: barriers, V zeroed, TMEM --------------------------------------
     if (tid == 0) {
@@ -277,9 +288,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         fence_mbar_init();
     }
-    // key rows that are never loaded must hold finite values (their weight is
-    // exactly 0, and 0 * NaN would not be)
-    {
+    // V rows that are never loaded must hold finite values (their weight is
+    // exactly 0, and 0 * NaN would not be).  Only a last key tile that ends
+    // past the context has such rows, and only in a slot no earlier tile of
+    // this CTA filled (tiles 0 and 1); a tile whose last box runs past the
+    // context is zeroed after its copy lands (kVTail).  Rows of a later slot
+    // past the context still hold the finite rows of the tile two before.
+    if (nk <= 2 && S < nk * BN && S % p.box_rows == 0) {
         uint4* v = reinterpret_cast<uint4*>(sbase + kOffV);
         for (int i = tid; i < 2 * kTile / 16; i += kThreads) v[i] = make_uint4(0u, 0u, 0u, 0u);
     }
@@ -323,13 +338,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         // the K/V tile whose last box runs past the context (its V rows past
         // the context are zeroed before the MMA may read the tile), or -1
         const int tail_tile = (S % p.box_rows != 0) ? (S - 1) / BN : -1;
-        int rows_cur[4], rows_next[4];
-        uint32_t bytes_cur, bytes_next;
-        tile_boxes(p, b, kvh, S, 0, lane, rows_cur, bytes_cur);
+        int rows_next[4] = {-1, -1, -1, -1};
+        uint32_t bytes_next = 0;
         int issued = 0;
         for (int t = 0; t < nk; ++t) {
-            // rows of the next tile requested before waiting for a free slot
-            if (t + 1 < nk) tile_boxes(p, b, kvh, S, t + 1, lane, rows_next, bytes_next);
             const int s = t & 1;
             if (t >= 2 && !warp_wait(bar(kKEmpty + s), ((t >> 1) - 1) & 1)) {
                 if (lane == 0) give_up(p, abort_flag);
@@ -351,6 +363,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             issue_boxes(&tm_v, base + kOffV + s * kTile, rows_cur, lane, p.box_rows, vbar, pol_kv);
             issued = t + 1;
+            // rows of the next tile, looked up before waiting for a free slot
+            if (t + 1 < nk) tile_boxes(p, b, kvh, S, t + 1, lane, rows_next, bytes_next);
             if (vtail) {  // the last tile this CTA loads: nothing waits behind it
                 if (!warp_wait(bar(kVTail), 0)) {
                     if (lane == 0) give_up(p, abort_flag);

@@ -277,14 +277,19 @@ int pa_launch_count(const pa_shape* shape, int schedule);
  * with its scratch in one fixed array of 8 MiB that the library keeps on
  * every device it is used on, for the life of the process.  Allocates
  * nothing: no cudaMalloc, no cudaFree, no allocating library call.
+ *   - Every argument is checked first, as in pa_paged_attention_sched
+ *     (PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED on a device other than
+ *     compute capability 10.3); a rejected call enqueues nothing.
  *   - Shapes whose decode scratch (pa_workspace_bytes) exceeds 8 MiB are
  *     rejected with PA_ERR_WORKSPACE before anything is enqueued.
- *   - The first call on a device looks up the array's device address with
- *     that device current and caches it; make that first call before any
- *     stream capture.
+ *   - Every call looks up the array's device address with the calling
+ *     thread's device current (cheap once the library's device code is
+ *     loaded there; still right after a cudaDeviceReset).  The first call on
+ *     a device may load that code: make it before any stream capture.
  *   - Each call clears the array's error flag, then runs; if device_flag_out
- *     (a device pointer to one uint32, may be NULL) is given, this call's
- *     PA_FLAG_* bits are copied there on the stream after the kernels.
+ *     (a 4-byte aligned device pointer to one uint32, may be NULL) is given,
+ *     this call's PA_FLAG_* bits are copied there on the stream after the
+ *     kernels.
  *   - All calls share the array and it keeps the last call's contents; calls
  *     whose kernels overlap on the GPU (e.g. on unordered streams) race. */
 pa_status pa_paged_attention_decode_noalloc(const pa_shape* shape, const void* query,

@@ -88,11 +88,11 @@ int choose(const pa_shape& s) {
     return work <= 65536 && cap <= 1024 ? PA_SCHED_PREFILL : PA_SCHED_DECODE;
 }
 
-pa_status run(const pa_shape* shape, const void* query, const void* key_pages,
-              const void* value_pages, const int32_t* block_table, const int32_t* context_lens,
-              float scale, int causal, void* out, void* workspace, size_t workspace_bytes,
-              void* cuda_stream, int schedule, void* ev_before = nullptr,
-              void* ev_after = nullptr, const float* mask = nullptr, long long mask_S = 0) {
+}  // namespace
+
+pa_status check_call_args(const pa_shape* shape, const void* query, const void* key_pages,
+                          const void* value_pages, const int32_t* block_table,
+                          const int32_t* context_lens, float scale, const void* out) {
     pa_status st = check_shape(shape);
     if (st != PA_OK) return st;
     if (!query || !key_pages || !value_pages || !block_table || !context_lens || !out)
@@ -101,6 +101,19 @@ pa_status run(const pa_shape* shape, const void* query, const void* key_pages,
         !aligned(out, 16) || !aligned(block_table, 4) || !aligned(context_lens, 4))
         return PA_ERR_INVALID_ARG;
     if (!scale_ok(scale)) return PA_ERR_INVALID_ARG;
+    return PA_OK;
+}
+
+namespace {
+
+pa_status run(const pa_shape* shape, const void* query, const void* key_pages,
+              const void* value_pages, const int32_t* block_table, const int32_t* context_lens,
+              float scale, int causal, void* out, void* workspace, size_t workspace_bytes,
+              void* cuda_stream, int schedule, void* ev_before = nullptr,
+              void* ev_after = nullptr, const float* mask = nullptr, long long mask_S = 0) {
+    pa_status st = check_call_args(shape, query, key_pages, value_pages, block_table,
+                                   context_lens, scale, out);
+    if (st != PA_OK) return st;
     if (!workspace || !aligned(workspace, 256)) return PA_ERR_WORKSPACE;
     if (schedule == PA_SCHED_AUTO) schedule = choose(*shape);
     if (schedule != PA_SCHED_DECODE && schedule != PA_SCHED_PREFILL) return PA_ERR_INVALID_ARG;

@@ -27,6 +27,12 @@ struct DeviceInfo {
 // Properties of the current device (cached per device).
 pa_status current_device_info(DeviceInfo* out);
 
+// Host-side checks of one attention call that need no device: the shape,
+// null and misaligned pointers, and the scale (finite, >= 0).
+pa_status check_call_args(const pa_shape* shape, const void* query, const void* key_pages,
+                          const void* value_pages, const int32_t* block_table,
+                          const int32_t* context_lens, float scale, const void* out);
+
 struct Call {
     pa_shape sh;
     const void* q;

@@ -10,17 +10,19 @@
 //
 // The array is a file-scope __device__ variable, so every GPU on which the
 // library is used holds kNoAllocScratchBytes for the life of the process.
-// Host code cannot use the array's name as a device address; the first call
-// on each device looks the address up with cudaGetSymbolAddress (with that
-// device current) and caches it.  That first call may load the module, so it
-// should happen before any stream capture.
+// Host code cannot use the array's name as a device address: each call looks
+// the address up with cudaGetSymbolAddress, with the calling thread's device
+// current.  The lookup is cheap once the library's device code is loaded on
+// that device, and it stays right if the context is destroyed and created
+// again (cudaDeviceReset).  The first call on a device may load that code, so
+// it should happen before any stream capture.
 //
-// All calls share the one array and it keeps the last call's contents.  Each
-// call clears the 4-byte error flag at its start; everything else in the
-// scratch is written before it is read.  Two calls whose kernels overlap on
-// the GPU (different streams, no ordering between them) race on the scratch.
-#include <mutex>
-
+// Every argument is checked before anything is enqueued: a rejected call
+// touches neither the array nor device_flag_out.  All calls share the one
+// array and it keeps the last call's contents.  Each accepted call clears the
+// 4-byte error flag at its start; everything else in the scratch is written
+// before it is read.  Two calls whose kernels overlap on the GPU (different
+// streams, no ordering between them) race on the scratch.
 #include "internal.h"
 
 namespace pa {
@@ -30,29 +32,6 @@ constexpr size_t kNoAllocScratchBytes = size_t(8) << 20;  // 8 MiB per device
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
-std::mutex g_scratch_mu;
-void* g_scratch_addr[64] = {};
-
-pa_status scratch_for_current_device(void** out) {
-    int dev = -1;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) {
-        cudaGetLastError();
-        return PA_ERR_CUDA;
-    }
-    if (dev >= 64) return PA_ERR_UNSUPPORTED;
-    std::lock_guard<std::mutex> lock(g_scratch_mu);
-    if (!g_scratch_addr[dev]) {
-        void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) {
-            cudaGetLastError();
-            return PA_ERR_CUDA;
-        }
-        g_scratch_addr[dev] = p;
-    }
-    *out = g_scratch_addr[dev];
-    return PA_OK;
-}
-
 }  // namespace
 }  // namespace pa
 
@@ -60,13 +39,23 @@ extern "C" pa_status pa_paged_attention_decode_noalloc(
     const pa_shape* shape, const void* query, const void* key_pages, const void* value_pages,
     const int32_t* block_table, const int32_t* context_lens, float scale, int causal, void* out,
     uint32_t* device_flag_out, void* cuda_stream) {
-    if (!shape) return PA_ERR_INVALID_ARG;
-    void* scratch = nullptr;
-    pa_status st = pa::scratch_for_current_device(&scratch);
+    // the same host-side checks as the regular entry points, first
+    pa_status st = pa::check_call_args(shape, query, key_pages, value_pages, block_table,
+                                       context_lens, scale, out);
     if (st != PA_OK) return st;
-    const size_t need = pa_workspace_bytes(shape);
-    if (need == 0) return PA_ERR_INVALID_ARG;
+    if (device_flag_out && reinterpret_cast<uintptr_t>(device_flag_out) % 4 != 0)
+        return PA_ERR_INVALID_ARG;
+    pa::DeviceInfo dev;
+    st = pa::current_device_info(&dev);
+    if (st != PA_OK) return st;
+    if (dev.cc_major != 10 || dev.cc_minor != 3) return PA_ERR_UNSUPPORTED;
+    const size_t need = pa::workspace_bytes_total(*shape, dev.sm_count);
     if (need > pa::kNoAllocScratchBytes) return PA_ERR_WORKSPACE;  // beyond the fixed maximum
+    void* scratch = nullptr;
+    if (cudaGetSymbolAddress(&scratch, pa::g_noalloc_scratch) != cudaSuccess || !scratch) {
+        cudaGetLastError();
+        return PA_ERR_CUDA;
+    }
     cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
     if (cudaMemsetAsync(scratch, 0, sizeof(uint32_t), s) != cudaSuccess) {
         cudaGetLastError();

@@ -40,6 +40,15 @@ class Unsupported(Exception):
     pass
 
 
+def tiles_take(dtype: str, H_q: int, H_kv: int, page_size: int) -> bool:
+    """Whether the tensor-core tile schedule takes a shape (the library's
+    documented rule): bf16, H_q/H_kv a divisor of 128 of at most 16, and a
+    page size that is a multiple of 8.  A forced tile call outside the rule
+    returns PA_ERR_UNSUPPORTED; one inside it must run."""
+    G = H_q // H_kv
+    return dtype == "bf16" and 1 <= G <= 16 and 128 % G == 0 and page_size % 8 == 0
+
+
 def run(inp: PagedInputs, schedule=B.PA_SCHED_AUTO, dev=None, workspace=None, check_flag=True,
         block_table=None, context_lens=None):
     """Runs the CUDA path; returns (out tensor, flag word).  Raises

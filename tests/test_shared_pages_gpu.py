@@ -53,10 +53,7 @@ def test_shared_prefix_pages(oracle_lib, case, sched):
                          seed=90 + case, name=f"shared{case}")
     private, shared = share_prefix(inp, n)
     schedule = {"decode": B.PA_SCHED_DECODE, "prefill": B.PA_SCHED_PREFILL}[sched]
-    try:
-        a, _ = gu.run(with_pool(inp, *private), schedule)
-    except gu.Unsupported:
-        pytest.skip("schedule not available for this shape")
+    a, _ = gu.run(with_pool(inp, *private), schedule)  # both schedules take every case
     sh_inp = with_pool(inp, *shared)
     b, _ = gu.run(sh_inp, schedule)
     assert torch.equal(a.view(torch.int16), b.view(torch.int16)), "page sharing changed the output"
@@ -77,8 +74,7 @@ def test_shared_prefix_pages_in_a_ragged_batch(oracle_lib, schedule):
         r = synth.RaggedInputs(inp.query, kp, vp, bt, inp.context_lens, inp.cu_q, inp.page_size,
                                inp.scale, inp.causal, inp.dtype, inp.name)
         res = run_varlen(r, schedule, dev=to_device(r))
-        if res is None:
-            pytest.skip("schedule not available for this shape")
+        assert res is not None, "the forced schedule refused a shape it takes"
         outs.append((r, res[0]))
     assert torch.equal(outs[0][1].view(torch.int16), outs[1][1].view(torch.int16))
     r, out = outs[1]

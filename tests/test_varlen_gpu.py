@@ -86,18 +86,42 @@ CASES = [
     # a tile of keys spanning many page pieces
     ("page3-walk-only", 8, 2, 3, [1, 0, 9, 2], [40, 5, 100, 7], True, 407),
     ("page1-walk-only", 4, 4, 1, [3, 1], [50, 20], True, 408),
+    # mask=None with more queries than keys in some sequences: every row sees
+    # the whole context
+    ("no-causal-more-queries-than-keys", 8, 2, 16, [40, 1, 130, 3, 9], [7, 3, 50, 1, 200],
+     False, 409),
+    ("no-causal-L-over-S-page128", 32, 8, 128, [300, 1, 65], [129, 1, 64], False, 410),
 ]
 
 
-@pytest.mark.parametrize("schedule", SCHEDULES, ids=SCHED_IDS)
-@pytest.mark.parametrize("case", CASES, ids=[c[0] for c in CASES])
+@pytest.mark.parametrize("case", [c for c in CASES if not gu.tiles_take("bf16", *c[1:4])],
+                         ids=lambda c: c[0])
+def test_varlen_tiles_refuse_page_sizes_they_do_not_take(case):
+    name, H_q, H_kv, ps, q_lens, ctx, causal, seed = case
+    inp = synth.generate_ragged(H_q, H_kv, 128, ps, q_lens, ctx, seed=seed, causal=causal,
+                                name=name)
+    assert run_varlen(inp, B.PA_SCHED_PREFILL) is None
+
+
+def _case_schedules():
+    """Every case on AUTO and the forced page walk; the forced tiles only
+    where the tiles take the page size (the walk-only cases check, in
+    test_varlen_tiles_refuse_page_sizes_they_do_not_take, that the library
+    refuses them)."""
+    for c in CASES:
+        for s, sid in zip(SCHEDULES, SCHED_IDS):
+            if s == B.PA_SCHED_PREFILL and not gu.tiles_take("bf16", c[1], c[2], c[3]):
+                continue
+            yield pytest.param(c, s, id=f"{c[0]}-{sid}")
+
+
+@pytest.mark.parametrize("case,schedule", list(_case_schedules()))
 def test_varlen_matches_oracle(oracle_lib, case, schedule):
     name, H_q, H_kv, ps, q_lens, ctx, causal, seed = case
     inp = synth.generate_ragged(H_q, H_kv, 128, ps, q_lens, ctx, seed=seed, causal=causal,
                                 name=name)
     res = run_varlen(inp, schedule)
-    if res is None:
-        pytest.skip("forced schedule does not take this shape")
+    assert res is not None, "the forced schedule refused a shape it takes"
     got = gu.out_to_f64(res[0])
     gu.assert_parity(got, oracle_varlen(oracle_lib, inp), "bf16", f"{name} sched {schedule}")
 

@@ -17,6 +17,11 @@ Metric: achieved HBM GB/s = algorithmic bytes / device time (bf16), or TFLOP/s
 the measured bf16 rate exceeds the byte time at the measured copy bandwidth
 (the causal prefill).
 
+The default line (the decode workload) carries a `prefill` record: the causal
+prefill workload (B=4, L=S=2048) measured the same way in the same run, in
+TFLOP/s, with its own roofline, e2e, clocks and cpu_baseline (--no-prefill
+leaves it out).
+
 The timed region holds two passes of K steps: the call as a user makes it
 (value, ms_per_step) and the same calls with CUDA events around the dominant
 kernel (roofline.achieved); L2 is flushed between steps.
@@ -376,6 +381,11 @@ def time_oracle(inp, target_s: float, unit_fn, mask_fn=None):
 # our arm
 # ---------------------------------------------------------------------------
 def run_ours(args):
+    """Our arm: the requested workload's line; on the default decode line, a
+    `prefill` record of the causal prefill workload measured the same way in
+    the same run (the metric's second half)."""
+    import copy
+
     import torch
     from paged_kv_cache_03_gb300 import binding as B
     world, rank, local = dist_env()
@@ -385,6 +395,41 @@ def run_ours(args):
     device = torch.device("cuda", local if world > 1 else 0)
     torch.cuda.set_device(device)
     B.load()
+    line = measure(args, device, world, rank)
+    if headline(args) and not args.no_prefill:
+        pargs = copy.copy(args)
+        pargs.workload = "prefill"
+        sub = measure(pargs, device, world, rank)
+        line["prefill"] = prefill_record(sub)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    return line
+
+
+def headline(args) -> bool:
+    """The default line (the decode workload as the library runs it), which
+    carries the causal prefill record beside it."""
+    return (args.workload == "decode" and args.op == "attention" and args.schedule == "auto"
+            and not args.mask and not args.no_causal)
+
+
+PREFILL_KEYS = ("metric", "value", "unit", "ms_per_step", "steps", "warmup", "dtype",
+                "clocks", "e2e", "gpu_launches", "roofline", "cpu_baseline", "step_ms_median",
+                "wall_s_timed_region")
+
+
+def prefill_record(sub) -> dict:
+    rec = {k: sub[k] for k in PREFILL_KEYS if k in sub}
+    rec["metric"] = "causal prefill TFLOP/s (4 * H_q * D * visible pairs / device time)"
+    rec["config"] = sub["config"]
+    return rec
+
+
+def measure(args, device, world, rank):
+    """One workload: warm-up, K timed steps (two passes), e2e, cpu baseline;
+    returns the JSON line (rank 0's cpu baseline only)."""
+    import torch
+    from paged_kv_cache_03_gb300 import binding as B
 
     inp = bench_inputs(args)
     bytes_step = algorithmic_bytes(inp) + (mask_bytes(inp) if args.mask else 0)
@@ -598,8 +643,6 @@ def run_ours(args):
         v, secs, desc, cores = time_oracle(inp, args.cpu_seconds, unit_fn, mask_fn)
         line["cpu_baseline"] = {"value": round(v, 6), "unit": value_unit, "cores": cores,
                                 "kind": "oracle", "sample": desc, "seconds": round(secs, 3)}
-    if rank == 0:
-        print(json.dumps(line), flush=True)
     return line
 
 
@@ -975,6 +1018,19 @@ def run_reference(args):
             "e2e": {"value": round(v, 6), "unit": unit, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0},
             "gpu_launches": 0}
+    if headline(args) and not args.no_prefill:
+        # the causal prefill beside it, on a bounded leading sample
+        pinp = synth.workload("prefill")
+        pv, secs, pdesc, _ = time_oracle(pinp, args.cpu_seconds,
+                                         lambda s: algorithmic_flops(s) / 1e12)
+        line["prefill"] = {
+            "metric": "causal prefill TFLOP/s (4 * H_q * D * visible pairs / device time)",
+            "value": round(pv, 6), "unit": "TFLOP/s", "seconds": round(secs, 3),
+            "config": {"workload": workload_desc("prefill", pinp), "sample": pdesc},
+            "cpu_baseline": {"value": round(pv, 6), "unit": "TFLOP/s", "cores": cores,
+                             "kind": "oracle", "sample": pdesc},
+            "e2e": {"value": round(pv, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return line
 
@@ -1051,6 +1107,8 @@ def main(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-prefill", action="store_true",
+                    help="leave the causal prefill record out of the default decode line")
     ap.add_argument("--ref-budget", type=float, default=90.0,
                     help="seconds the reference arm's timed steps should take in total")
     args = ap.parse_args(argv)

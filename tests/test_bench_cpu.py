@@ -91,3 +91,25 @@ def test_reference_arm_of_the_ragged_step():
                       "3", "--ref-budget", "2")
     assert line["impl"] == "reference" and line["unit"] == "GB/s" and line["value"] > 0
     assert line["config"]["workload"].startswith("mixed")
+
+
+def test_reference_arm_default_line_carries_the_prefill_record():
+    """The default (decode) line of the reference arm carries the causal
+    prefill workload's oracle rate beside it, in TFLOP/s."""
+    line = _run_bench("--impl", "reference", "--steps", "3", "--warmup", "3", "--ref-budget",
+                      "2", "--cpu-seconds", "0.5")
+    assert line["unit"] == "GB/s" and line["config"]["workload"].startswith("decode")
+    pre = line["prefill"]
+    assert pre["unit"] == "TFLOP/s" and pre["value"] > 0
+    assert pre["config"]["workload"].startswith("prefill")
+    assert pre["cpu_baseline"]["kind"] == "oracle"
+
+
+def test_headline_rule():
+    import argparse
+    base = dict(workload="decode", op="attention", schedule="auto", mask=False,
+                no_causal=False)
+    assert bench.headline(argparse.Namespace(**base))
+    for k, v in (("workload", "prefill"), ("mask", True), ("schedule", "decode"),
+                 ("no_causal", True), ("op", "append")):
+        assert not bench.headline(argparse.Namespace(**{**base, k: v}))

@@ -22,27 +22,39 @@
 //     leaves one fp32 partial (m, l, o[D]) per piece, merged by
 //     decode_combine_kernel (the split-combine of "Week 2 Day 5", Task 2,
 //     across CTAs instead of SIMD groups).
-//   * One producer warp resolves page ids through the block table and issues
-//     1-D bulk (TMA) copies of the page-contiguous K and V rows of each tile
-//     into a 3-stage shared-memory ring (mbarrier completion by bytes).  A
-//     tile that crosses a page boundary is simply copied as several pieces.
-//   * Seven consumer warps each take TK/7 keys of a stage (seven consumers
-//     plus the producer make eight warps, two per SM sub-partition, so each
-//     thread may hold up to 255 registers).  P lanes share one
-//     key: each lane holds 128/P dims of the query rows in registers (fp32,
-//     pre-scaled), forms partial dot products with packed f32x2 FMAs and
-//     reduces them with warp shuffles.  State stays in registers; the
-//     running max is only moved when a tile raises it by more than 2^8, so
-//     the accumulators are rescaled rarely (the result is unchanged: m only
-//     needs to bound the exponents).
+//   * One producer warp resolves page ids through the block table and fills
+//     a 3-stage shared-memory ring (mbarrier completion by bytes), in one of
+//     two forms:
+//       - bf16 on pages of a multiple of 64 slots, up to 4 query rows per
+//         segment: 128-key tiles that start on 128-key boundaries, landed by
+//         2-D TMA boxes with the 128-byte swizzle (one box per operand half
+//         when a page holds the whole tile; a segment's last, partial tile
+//         in 16-row boxes).  Eight consumer warps take 16 keys each and run
+//         S^T = K Q^T and O^T += V^T P^T on the warp-level tensor cores
+//         (mma m16n8k16 bf16, fragments by ldmatrix from the swizzled tile,
+//         P rounded to bf16 with the row sums adding the rounded weights).
+//       - otherwise: 1-D bulk copies of the page-contiguous K and V rows (a
+//         tile that crosses a page boundary is several pieces), and seven
+//         consumer warps on CUDA cores, TK/7 keys each.  P lanes share one
+//         key: each lane holds 128/P dims of the query rows in registers
+//         (fp32, pre-scaled), forms partial dot products with packed f32x2
+//         FMAs and reduces them with warp shuffles.
+//     Few large copies per tile matter: a measured producer spent about 65
+//     cycles of issue per TMA request, so 28 requests a tile (16-row boxes)
+//     made the single producer warp the bottleneck.
+//   * State stays in registers; the running max is only moved when a tile
+//     raises it by more than 2^8, so the accumulators are rescaled rarely
+//     (the result is unchanged: m only needs to bound the exponents).
 //   * Warps merge their states through shared memory at the end of each
 //     segment piece.  All intra-CTA waits are bounded mbarrier waits.
 #include <cuda_bf16.h>
 
 #include <climits>
+#include <cstring>
 
 #include "internal.h"
 #include "ptx.cuh"
+#include "tc.cuh"
 
 namespace pa {
 namespace {
@@ -69,6 +81,9 @@ struct DecodeParams {
     long long max_S;
     float scale_log2;
     int tk_pages, tk_slots;  // a full tile of TK keys spans TK / ps pages + TK % ps slots
+    // tensor-core consumers: TMA box heights in keys, for a full tile (a divisor
+    // of the page size and of GRAN) and for a segment's last, partial tile
+    int boxr, boxr_tail;
     const float* mask;       // optional additive mask [B * H_q, L, mask_S], or null
     long long mask_S;
     // ragged batch: query rows packed by token [total_q, H_q, D], sequence b
@@ -78,28 +93,44 @@ struct DecodeParams {
     int route_mixed;  // 1: sequences with more than L query positions belong to the tiles
 };
 
-template <typename T, int RB_, int P_, int TK_, int NCW_, int NST_, int MINB_ = 1, int GRAN_ = 0>
+// MMA_: the consumers run Q.K^T and P.V on the warp-level tensor cores
+// (mma m16n8k16, bf16) over K/V tiles that TMA boxes land 128-byte swizzled;
+// otherwise they run them on CUDA cores over rows copied as they lie.
+template <typename T, int RB_, int P_, int TK_, int NCW_, int NST_, int MINB_ = 1, int GRAN_ = 0,
+          bool MMA_ = false>
 struct Cfg {
     using Elem = T;
     static constexpr int RB = RB_;    // query rows per segment
-    static constexpr int P = P_;      // lanes sharing one key
+    static constexpr int P = P_;      // lanes sharing one key (CUDA-core consumers)
     static constexpr int TK = TK_;    // keys per stage
     static constexpr int NCW = NCW_;  // consumer warps
     static constexpr int NST = NST_;  // pipeline stages
     static constexpr int MINB = MINB_;  // CTAs resident per SM
+    static constexpr bool MMA = MMA_;
     static constexpr int ES = sizeof(T);
     static constexpr int ROW = kD * ES;
     static constexpr int HDR = 128;
     static constexpr int QBYTES = RB * ROW;
     static constexpr int KBYTES = TK * ROW;
-    static constexpr int STAGE = HDR + QBYTES + 2 * KBYTES;
+    // Stage layout.  CUDA-core consumers: header, query rows, K rows, V rows
+    // (256-byte rows as they lie in the pool).  Tensor-core consumers: K and
+    // V each as two 64-dim halves of TK rows x 128 bytes (128-byte swizzle,
+    // every half 1024-byte aligned), then the query rows and the header.
+    static constexpr int KHALF = TK * 128;
+    static constexpr int OFF_K = MMA ? 0 : HDR + QBYTES;
+    static constexpr int OFF_V = MMA ? 2 * KHALF : HDR + QBYTES + KBYTES;
+    static constexpr int OFF_Q = MMA ? 4 * KHALF : HDR;
+    static constexpr int OFF_HDR = MMA ? 4 * KHALF + QBYTES : 0;
+    static constexpr int STAGE =
+        MMA ? (4 * KHALF + QBYTES + HDR + 1023) / 1024 * 1024 : HDR + QBYTES + 2 * KBYTES;
     // merge record per (warp, row): o[128] then m, l (16-byte aligned rows)
     static constexpr int MSTRIDE = kD + 4;
     static constexpr int MERGE = (NCW * RB * MSTRIDE * 4 + 127) / 128 * 128;
     // per-warp softmax weights of one stage, [KPW keys][RB rows]
-    static constexpr int PBUF = (NCW * (TK / NCW) * RB * 4 + 127) / 128 * 128;
+    static constexpr int PBUF = MMA ? 0 : (NCW * (TK / NCW) * RB * 4 + 127) / 128 * 128;
     static constexpr int NBARS = 2 * NST + 2;
-    static constexpr int SMEM = NST * STAGE + MERGE + PBUF + NBARS * 8;
+    // (+1024: the tensor-core layout aligns its base to 1024 bytes)
+    static constexpr int SMEM = NST * STAGE + MERGE + PBUF + NBARS * 8 + (MMA ? 1024 : 0);
     static constexpr int THREADS = (NCW + 1) * 32;
     static constexpr int KPW = TK / NCW;  // keys per warp per stage
     // Keys per unit of the split over CTAs (a power of two dividing TK);
@@ -115,7 +146,10 @@ struct Cfg {
     static_assert(DPL % CH == 0 && DPL % 2 == 0, "lane dims must be whole chunks");
     static_assert(STAGE % 128 == 0, "stage alignment");
     static constexpr int PIECE_ITERS = (TK + 31) / 32;  // page pieces per producer lane (ps = 1)
-    static_assert((THREADS * MINB) % 128 == 0, "whole warps per SM sub-partition");
+    static_assert(MMA || (THREADS * MINB) % 128 == 0, "whole warps per SM sub-partition");
+    static_assert(!MMA || (ES == 2 && KPW == 16 && RB <= 8 && KHALF % 1024 == 0 &&
+                           GRAN % 16 == 0),
+                  "tensor-core consumers: bf16, 16 keys per warp, up to 8 rows");
 };
 
 struct alignas(16) StageHdr {
@@ -398,13 +432,70 @@ __device__ __forceinline__ void store4<float>(float* base, long long idx, float4
     *reinterpret_cast<float4*>(base + idx) = v;
 }
 
+// The end of a segment piece, once this warp has written its record (o[D],
+// m, l per row) into the merge buffer: after every consumer warp has, warp r
+// merges row r (and r + NCW, ...) over the warps' records, four dims per
+// lane, and writes the normalised output (a piece that is the whole segment)
+// or an fp32 partial for the combine kernel.  Returns false if a wait timed
+// out.
+template <class C, bool kVar>
+__device__ __forceinline__ bool merge_piece(const DecodeParams& p, const StageHdr& h, int hLb,
+                                            const float* merge, int warp, int lane,
+                                            uint32_t mfull, uint32_t mdone, int nend) {
+    using T = typename C::Elem;
+    if (lane == 0) mbar_arrive(mfull);
+    if (!__all_sync(0xffffffffu, mbar_wait(mfull, nend & 1))) return false;
+    const int rows_valid = min(C::RB, p.G * hLb - h.chunk * C::RB);
+    const long long slot = h.slot;
+    T* const out = static_cast<T*>(p.out);
+    for (int r = warp; r < rows_valid; r += C::NCW) {
+        float M = neg_inf();
+#pragma unroll
+        for (int wq = 0; wq < C::NCW; ++wq) M = fmaxf(M, merge[(wq * C::RB + r) * C::MSTRIDE + kD]);
+        float den = 0.f;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (M != neg_inf()) {
+#pragma unroll
+            for (int wq = 0; wq < C::NCW; ++wq) {
+                const float* rec = merge + (wq * C::RB + r) * C::MSTRIDE;
+                const float a = fast_exp2(rec[kD] - M);
+                den += a * rec[kD + 1];
+                const float4 ov = *reinterpret_cast<const float4*>(rec + 4 * lane);
+                acc.x += a * ov.x;
+                acc.y += a * ov.y;
+                acc.z += a * ov.z;
+                acc.w += a * ov.w;
+            }
+        }
+        if (h.flags & kFinal) {
+            const float inv = den > 0.f ? 1.f / den : 0.f;
+            store4<T>(out, out_row<kVar>(p, h.b, h.kvh, hLb, h.q0, h.chunk * C::RB + r) * kD + 4 * lane,
+                      make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv));
+        } else {
+            *reinterpret_cast<float4*>(p.part_o + (slot * C::RB + r) * kD + 4 * lane) = acc;
+            if (lane == 0) p.part_ml[slot * C::RB + r] = make_float2(M, den);
+        }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(mdone);
+    return __all_sync(0xffffffffu, mbar_wait(mdone, nend & 1));
+}
+
 // F: 0 plain, 1 with an explicit mask, 2 a ragged batch.  Separate
 // instantiations, so the plain kernel carries none of the others' code.
 template <class C, int F>
-__global__ void __launch_bounds__(C::THREADS, C::MINB) decode_split_kernel(const DecodeParams p) {
+__global__ void __launch_bounds__(C::THREADS, C::MINB)
+    decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
+                        const __grid_constant__ CUtensorMap tm_v,
+                        const __grid_constant__ CUtensorMap tm_kt,
+                        const __grid_constant__ CUtensorMap tm_vt, const DecodeParams p) {
     using T = typename C::Elem;
     constexpr bool kMask = F == 1, kVar = F == 2;
-    extern __shared__ __align__(128) uint8_t smem[];
+    static_assert(!(C::MMA && kMask), "the tensor-core consumers take no explicit mask");
+    extern __shared__ __align__(128) uint8_t smem_raw[];
+    // the tensor-core layout's swizzled halves need a 1024-byte aligned base
+    uint8_t* const smem =
+        C::MMA ? smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u) : smem_raw;
     uint8_t* const stage0 = smem;
     float* const merge = reinterpret_cast<float*>(smem + C::NST * C::STAGE);
     float* const pbuf_all = reinterpret_cast<float*>(smem + C::NST * C::STAGE + C::MERGE);
@@ -526,6 +617,35 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB) decode_split_kernel(const
             const int nrows = min(C::RB, p.G * (kVar ? w.Lb : p.L) - row0);
             int pid[C::PIECE_ITERS], klo[C::PIECE_ITERS], kn[C::PIECE_ITERS];
             bool any_bad = false;
+            uint32_t bytes;
+            int box_row = -1;  // tensor-core layout: pool row of this lane's box
+            const bool full_tile = nvalid == C::TK;
+            const int bh = full_tile ? p.boxr : p.boxr_tail;  // box height of this tile
+            if constexpr (C::MMA) {
+                // Boxes of bh keys, lane i copying box i (keys key0 + i * bh ...):
+                // a full tile in boxes of p.boxr keys (one box when a page holds
+                // the whole tile), a segment's last, partial tile in boxes of
+                // p.boxr_tail keys.  Box heights divide the page size and every
+                // tile start, so no box crosses a page.  The last box may run past
+                // the context into unused page slots (< boxr_tail rows); the
+                // consumers mask those keys and zero those V rows.
+                const int nb = (nvalid + bh - 1) / bh;
+                const bool act = lane < nb;
+                const int off = w.slot + lane * bh;  // from the start of page w.lp
+                const int lpo = off / p.ps;
+                const int id = page_id<C>(p, w, w.lp + lpo, act);
+                if (act) {
+                    if (id >= 0 && id < p.num_pages)
+                        box_row = (id * p.H_kv + w.kvh) * p.ps + (off - lpo * p.ps);
+                    else
+                        any_bad = true;
+                }
+                const int good = __popc(__ballot_sync(0xffffffffu, box_row >= 0));
+                bytes = static_cast<uint32_t>(good) * 4u * 128u * static_cast<uint32_t>(bh) +
+                        (start ? static_cast<uint32_t>(nrows) * C::ROW : 0u);
+                if (any_bad) atomicOr(p.flag, PA_FLAG_BAD_PAGE);
+            }
+            if constexpr (!C::MMA) {
 #pragma unroll
             for (int k = 0; k < C::PIECE_ITERS; ++k) {
                 pid[k] = -1;
@@ -547,11 +667,12 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB) decode_split_kernel(const
                     }
                 }
             }
+            }
             // bytes the stage will receive: all K/V rows of the tile (plus the
             // query rows at a piece start), minus pieces with a bad page id
-            uint32_t bytes = 2u * static_cast<uint32_t>(nvalid) * C::ROW +
-                             (start ? static_cast<uint32_t>(nrows) * C::ROW : 0u);
-            if (__ballot_sync(0xffffffffu, any_bad)) {
+            if constexpr (!C::MMA) bytes = 2u * static_cast<uint32_t>(nvalid) * C::ROW +
+                                           (start ? static_cast<uint32_t>(nrows) * C::ROW : 0u);
+            if (!C::MMA && __ballot_sync(0xffffffffu, any_bad)) {
                 uint32_t miss = 0;
 #pragma unroll
                 for (int k = 0; k < C::PIECE_ITERS; ++k)
@@ -583,14 +704,28 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB) decode_split_kernel(const
             uint8_t* const st = stage0 + stage * C::STAGE;
             if (lane == 0) {
                 const int seg_id = (w.b * p.H_kv + w.kvh) * p.nchunk + w.chunk_r;
-                uint4* h = reinterpret_cast<uint4*>(st);
+                uint4* h = reinterpret_cast<uint4*>(st + C::OFF_HDR);
                 h[0] = make_uint4(seg_id, w.b, w.kvh, w.chunk_r);
                 h[1] = make_uint4(w.key0, nvalid, w.S, flags);
                 h[2] = make_uint4(seg_id + w.chunk, w.Lb, w.q0, 0);
                 mbar_arrive_expect_tx(fb, bytes);
             }
             __syncwarp();
-            const uint32_t kdst = smem_u32(st) + C::HDR + C::QBYTES;
+            const uint32_t kdst = smem_u32(st) + C::OFF_K;
+            if constexpr (C::MMA) {
+                if (box_row >= 0) {
+                    const uint32_t kd = kdst + static_cast<uint32_t>(lane * bh) * 128u;
+                    const uint32_t vd = smem_u32(st) + C::OFF_V +
+                                        static_cast<uint32_t>(lane * bh) * 128u;
+                    const CUtensorMap* mk = full_tile ? &tm_k : &tm_kt;
+                    const CUtensorMap* mv = full_tile ? &tm_v : &tm_vt;
+                    tc::tma_load_2d(kd, mk, 0, box_row, fb, pol);
+                    tc::tma_load_2d(kd + C::KHALF, mk, 64, box_row, fb, pol);
+                    tc::tma_load_2d(vd, mv, 0, box_row, fb, pol);
+                    tc::tma_load_2d(vd + C::KHALF, mv, 64, box_row, fb, pol);
+                }
+            }
+            if constexpr (!C::MMA) {
 #pragma unroll
             for (int k = 0; k < C::PIECE_ITERS; ++k) {
                 if (pid[k] < 0) continue;
@@ -602,14 +737,15 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB) decode_split_kernel(const
                 bulk_g2s(kdst + off, kp + row * C::ROW, nb, fb, pol);
                 bulk_g2s(kdst + C::KBYTES + off, vp + row * C::ROW, nb, fb, pol);
             }
+            }
             if (start) {
                 if constexpr (!kVar) {  // the segment's rows are contiguous
                     if (lane == 0)
-                        bulk_g2s(smem_u32(st) + C::HDR,
+                        bulk_g2s(smem_u32(st) + C::OFF_Q,
                                  qp + out_row<false>(p, w.b, w.kvh, p.L, 0, row0) * C::ROW,
                                  static_cast<uint32_t>(nrows) * C::ROW, fb, pol);
                 } else if (lane < nrows) {  // one token-major row per lane
-                    bulk_g2s(smem_u32(st) + C::HDR + lane * C::ROW,
+                    bulk_g2s(smem_u32(st) + C::OFF_Q + lane * C::ROW,
                              qp + out_row<true>(p, w.b, w.kvh, w.Lb, w.q0, row0 + lane) * C::ROW,
                              C::ROW, fb, pol);
                 }
@@ -686,6 +822,196 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB) decode_split_kernel(const
     }
 
     // ============================ consumer warps ============================
+    if constexpr (C::MMA) {
+        // Tensor-core consumers.  Warp w takes keys kw0 .. kw0 + 15 of each
+        // stage and computes S^T = K Q^T (m16n8k16: 16 keys x 8 query rows,
+        // rows past RB are zero) and O^T += V^T P^T (16 dims x 8 rows per
+        // instruction, 8 of them for D = 128).  Lane 4g + t holds the scores
+        // of keys g and g + 8 for rows 2t and 2t + 1, and O^T of dims
+        // 16 i + g and 16 i + g + 8 for the same two rows.  P is rounded to
+        // bf16 for the product, and the row sums add the rounded weights.
+        const int g = lane >> 2, t4 = lane & 3;
+        const int kw0 = warp * C::KPW;
+        uint32_t qf[8][2];   // Q^T B fragments of the 8 k-steps (16 dims each)
+        float oacc[8][4];    // O^T accumulators
+        float m_r[2] = {neg_inf(), neg_inf()}, l_r[2] = {0.f, 0.f};
+        int lpos[2] = {0, 0};  // query positions of rows 2t, 2t + 1
+        int lmin = 0;
+        int nend = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            qf[i][0] = qf[i][1] = 0u;
+            oacc[i][0] = oacc[i][1] = oacc[i][2] = oacc[i][3] = 0.f;
+        }
+        for (int i = 0;; ++i) {
+            const int stage = i % C::NST;
+            if (!__all_sync(0xffffffffu, mbar_wait(full0 + 8 * stage, (i / C::NST) & 1))) {
+                if (lane == 0) atomicOr(p.flag, PA_FLAG_TIMEOUT);
+                s_abort = 1;
+                break;
+            }
+            if ((i & 7) == 0 && __any_sync(0xffffffffu, s_abort != 0)) break;
+            uint8_t* const st = stage0 + stage * C::STAGE;
+            const StageHdr h = *reinterpret_cast<const StageHdr*>(st + C::OFF_HDR);
+            const int hLb = kVar ? h.Lb : p.L;
+
+            if (h.flags & kStart) {
+                const int rows = p.G * hLb - h.chunk * C::RB;
+                const bool qrow_ok = g < C::RB && g < rows;
+                const uint8_t* const qrow = st + C::OFF_Q + g * C::ROW;
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks) {
+                    qf[ks][0] = qrow_ok ? *reinterpret_cast<const uint32_t*>(qrow + (ks * 16 + 2 * t4) * 2) : 0u;
+                    qf[ks][1] = qrow_ok ? *reinterpret_cast<const uint32_t*>(qrow + (ks * 16 + 8 + 2 * t4) * 2) : 0u;
+                }
+#pragma unroll
+                for (int mt = 0; mt < 8; ++mt)
+                    oacc[mt][0] = oacc[mt][1] = oacc[mt][2] = oacc[mt][3] = 0.f;
+                m_r[0] = m_r[1] = neg_inf();
+                l_r[0] = l_r[1] = 0.f;
+                lmin = INT_MAX;
+#pragma unroll
+                for (int r = 0; r < C::RB; ++r)
+                    lmin = min(lmin, r < rows ? (h.chunk * C::RB + r) % hLb : hLb - 1);
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int r = 2 * t4 + e;
+                    lpos[e] = (r < C::RB && r < rows) ? (h.chunk * C::RB + r) % hLb : hLb - 1;
+                }
+            }
+
+            if (h.nvalid > kw0) {
+                // The last box of a context may bring unused page slots past it
+                // (any contents): their scores are masked below, and their V
+                // rows are zeroed here, since a weight of 0 times NaN is NaN.
+                {
+                    const int zlo = h.nvalid;
+                    const int zhi =
+                        min(kw0 + C::KPW, (h.nvalid + p.boxr_tail - 1) / p.boxr_tail * p.boxr_tail);
+                    if (zlo < zhi) {  // uniform over the warp
+                        for (int idx = lane; idx < (zhi - zlo) * 16; idx += 32) {
+                            const int r = zlo + (idx >> 4), c = idx & 15;
+                            *reinterpret_cast<uint4*>(st + C::OFF_V + (c >> 3) * C::KHALF + r * 128 +
+                                                      (((c & 7) ^ (r & 7)) << 4)) =
+                                make_uint4(0u, 0u, 0u, 0u);
+                        }
+                        fence_proxy_async_smem();  // before the stage's next TMA fill
+                        __syncwarp();
+                    }
+                }
+                // S^T = K Q^T over the 8 k-steps of 16 dims
+                float sacc[4] = {0.f, 0.f, 0.f, 0.f};
+                {
+                    const int r = kw0 + (lane & 7) + ((lane >> 3) & 1) * 8;
+                    const uint32_t rb = smem_u32(st) + C::OFF_K + r * 128;
+#pragma unroll
+                    for (int ks = 0; ks < 8; ++ks) {
+                        const int c = ks * 2 + (lane >> 4);
+                        uint32_t a[4];
+                        ldmatrix_x4(a, rb + (c >> 3) * C::KHALF + (((c & 7) ^ (r & 7)) << 4));
+                        mma_16816(sacc, a, qf[ks][0], qf[ks][1]);
+                    }
+                }
+                // log2-unit scores; keys past the context or a row's causal
+                // frontier get -inf
+                const float c = p.scale_log2;
+                float x[4] = {sacc[0] * c, sacc[1] * c, sacc[2] * c, sacc[3] * c};
+                const int last_key = h.key0 + kw0 + C::KPW - 1;
+                if (h.nvalid < kw0 + C::KPW || (p.causal && last_key > lmin + h.S - hLb)) {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int kl = kw0 + g + (e >> 1) * 8;
+                        const bool vis = kl < h.nvalid &&
+                                         (!p.causal || h.key0 + kl <= lpos[e & 1] + h.S - hLb);
+                        if (!vis) x[e] = neg_inf();
+                    }
+                }
+                float mt0 = fmaxf(x[0], x[2]), mt1 = fmaxf(x[1], x[3]);
+#pragma unroll
+                for (int o = 4; o < 32; o <<= 1) {
+                    mt0 = fmaxf(mt0, __shfl_xor_sync(0xffffffffu, mt0, o));
+                    mt1 = fmaxf(mt1, __shfl_xor_sync(0xffffffffu, mt1, o));
+                }
+                const bool gr0 = mt0 > m_r[0] + kLazyRescaleLog2;
+                const bool gr1 = mt1 > m_r[1] + kLazyRescaleLog2;
+                if (__any_sync(0xffffffffu, gr0 || gr1)) {
+                    // rows whose max grew by more than 2^8 move it and rescale
+                    const float a0 = gr0 ? fast_exp2(m_r[0] - mt0) : 1.f;  // 2^-inf = 0
+                    const float a1 = gr1 ? fast_exp2(m_r[1] - mt1) : 1.f;
+                    if (gr0) m_r[0] = mt0;
+                    if (gr1) m_r[1] = mt1;
+                    l_r[0] *= a0;
+                    l_r[1] *= a1;
+#pragma unroll
+                    for (int mt = 0; mt < 8; ++mt) {
+                        oacc[mt][0] *= a0;
+                        oacc[mt][1] *= a1;
+                        oacc[mt][2] *= a0;
+                        oacc[mt][3] *= a1;
+                    }
+                }
+                const float mu0 = m_r[0] == neg_inf() ? 0.f : m_r[0];
+                const float mu1 = m_r[1] == neg_inf() ? 0.f : m_r[1];
+                // P^T as bf16: (key g, rows 2t, 2t+1) and (key g + 8, ...), each
+                // an 8 x 8 block in C layout, transposed into B fragments
+                const uint32_t X0 = pack_bf16x2(fast_exp2(x[0] - mu0), fast_exp2(x[1] - mu1));
+                const uint32_t X1 = pack_bf16x2(fast_exp2(x[2] - mu0), fast_exp2(x[3] - mu1));
+                {
+                    const float2 f0 = bf16x2_to_float2(X0), f1 = bf16x2_to_float2(X1);
+                    l_r[0] += f0.x + f1.x;
+                    l_r[1] += f0.y + f1.y;
+                }
+                const uint32_t pb0 = movmatrix_trans(X0), pb1 = movmatrix_trans(X1);
+                // O^T += V^T P^T, 16 dims per instruction
+                {
+                    const int r = kw0 + (lane & 7) + (lane >> 4) * 8;
+                    const uint32_t rb = smem_u32(st) + C::OFF_V + r * 128;
+#pragma unroll
+                    for (int mt = 0; mt < 8; ++mt) {
+                        const int cc = mt * 2 + ((lane >> 3) & 1);
+                        uint32_t a[4];
+                        ldmatrix_x4_trans(a, rb + (cc >> 3) * C::KHALF + (((cc & 7) ^ (r & 7)) << 4));
+                        mma_16816(oacc[mt], a, pb0, pb1);
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(empty0 + 8 * stage);
+
+            if (h.flags & kEnd) {
+                // this warp's record: o[D], m, l of every row of the piece
+#pragma unroll
+                for (int o = 4; o < 32; o <<= 1) {
+                    l_r[0] += __shfl_xor_sync(0xffffffffu, l_r[0], o);
+                    l_r[1] += __shfl_xor_sync(0xffffffffu, l_r[1], o);
+                }
+                float* const mw = merge + warp * C::RB * C::MSTRIDE;
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int r = 2 * t4 + e;
+                    if (r < C::RB) {
+#pragma unroll
+                        for (int mt = 0; mt < 8; ++mt) {
+                            mw[r * C::MSTRIDE + 16 * mt + g] = oacc[mt][e];
+                            mw[r * C::MSTRIDE + 16 * mt + g + 8] = oacc[mt][2 + e];
+                        }
+                        if (g == 0) {
+                            mw[r * C::MSTRIDE + kD] = m_r[e];
+                            mw[r * C::MSTRIDE + kD + 1] = l_r[e];
+                        }
+                    }
+                }
+                __syncwarp();
+                if (!merge_piece<C, kVar>(p, h, hLb, merge, warp, lane, mfull, mdone, nend)) {
+                    if (lane == 0) atomicOr(p.flag, PA_FLAG_TIMEOUT);
+                    s_abort = 1;
+                    break;
+                }
+                ++nend;
+            }
+            if (h.flags & kLast) break;
+        }
+    } else {
     // Q.K^T: P lanes share one key (each holds DPL dims of every query row in
     // registers); after the transposed reduction each lane owns the score of
     // row `rho` of its group's key, so exp2 and the running sum run once per
@@ -702,7 +1028,6 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB) decode_split_kernel(const
     int lrow_mine = 0;
     int lmin = 0;
     int nend = 0;
-    T* const out = static_cast<T*>(p.out);
 #pragma unroll
     for (int r = 0; r < C::RB; ++r) {
 #pragma unroll
@@ -719,7 +1044,7 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB) decode_split_kernel(const
         }
         if ((i & 7) == 0 && __any_sync(0xffffffffu, s_abort != 0)) break;
         const uint8_t* const st = stage0 + stage * C::STAGE;
-        const StageHdr h = *reinterpret_cast<const StageHdr*>(st);
+        const StageHdr h = *reinterpret_cast<const StageHdr*>(st + C::OFF_HDR);
         const int hLb = kVar ? h.Lb : p.L;  // the segment's query positions
 
         if (h.flags & kStart) {
@@ -727,7 +1052,7 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB) decode_split_kernel(const
             lmin = INT_MAX;
 #pragma unroll
             for (int r = 0; r < C::RB; ++r) {
-                load_row<C>(st + C::HDR + r * C::ROW, li, q2[r]);
+                load_row<C>(st + C::OFF_Q + r * C::ROW, li, q2[r]);
 #pragma unroll
                 for (int e = 0; e < C::DPL / 2; ++e) {
                     q2[r][e].x *= p.scale_log2;
@@ -743,8 +1068,8 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB) decode_split_kernel(const
 
         const int kw0 = warp * C::KPW;
         if (h.nvalid > kw0) {
-            const uint8_t* const Ks = st + C::HDR + C::QBYTES;
-            const uint8_t* const Vs = Ks + C::KBYTES;
+            const uint8_t* const Ks = st + C::OFF_K;
+            const uint8_t* const Vs = st + C::OFF_V;
             // An explicit additive mask joins the score of (key, row) in log2
             // units before the max; its loads go out before the dot products.
             float mv[C::IT];
@@ -867,49 +1192,7 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB) decode_split_kernel(const
                 mw[rho * C::MSTRIDE + kD + 1] = l_mine;
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive(mfull);
-            if (!__all_sync(0xffffffffu, mbar_wait(mfull, nend & 1))) {
-                if (lane == 0) atomicOr(p.flag, PA_FLAG_TIMEOUT);
-                s_abort = 1;
-                break;
-            }
-            const int rows_valid = min(C::RB, p.G * hLb - h.chunk * C::RB);
-            const long long slot = h.slot;
-            // warp r merges row r (and r + NCW, ...), four dims per lane
-            for (int r = warp; r < rows_valid; r += C::NCW) {
-                float M = neg_inf();
-#pragma unroll
-                for (int wq = 0; wq < C::NCW; ++wq)
-                    M = fmaxf(M, merge[(wq * C::RB + r) * C::MSTRIDE + kD]);
-                float den = 0.f;
-                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (M != neg_inf()) {
-#pragma unroll
-                    for (int wq = 0; wq < C::NCW; ++wq) {
-                        const float* rec = merge + (wq * C::RB + r) * C::MSTRIDE;
-                        const float a = fast_exp2(rec[kD] - M);
-                        den += a * rec[kD + 1];
-                        const float4 ov = *reinterpret_cast<const float4*>(rec + 4 * lane);
-                        acc.x += a * ov.x;
-                        acc.y += a * ov.y;
-                        acc.z += a * ov.z;
-                        acc.w += a * ov.w;
-                    }
-                }
-                if (h.flags & kFinal) {
-                    const float inv = den > 0.f ? 1.f / den : 0.f;
-                    store4<T>(out,
-                              out_row<kVar>(p, h.b, h.kvh, hLb, h.q0, h.chunk * C::RB + r) * kD +
-                                  4 * lane,
-                              make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv));
-                } else {
-                    *reinterpret_cast<float4*>(p.part_o + (slot * C::RB + r) * kD + 4 * lane) = acc;
-                    if (lane == 0) p.part_ml[slot * C::RB + r] = make_float2(M, den);
-                }
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(mdone);
-            if (!__all_sync(0xffffffffu, mbar_wait(mdone, nend & 1))) {
+            if (!merge_piece<C, kVar>(p, h, hLb, merge, warp, lane, mfull, mdone, nend)) {
                 if (lane == 0) atomicOr(p.flag, PA_FLAG_TIMEOUT);
                 s_abort = 1;
                 break;
@@ -917,6 +1200,7 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB) decode_split_kernel(const
             ++nend;
         }
         if (h.flags & kLast) break;
+    }
     }
     pdl_wait_primary();
 }
@@ -1016,8 +1300,13 @@ WsLayout ws_layout(const pa_shape& sh, int grid, int RB) {
     return w;
 }
 
+struct PoolMaps {
+    CUtensorMap k, v, kt, vt;  // full tiles, partial tiles
+};
+
 template <class C, int F>
-pa_status launch_split_combine(const Call& c, const DecodeParams& p, int grid, long long nseg) {
+pa_status launch_split_combine(const Call& c, const DecodeParams& p, int grid, long long nseg,
+                               const PoolMaps& m) {
     static int attr_done[64] = {0};
     if (c.dev.device >= 0 && c.dev.device < 64 && !attr_done[c.dev.device]) {
         if (cudaFuncSetAttribute(decode_split_kernel<C, F>,
@@ -1038,10 +1327,11 @@ pa_status launch_split_combine(const Call& c, const DecodeParams& p, int grid, l
         attr[0].val.programmaticStreamSerializationAllowed = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        if (cudaLaunchKernelEx(&cfg, decode_split_kernel<C, F>, p) != cudaSuccess)
+        if (cudaLaunchKernelEx(&cfg, decode_split_kernel<C, F>, m.k, m.v, m.kt, m.vt, p) !=
+            cudaSuccess)
             return PA_ERR_CUDA;
     } else {
-        decode_split_kernel<C, F><<<grid, C::THREADS, C::SMEM, c.stream>>>(p);
+        decode_split_kernel<C, F><<<grid, C::THREADS, C::SMEM, c.stream>>>(m.k, m.v, m.kt, m.vt, p);
         if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
     }
     if (c.ev_after && cudaEventRecord(c.ev_after, c.stream) != cudaSuccess) return PA_ERR_CUDA;
@@ -1106,10 +1396,45 @@ pa_status launch_cfg(const Call& c) {
     p.route_mixed = c.route_mixed;
     p.tk_pages = C::TK / sh.page_size;
     p.tk_slots = C::TK % sh.page_size;
+    // tensor-core consumers: K and V land through 2-D maps over the pools,
+    // boxes of gcd(page_size, GRAN) rows for full tiles and of 16 (or 8) rows
+    // for a segment's last tile
+    {
+        int a = sh.page_size, b = C::GRAN;
+        while (b) {
+            const int t = a % b;
+            a = b;
+            b = t;
+        }
+        p.boxr = a;
+    }
+    p.boxr_tail = sh.page_size % 16 == 0 ? 16 : 8;
+    PoolMaps m;
+    memset(&m, 0, sizeof m);
+    if constexpr (C::MMA) {
+        const long long pool_rows = static_cast<long long>(sh.num_pages) * sh.H_kv * sh.page_size;
+        if (!make_map(&m.k, c.kp, pool_rows, p.boxr) || !make_map(&m.v, c.vp, pool_rows, p.boxr) ||
+            !make_map(&m.kt, c.kp, pool_rows, p.boxr_tail) ||
+            !make_map(&m.vt, c.vp, pool_rows, p.boxr_tail))
+            return PA_ERR_CUDA;
+        if (c.cu_q) return launch_split_combine<C, 2>(c, p, grid, w.nseg, m);
+        return launch_split_combine<C, 0>(c, p, grid, w.nseg, m);
+    } else {
+        if (c.cu_q) return launch_split_combine<C, 2>(c, p, grid, w.nseg, m);
+        if (c.mask) return launch_split_combine<C, 1>(c, p, grid, w.nseg, m);
+        return launch_split_combine<C, 0>(c, p, grid, w.nseg, m);
+    }
+}
 
-    if (c.cu_q) return launch_split_combine<C, 2>(c, p, grid, w.nseg);
-    if (c.mask) return launch_split_combine<C, 1>(c, p, grid, w.nseg);
-    return launch_split_combine<C, 0>(c, p, grid, w.nseg);
+// The tensor-core consumers (128-key tiles that start on 128-key boundaries,
+// up to 4 query rows per segment) take bf16 without an explicit mask on pages
+// of a multiple of 64 slots: a full tile is then one or two TMA boxes per
+// operand half.  Smaller pages would need up to 16 boxes a tile, and the
+// producer's issue cost would bind; those keep the CUDA-core consumers and 1-D
+// bulk copies.
+bool decode_mma_ok(const Call& c) {
+    return c.sh.dtype == PA_BF16 && !c.mask && c.sh.page_size % 64 == 0 &&
+           decode_rows_per_chunk(c.sh) <= 4;
 }
 
 }  // namespace
@@ -1141,6 +1466,13 @@ size_t workspace_bytes_total(const pa_shape& sh, int sm_count) {
 pa_status decode_launch(const Call& c) {
     const int RB = decode_rows_per_chunk(c.sh);
     using bf = __nv_bfloat16;
+    if (decode_mma_ok(c)) {
+        switch (RB) {
+            case 1: return launch_cfg<Cfg<bf, 1, 8, 128, 8, 3, 1, 128, true>>(c);
+            case 2: return launch_cfg<Cfg<bf, 2, 8, 128, 8, 3, 1, 128, true>>(c);
+            default: return launch_cfg<Cfg<bf, 4, 8, 128, 8, 3, 1, 128, true>>(c);
+        }
+    }
     if (c.sh.dtype == PA_BF16) {
         switch (RB) {
             case 1: return launch_cfg<Cfg<bf, 1, 8, 112, 7, 3>>(c);

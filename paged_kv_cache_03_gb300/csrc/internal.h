@@ -4,6 +4,7 @@
 #include <cstddef>
 #include <cstdint>
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "paged_attn.h"
@@ -82,6 +83,10 @@ pa_status decode_launch(const Call& c);
 
 // ---- prefill schedule (tcgen05 tensor cores) ------------------------------
 bool prefill_supported(const pa_shape& sh);
+// 2-D TMA map over a bf16 row-major [rows, 128] matrix (the K or V pool seen
+// as rows (page * H_kv + kv_head) * page_size + slot), boxes of 64 dims x
+// box_rows rows, 128-byte swizzle.
+bool make_map(CUtensorMap* map, const void* ptr, long long rows, int box_rows);
 pa_status prefill_launch(const Call& c);
 
 // ---- K/V append -----------------------------------------------------------

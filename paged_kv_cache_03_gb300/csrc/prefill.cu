@@ -700,9 +700,12 @@ __global__ void __launch_bounds__(1024) pair_plan_kernel(const int32_t* cu_q, in
     if (tid == 0) pair_prefix[B] = carry_s;
 }
 
+}  // namespace
+
 // ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
+namespace {
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static std::once_flag once;
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -719,6 +722,8 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
+}  // namespace
+
 // 2-D bf16 map over a row-major [rows, 128] matrix, boxes of 64 x box_rows,
 // 128-byte swizzle.
 bool make_map(CUtensorMap* map, const void* ptr, long long rows, int box_rows) {
@@ -732,6 +737,8 @@ bool make_map(CUtensorMap* map, const void* ptr, long long rows, int box_rows) {
               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
+
+namespace {
 
 // Token-major query map (D, H_q, tokens): one box = box_rows tokens of one
 // head, laid out in shared memory exactly like a box of the 2-D map.

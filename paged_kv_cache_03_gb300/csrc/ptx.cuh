@@ -151,4 +151,40 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return r;
 }
 
+// ---- warp-level tensor-core MMA (m16n8k16, bf16 in, fp32 accumulate) ------
+// Fragment layouts (lane = 4 * g + t): A (16 x 16, row-major) regs {a0..a3} =
+// rows {g, g + 8, g, g + 8} x cols {2t, 2t, 2t + 8, 2t + 8} (+1 in the high
+// half); B (16 x 8, k x n) regs {b0, b1} = k {2t, 2t + 8} (+1) x n = g; C/D
+// (16 x 8) {c0..c3} = (g, 2t), (g, 2t + 1), (g + 8, 2t), (g + 8, 2t + 1).
+__device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                          uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Four 8 x 8 b16 matrices from shared memory: lanes 8i .. 8i + 7 give the
+// row addresses (16 bytes each) of matrix i; lane 4g + t receives row g,
+// elements 2t and 2t + 1 of each (the transposed matrix with .trans).
+__device__ __forceinline__ void ldmatrix_x4(uint32_t (&r)[4], uint32_t addr) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+__device__ __forceinline__ void ldmatrix_x4_trans(uint32_t (&r)[4], uint32_t addr) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+
+// Transposes an 8 x 8 b16 matrix held one 32-bit word per lane (lane 4g + t:
+// row g, elements 2t, 2t + 1).
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t a) {
+    uint32_t d;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(a));
+    return d;
+}
+
 }  // namespace pa

@@ -196,7 +196,7 @@ def load_peaks():
 # The sources each kernel is built from: its recorded DRAM traffic stays valid
 # while these are unchanged.
 KERNEL_SOURCES = {
-    "decode_split_kernel": ("decode.cu", "ptx.cuh", "internal.h"),
+    "decode_split_kernel": ("decode.cu", "ptx.cuh", "tc.cuh", "internal.h"),
     "prefill_tile_kernel": ("prefill.cu", "tc.cuh", "ptx.cuh", "internal.h"),
     "append_kv_kernel": ("append.cu", "internal.h"),
 }

@@ -17,6 +17,8 @@ constexpr int kHeadDim = 128;
 constexpr size_t kFlagBytes = 256;
 constexpr size_t kChunkCounterOffset = 64;
 constexpr size_t kDoneCounterOffset = 128;
+// the tile schedule's work-item counter and its CTAs-done counter (2 ints)
+constexpr size_t kTileCounterOffset = 192;
 
 struct DeviceInfo {
     int device = -1;

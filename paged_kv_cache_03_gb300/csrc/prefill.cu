@@ -7,7 +7,10 @@
 // sum -> P.V), whole K/V tiles past the causal frontier skipped, and the
 // normalised bf16 output written once.
 //
-// How it is laid out on GB300 (one CTA per pair of 128-row query tiles):
+// How it is laid out on GB300 (a persistent CTA per SM, each claiming work
+// items = pairs of 128-row query tiles from a counter, heaviest first; one
+// item's query load and first K/V tiles overlap the previous item's last
+// products and epilogue):
 //   * The 128 rows of a tile are Lt = 128/G consecutive positions l of all G
 //     query heads that share one kv head (GQA packing), so one K/V tile feeds
 //     128 rows and the causal frontier moves by only Lt keys across the tile.
@@ -79,13 +82,17 @@ enum Bar {
     kPFull = 11,  // + tile
     kODone = 13,  // + tile
     kMmaDone = 15,
-    kVTail = 16,  // the V tile that holds rows past the context
-    kNumBars = 18  // (even: what follows stays 16-byte aligned)
+    kVTail = 16,      // the V tile that holds rows past the context
+    kQEmpty = 17,     // the item's Q.K^T products are done with the query tiles
+    kOFree = 18,      // + tile: the item's epilogue has read O
+    kItemFull = 20,   // + slot: a work item is published
+    kItemEmpty = 22,  // + slot: every role has read it
+    kNumBars = 24     // (even: what follows stays 16-byte aligned)
 };
-constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
+constexpr int kOffItems = kOffBar + kNumBars * 8;  // 2 slots x 32 bytes
+constexpr int kOffTmemSlot = kOffItems + 64;
 constexpr int kOffAbort = kOffTmemSlot + 8;
-constexpr int kOffRows = kOffAbort + 8;  // output row (b, h, l) = base + h * sh + l * sl
-constexpr int kSmemUsed = kOffRows + 16;
+constexpr int kSmemUsed = kOffAbort + 8;
 constexpr int kSmemBytes = kSmemUsed + 1024;  // slack to align the base
 
 struct PrefillParams {
@@ -104,17 +111,11 @@ struct PrefillParams {
     const int32_t* cu_q;
     const int* pair_prefix;
     int total_q;
+    int n_items;        // work items (query-tile pairs x kv heads); a ragged batch's come from its plan
+    int* item_counter;  // [next item to claim, CTAs done]: zero between calls
 };
 
 __device__ __forceinline__ float neg_inf() { return __int_as_float(0xff800000); }
-
-// Output rows of one CTA's sequence, in units of D elements: row (b, h, l)
-// is base + h * sh + l * sl ([B, H_q, L, D], or [tokens, H_q, D] from token
-// q0 on).  Kept in shared memory between the set-up and the epilogue.
-struct alignas(16) OutRows {
-    long long base;
-    int sh, sl;
-};
 
 // All 32 lanes wait; the warp agrees on the outcome (a lane that timed out
 // makes the whole warp give up, so warp-collective instructions stay uniform).
@@ -189,9 +190,82 @@ __device__ __forceinline__ void exp_pack(const float (&x)[4][32], float2 c2, flo
     }
 }
 
+// One work item: query-tile pair mp of sequence b under kv head kvh.
+struct Item {
+    int b, kvh, mp, S, Lb, q0, nM, live;
+};
+
+// Work item i, heaviest pairs first (a CTA claims items from a counter, so
+// the heavy ones start early and the light ones fill the gaps at the end).
+template <bool kVarlen>
+__device__ __forceinline__ Item decode_item(const PrefillParams& p, int i, int n_items) {
+    Item it{0, 0, 0, 0, 0, 0, 0, 0};
+    if (i >= n_items) return it;
+    it.live = 1;
+    if constexpr (kVarlen) {
+        const int ip = i / p.H_kv;
+        it.kvh = i % p.H_kv;
+        int lo = 0, hi = p.B - 1;  // the last sequence whose pairs start at or before ip
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (__ldg(p.pair_prefix + mid) <= ip) lo = mid;
+            else hi = mid - 1;
+        }
+        it.b = lo;
+        it.q0 = __ldg(p.cu_q + lo);
+        it.Lb = __ldg(p.cu_q + lo + 1) - it.q0;
+        it.nM = (it.Lb + p.Lt - 1) / p.Lt;
+        it.mp = (it.nM + 1) / 2 - 1 - (ip - __ldg(p.pair_prefix + lo));  // heavy pairs first
+    } else {
+        const int per_m = p.H_kv * p.B;
+        it.mp = p.nPairs - 1 - i / per_m;
+        const int rest = i % per_m;
+        it.b = rest / p.H_kv;
+        it.kvh = rest % p.H_kv;
+        it.Lb = p.L;
+        it.nM = p.nM;
+    }
+    it.S = __ldg(p.ctx + it.b);
+    return it;
+}
+
+// What an item asks of each role: key tiles per query tile (0 for a tile past
+// the sequence's queries or a sequence whose context breaks the contract),
+// the first query position of each tile and the last key its first row sees.
+struct ItemWork {
+    int nk_t[2], lim_min_t[2], l0_t[2], nk, ntiles;
+    bool valid_seq;
+};
+
+__device__ __forceinline__ ItemWork item_work(const PrefillParams& p, const Item& it) {
+    ItemWork w;
+    w.valid_seq = it.S >= 1 && static_cast<long long>(it.S) <= p.max_S &&
+                  !(p.causal && it.S < it.Lb);
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+        const int m = 2 * it.mp + t;
+        w.l0_t[t] = m * p.Lt;
+        const bool exists = m < it.nM && w.valid_seq;
+        const int l_last = min(w.l0_t[t] + p.Lt, it.Lb) - 1;
+        const int lim_max = p.causal ? l_last + it.S - it.Lb : it.S - 1;  // last key any row sees
+        w.lim_min_t[t] = p.causal ? w.l0_t[t] + it.S - it.Lb : it.S - 1;  // last key row l0 sees
+        w.nk_t[t] = exists ? lim_max / BN + 1 : 0;
+    }
+    w.nk = max(w.nk_t[0], w.nk_t[1]);
+    w.ntiles = (2 * it.mp + 1 < it.nM) ? 2 : 1;
+    return w;
+}
+
 // kMask: an explicit additive mask is read; kVarlen: a ragged batch (queries
 // packed by token, per-sequence query counts).  Separate instantiations, so
 // the plain kernel carries none of their code or registers.
+//
+// Persistent: one CTA per SM claims work items (query-tile pairs) from a
+// counter in the workspace until none are left, so one item's set-up, query
+// load and first K/V tiles overlap the previous item's last products and
+// epilogue instead of each CTA paying them alone.  The producer publishes
+// each item through a 2-slot ring in shared memory; every role runs the
+// item's steps with its own running counts of the barriers' phases.
 template <bool kMask, bool kVarlen>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tile_kernel(const __grid_constant__ CUtensorMap tm_q,
@@ -205,96 +279,39 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto bar = [&](int i) { return bar0 + 8u * static_cast<uint32_t>(i); };
     volatile int* const abort_flag = reinterpret_cast<volatile int*>(sbase + kOffAbort);
     uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(sbase + kOffTmemSlot);
-    OutRows* const out_rows = reinterpret_cast<OutRows*>(sbase + kOffRows);
+    int4* const item_slot = reinterpret_cast<int4*>(sbase + kOffItems);  // [2][2]
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-
-    // ---- which tiles ----------------------------------------------------------
-    // (b, kv head, pair mp of 128-row query tiles); Lb query positions of
-    // sequence b, the first at token q0 (ragged batch)
-    int b, kvh, mp, Lb = p.L, q0 = 0, nM = p.nM;
-    if constexpr (kVarlen) {
-        // a page walk over the batch's other sequences may start beside us
-        pdl_launch_dependents();
-        const int i = static_cast<int>(blockIdx.x) / p.H_kv;
-        kvh = static_cast<int>(blockIdx.x) % p.H_kv;
-        if (i >= p.pair_prefix[p.B]) return;  // past the batch's pairs: before any set-up
-        int lo = 0, hi = p.B - 1;  // the last sequence whose pairs start at or before i
-        while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if (p.pair_prefix[mid] <= i) lo = mid;
-            else hi = mid - 1;
-        }
-        b = lo;
-        q0 = p.cu_q[b];
-        Lb = p.cu_q[b + 1] - q0;
-        nM = (Lb + p.Lt - 1) / p.Lt;
-        mp = (nM + 1) / 2 - 1 - (i - p.pair_prefix[b]);  // heavy pairs of a sequence first
-    } else {
-        const int per_m = p.H_kv * p.B;
-        mp = p.nPairs - 1 - static_cast<int>(blockIdx.x) / per_m;  // heavy pairs first
-        const int rest = static_cast<int>(blockIdx.x) % per_m;
-        b = rest / p.H_kv;
-        kvh = rest % p.H_kv;
-    }
-    const int S = p.ctx[b];
-    const bool valid_seq =
-        S >= 1 && static_cast<long long>(S) <= p.max_S && !(p.causal && S < Lb);
-    int nk_t[2], lim_min_t[2], l0_t[2];
-#pragma unroll
-    for (int t = 0; t < 2; ++t) {
-        const int m = 2 * mp + t;
-        l0_t[t] = m * p.Lt;
-        const bool exists = m < nM && valid_seq;
-        const int l_last = min(l0_t[t] + p.Lt, Lb) - 1;
-        const int lim_max = p.causal ? l_last + S - Lb : S - 1;  // last key any row sees
-        lim_min_t[t] = p.causal ? l0_t[t] + S - Lb : S - 1;      // last key row l0 sees
-        nk_t[t] = exists ? lim_max / BN + 1 : 0;
-    }
-    const int nk = max(nk_t[0], nk_t[1]);
-    const int ntiles = (2 * mp + 1 < nM) ? 2 : 1;
-    // The producer's block-table lookup of K/V tile 0 goes out before the
-    // set-up below, so its latency overlaps the set-up instead of delaying
-    // the first copies.
-    int rows_cur[4] = {-1, -1, -1, -1};
-    uint32_t bytes_cur = 0;
-    if (warp == 0 && nk > 0) tile_boxes(p, b, kvh, S, 0, lane, rows_cur, bytes_cur);
+    if constexpr (kVarlen) pdl_launch_dependents();  // a page walk may start beside us
 
     // ---- set-up: barriers, V zeroed, TMEM --------------------------------------
     if (tid == 0) {
         mbar_init(bar(kQFull), 1);
+        mbar_init(bar(kQEmpty), 1);
         for (int s = 0; s < 2; ++s) {
             mbar_init(bar(kKFull + s), 1);
             mbar_init(bar(kKEmpty + s), 1);
             mbar_init(bar(kSFull + s), 1);
             mbar_init(bar(kPFull + s), 4);
             mbar_init(bar(kODone + s), 1);
-        }
-        for (int s = 0; s < 2; ++s) {
+            mbar_init(bar(kOFree + s), 4);
             mbar_init(bar(kVFull + s), 1);
             mbar_init(bar(kVEmpty + s), 1);
+            mbar_init(bar(kItemFull + s), 1);
+            mbar_init(bar(kItemEmpty + s), 9);  // the MMA thread + 8 softmax warps
         }
         mbar_init(bar(kMmaDone), 1);
         mbar_init(bar(kVTail), 1);
         *abort_flag = 0;
-        if constexpr (kVarlen) {
-            out_rows->base = static_cast<long long>(q0) * p.H_q;
-            out_rows->sh = 1;
-            out_rows->sl = p.H_q;
-        } else {
-            out_rows->base = static_cast<long long>(b) * p.H_q * p.L;
-            out_rows->sh = p.L;
-            out_rows->sl = 1;
-        }
         fence_mbar_init();
     }
     // V rows that are never loaded must hold finite values (their weight is
-    // exactly 0, and 0 * NaN would not be).  Only a last key tile that ends
-    // past the context has such rows, and only in a slot no earlier tile of
-    // this CTA filled (tiles 0 and 1); a tile whose last box runs past the
-    // context is zeroed after its copy lands (kVTail).  Rows of a later slot
-    // past the context still hold the finite rows of the tile two before.
-    if (nk <= 2 && S < nk * BN && S % p.box_rows == 0) {
+    // exactly 0, and 0 * NaN would not be).  A key tile that ends past the
+    // context leaves such rows when no box reaches them; later uses of a slot
+    // find the finite rows of an earlier tile there, the first use these
+    // zeros.  (A tile whose last box runs past the context is zeroed after
+    // its copy lands: kVTail.)
+    {
         uint4* v = reinterpret_cast<uint4*>(sbase + kOffV);
         for (int i = tid; i < 2 * kTile / 16; i += kThreads) v[i] = make_uint4(0u, 0u, 0u, 0u);
     }
@@ -307,157 +324,261 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tmem = *tmem_slot;
-    if (!valid_seq && tid == 0) atomicOr(p.flag, PA_FLAG_BAD_CONTEXT);
 
-    if (warp == 0 && nk > 0) {
+    // Item k sits in ring slot k & 1 until every reader has arrived on
+    // kItemEmpty.
+    auto read_item = [&](int k) {
+        const int4 a = item_slot[2 * (k & 1)], c = item_slot[2 * (k & 1) + 1];
+        return Item{a.x, a.y, a.z, a.w, c.x, c.y, c.z, c.w};
+    };
+    auto take_item = [&](int k, Item& it) -> bool {  // a whole warp
+        if (!warp_wait(bar(kItemFull + (k & 1)), (k >> 1) & 1)) return false;
+        it = read_item(k);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(kItemEmpty + (k & 1)));
+        return true;
+    };
+
+    if (warp == 0) {
         // ============================ TMA producer ============================
         const uint64_t pol_q = l2_policy_evict_first();
         const uint64_t pol_kv = l2_policy_evict_last();
+        const int n_items = kVarlen ? __ldg(p.pair_prefix + p.B) * p.H_kv : p.n_items;
         if (lane == 0) {
             tc::prefetch_tensormap(&tm_q);
             tc::prefetch_tensormap(&tm_k);
             tc::prefetch_tensormap(&tm_v);
-            mbar_arrive_expect_tx(bar(kQFull),
-                                  static_cast<uint32_t>(ntiles * p.G * p.Lt * 128 * 2));
-            for (int t = 0; t < ntiles; ++t)
-                for (int g = 0; g < p.G; ++g) {
-                    const uint32_t dst = base + kOffQ + t * kTile + g * p.Lt * 128;
-                    if constexpr (kVarlen) {  // map (D, H_q, tokens): Lt tokens of head kvh*G + g
-                        for (int h = 0; h < 2; ++h)
-                            tc::tma_load_3d(dst + h * kHalf, &tm_q, h * 64, kvh * p.G + g,
-                                            q0 + l0_t[t], bar(kQFull), pol_q);
-                    } else {
-                        const int row = ((b * p.H_q) + kvh * p.G + g) * p.L + l0_t[t];
-                        for (int h = 0; h < 2; ++h)
-                            tc::tma_load_2d(dst + h * kHalf, &tm_q, h * 64, row, bar(kQFull),
-                                            pol_q);
-                    }
-                }
         }
-        __syncwarp();
-        // the K/V tile whose last box runs past the context (its V rows past
-        // the context are zeroed before the MMA may read the tile), or -1
-        const int tail_tile = (S % p.box_rows != 0) ? (S - 1) / BN : -1;
-        int rows_next[4] = {-1, -1, -1, -1};
-        uint32_t bytes_next = 0;
-        int issued = 0;
-        for (int t = 0; t < nk; ++t) {
-            const int s = t & 1;
-            if (t >= 2 && !warp_wait(bar(kKEmpty + s), ((t >> 1) - 1) & 1)) {
+        auto claim = [&]() {
+            return __shfl_sync(0xffffffffu, lane == 0 ? atomicAdd(p.item_counter, 1) : 0, 0);
+        };
+        int idx = claim();
+        int kt = 0;       // K/V tiles issued before this item (ring position)
+        int qn = 0;       // items whose queries were loaded
+        int vtails = 0;   // tail-tile copies (kVTail phases)
+        int kdone = 0, vdone = 0;  // K and V tiles issued in all
+        bool ok = true;
+        for (int k = 0; ok; ++k) {
+            const Item it = decode_item<kVarlen>(p, idx, n_items);
+            const int next = it.live ? claim() : idx;  // the next item's claim goes out early
+            const ItemWork w = item_work(p, it);
+            if (k >= 2 && !warp_wait(bar(kItemEmpty + (k & 1)), ((k >> 1) - 1) & 1)) {
                 if (lane == 0) give_up(p, abort_flag);
                 break;
             }
-            if (aborted(abort_flag)) break;
-            if (lane == 0) mbar_arrive_expect_tx(bar(kKFull + s), bytes_cur);
+            if (lane == 0) {
+                item_slot[2 * (k & 1)] = make_int4(it.b, it.kvh, it.mp, it.S);
+                item_slot[2 * (k & 1) + 1] = make_int4(it.Lb, it.q0, it.nM, it.live);
+                mbar_arrive(bar(kItemFull + (k & 1)));
+            }
             __syncwarp();
-            issue_boxes(&tm_k, base + kOffK + s * kTile, rows_cur, lane, p.box_rows,
-                        bar(kKFull + s), pol_kv);
-            if (t >= 2 && !warp_wait(bar(kVEmpty + s), ((t >> 1) - 1) & 1)) {
+            if (!it.live) break;
+            idx = next;
+            if (!w.valid_seq && lane == 0) atomicOr(p.flag, PA_FLAG_BAD_CONTEXT);
+            if (w.nk == 0) continue;
+            // the query tiles, once the previous item's products have read theirs
+            if (qn > 0 && !warp_wait(bar(kQEmpty), (qn - 1) & 1)) {
                 if (lane == 0) give_up(p, abort_flag);
-                issued = -(t + 1);  // K(t) issued, V(t) not
                 break;
             }
-            const bool vtail = t == tail_tile;
-            const uint32_t vbar = vtail ? bar(kVTail) : bar(kVFull + s);
-            if (lane == 0) mbar_arrive_expect_tx(vbar, bytes_cur);
+            if (lane == 0) {
+                mbar_arrive_expect_tx(bar(kQFull),
+                                      static_cast<uint32_t>(w.ntiles * p.G * p.Lt * 128 * 2));
+                for (int t = 0; t < w.ntiles; ++t)
+                    for (int g = 0; g < p.G; ++g) {
+                        const uint32_t dst = base + kOffQ + t * kTile + g * p.Lt * 128;
+                        if constexpr (kVarlen) {  // map (D, H_q, tokens): Lt tokens of one head
+                            for (int h = 0; h < 2; ++h)
+                                tc::tma_load_3d(dst + h * kHalf, &tm_q, h * 64, it.kvh * p.G + g,
+                                                it.q0 + w.l0_t[t], bar(kQFull), pol_q);
+                        } else {
+                            const int row = ((it.b * p.H_q) + it.kvh * p.G + g) * p.L + w.l0_t[t];
+                            for (int h = 0; h < 2; ++h)
+                                tc::tma_load_2d(dst + h * kHalf, &tm_q, h * 64, row, bar(kQFull),
+                                                pol_q);
+                        }
+                    }
+            }
             __syncwarp();
-            issue_boxes(&tm_v, base + kOffV + s * kTile, rows_cur, lane, p.box_rows, vbar, pol_kv);
-            issued = t + 1;
-            // rows of the next tile, looked up before waiting for a free slot
-            if (t + 1 < nk) tile_boxes(p, b, kvh, S, t + 1, lane, rows_next, bytes_next);
-            if (vtail) {  // the last tile this CTA loads: nothing waits behind it
-                if (!warp_wait(bar(kVTail), 0)) {
+            ++qn;
+            // the K/V tile whose last box runs past the context (its V rows
+            // past the context are zeroed before the MMA may read it), or -1
+            const int tail_tile = (it.S % p.box_rows != 0) ? (it.S - 1) / BN : -1;
+            int rows_cur[4], rows_next[4] = {-1, -1, -1, -1};
+            uint32_t bytes_cur, bytes_next = 0;
+            tile_boxes(p, it.b, it.kvh, it.S, 0, lane, rows_cur, bytes_cur);
+            for (int j = 0; j < w.nk; ++j) {
+                const int gk = kt + j, s = gk & 1;
+                if (gk >= 2 && !warp_wait(bar(kKEmpty + s), ((gk >> 1) - 1) & 1)) {
                     if (lane == 0) give_up(p, abort_flag);
+                    ok = false;
                     break;
                 }
-                for (int r = S - t * BN + lane; r < BN; r += 32) {
-                    uint4* const vrow =
-                        reinterpret_cast<uint4*>(sbase + kOffV + s * kTile + r * 128);
-#pragma unroll
-                    for (int q = 0; q < 8; ++q) {
-                        vrow[q] = make_uint4(0u, 0u, 0u, 0u);
-                        vrow[kHalf / 16 + q] = make_uint4(0u, 0u, 0u, 0u);
-                    }
+                if (aborted(abort_flag)) {
+                    ok = false;
+                    break;
                 }
-                fence_proxy_async_smem();  // the MMA reads them through the async proxy
+                if (lane == 0) mbar_arrive_expect_tx(bar(kKFull + s), bytes_cur);
                 __syncwarp();
-                if (lane == 0) mbar_arrive(bar(kVFull + s));
-            }
+                issue_boxes(&tm_k, base + kOffK + s * kTile, rows_cur, lane, p.box_rows,
+                            bar(kKFull + s), pol_kv);
+                kdone = gk + 1;
+                if (gk >= 2 && !warp_wait(bar(kVEmpty + s), ((gk >> 1) - 1) & 1)) {
+                    if (lane == 0) give_up(p, abort_flag);
+                    ok = false;
+                    break;
+                }
+                const bool vtail = j == tail_tile;
+                const uint32_t vbar = vtail ? bar(kVTail) : bar(kVFull + s);
+                if (lane == 0) mbar_arrive_expect_tx(vbar, bytes_cur);
+                __syncwarp();
+                issue_boxes(&tm_v, base + kOffV + s * kTile, rows_cur, lane, p.box_rows, vbar,
+                            pol_kv);
+                // rows of the next tile, looked up before waiting for a free slot
+                if (j + 1 < w.nk) tile_boxes(p, it.b, it.kvh, it.S, j + 1, lane, rows_next, bytes_next);
+                if (vtail) {  // the item's last tile: nothing of this item waits behind it
+                    if (!warp_wait(bar(kVTail), vtails & 1)) {
+                        if (lane == 0) give_up(p, abort_flag);
+                        ok = false;
+                        break;
+                    }
+                    ++vtails;
+                    for (int r = it.S - j * BN + lane; r < BN; r += 32) {
+                        uint4* const vrow =
+                            reinterpret_cast<uint4*>(sbase + kOffV + s * kTile + r * 128);
 #pragma unroll
-            for (int w = 0; w < 4; ++w) rows_cur[w] = rows_next[w];
-            bytes_cur = bytes_next;
+                        for (int q = 0; q < 8; ++q) {
+                            vrow[q] = make_uint4(0u, 0u, 0u, 0u);
+                            vrow[kHalf / 16 + q] = make_uint4(0u, 0u, 0u, 0u);
+                        }
+                    }
+                    fence_proxy_async_smem();  // the MMA reads them through the async proxy
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar(kVFull + s));
+                }
+                vdone = gk + 1;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) rows_cur[q] = rows_next[q];
+                bytes_cur = bytes_next;
+            }
+            kt += w.nk;
         }
         // let every copy into this CTA's shared memory land before leaving
-        if (!mbar_wait(bar(kQFull), 0)) give_up(p, abort_flag);
-        const int kdone = issued < 0 ? -issued : issued, vdone = issued < 0 ? -issued - 1 : issued;
-        for (int t = max(0, kdone - 2); t < kdone; ++t)
-            if (!mbar_wait(bar(kKFull + (t & 1)), (t >> 1) & 1)) give_up(p, abort_flag);
-        for (int t = max(0, vdone - 2); t < vdone; ++t)
-            if (!(t == tail_tile ? mbar_wait(bar(kVTail), 0)
-                                 : mbar_wait(bar(kVFull + (t & 1)), (t >> 1) & 1)))
-                give_up(p, abort_flag);
-    } else if (warp == 1 && nk > 0) {
+        if (qn > 0 && !mbar_wait(bar(kQFull), (qn - 1) & 1)) give_up(p, abort_flag);
+        for (int g = max(0, kdone - 2); g < kdone; ++g)
+            if (!mbar_wait(bar(kKFull + (g & 1)), (g >> 1) & 1)) give_up(p, abort_flag);
+        for (int g = max(0, vdone - 2); g < vdone; ++g)
+            if (!mbar_wait(bar(kVFull + (g & 1)), (g >> 1) & 1)) give_up(p, abort_flag);
+        // the last CTA to stop claiming resets the counters for the next call
+        if (lane == 0) {
+            __threadfence();
+            if (atomicAdd(p.item_counter + 1, 1) == static_cast<int>(gridDim.x) - 1) {
+                atomicExch(p.item_counter, 0);
+                atomicExch(p.item_counter + 1, 0);
+                __threadfence();
+            }
+        }
+    } else if (warp == 1) {
         // ============================ MMA issuer =============================
         if (lane == 0) {
             constexpr uint32_t idS = tc::idesc_bf16(BM, BN, 0, 0);  // Q, K both K-major
             constexpr uint32_t idO = tc::idesc_bf16(BM, kD, 0, 1);  // P K-major, V MN-major
-            auto qk = [&](int t, int j) {
-                const uint32_t kaddr = base + kOffK + (j & 1) * kTile;
-                const uint32_t qaddr = base + kOffQ + t * kTile;
+            // Operand descriptors of every tile base, formed once; a k-step's
+            // descriptor is the base one advanced by its byte offset.
+            const uint64_t dQ0 = tc::smem_desc_sw128(base + kOffQ, 16, 1024);
+            const uint64_t dQ1 = tc::smem_desc_sw128(base + kOffQ + kTile, 16, 1024);
+            const uint64_t dK0 = tc::smem_desc_sw128(base + kOffK, 16, 1024);
+            const uint64_t dK1 = tc::smem_desc_sw128(base + kOffK + kTile, 16, 1024);
+            const uint64_t dP = tc::smem_desc_sw128(base + kOffP, 16, 1024);
+            const uint64_t dV0 = tc::smem_desc_sw128(base + kOffV, kHalf, 1024);
+            const uint64_t dV1 = tc::smem_desc_sw128(base + kOffV + kTile, kHalf, 1024);
+            auto qk = [&](int t, int gk) {
+                const uint64_t dq = t ? dQ1 : dQ0, dk = (gk & 1) ? dK1 : dK0;
+                const uint32_t d = tmem + col_s(t);
+                tc::mma_bf16_c<0>(d, dq, dk, idS);
 #pragma unroll
-                for (int kk = 0; kk < kD / 16; ++kk) {
+                for (int kk = 1; kk < kD / 16; ++kk) {
                     const uint32_t koff = (kk >> 2) * kHalf + (kk & 3) * 32;
-                    tc::mma_bf16(tmem + col_s(t), tc::smem_desc_sw128(qaddr + koff, 16, 1024),
-                                 tc::smem_desc_sw128(kaddr + koff, 16, 1024), idS, kk > 0);
+                    tc::mma_bf16_c<1>(d, tc::desc_advance(dq, koff), tc::desc_advance(dk, koff), idS);
                 }
                 tc::commit(bar(kSFull + t));
             };
-            auto pv = [&](int t, int j) {
-                const uint32_t paddr = base + kOffP;
-                const uint32_t vaddr = base + kOffV + (j & 1) * kTile;
+            auto pv = [&](int t, int j, int gk) {
+                const uint64_t dv = (gk & 1) ? dV1 : dV0;
+                const uint32_t d = tmem + col_o(t);
+                if (j > 0) tc::mma_bf16_c<1>(d, dP, dv, idO);
+                else tc::mma_bf16_c<0>(d, dP, dv, idO);
 #pragma unroll
-                for (int kk = 0; kk < BN / 16; ++kk) {
+                for (int kk = 1; kk < BN / 16; ++kk) {
                     const uint32_t poff = (kk >> 2) * kHalf + (kk & 3) * 32;
-                    tc::mma_bf16(tmem + col_o(t), tc::smem_desc_sw128(paddr + poff, 16, 1024),
-                                 tc::smem_desc_sw128(vaddr + kk * 16 * 128, kHalf, 1024), idO,
-                                 (j > 0 || kk > 0) ? 1u : 0u);
+                    tc::mma_bf16_c<1>(d, tc::desc_advance(dP, poff),
+                                      tc::desc_advance(dv, kk * 16 * 128), idO);
                 }
                 tc::commit(bar(kODone + t));
             };
-            bool ok = mbar_wait(bar(kQFull), 0) && mbar_wait(bar(kKFull), 0);
-            if (ok) {
-                tc::fence_after_sync();
-                if (nk_t[0] > 0) qk(0, 0);
-                if (nk_t[1] > 0) qk(1, 0);
-                tc::commit(bar(kKEmpty));
-            }
-            for (int j = 0; ok && j < nk; ++j) {
-                ok = mbar_wait(bar(kVFull + (j & 1)), (j >> 1) & 1);
+            int kt = 0, qn = 0;
+            int pc[2] = {0, 0};  // P fills consumed per tile (kPFull phases)
+            int oe[2] = {0, 0};  // epilogues of each tile so far (kOFree phases)
+            bool ok = true;
+            Item it;
+            for (int k = 0; ok; ++k) {
+                ok = mbar_wait(bar(kItemFull + (k & 1)), (k >> 1) & 1);
+                if (!ok) break;
+                it = read_item(k);
+                mbar_arrive(bar(kItemEmpty + (k & 1)));
+                if (!it.live) break;
+                const ItemWork w = item_work(p, it);
+                if (w.nk == 0) continue;
+                const int* nk_t = w.nk_t;
+                const int nk = w.nk;
+                ok = mbar_wait(bar(kQFull), qn & 1) && mbar_wait(bar(kKFull + (kt & 1)), (kt >> 1) & 1);
                 if (!ok || *abort_flag) break;
-                const bool more = j + 1 < nk;
-                if (j < nk_t[0]) {
-                    ok = mbar_wait(bar(kPFull), j & 1);
+                tc::fence_after_sync();
+                if (nk_t[0] > 0) qk(0, kt);
+                if (nk_t[1] > 0) qk(1, kt);
+                tc::commit(bar(kKEmpty + (kt & 1)));
+                if (nk == 1) tc::commit(bar(kQEmpty));  // all of the item's Q.K^T issued
+                for (int j = 0; ok && j < nk; ++j) {
+                    const int gk = kt + j;
+                    ok = mbar_wait(bar(kVFull + (gk & 1)), (gk >> 1) & 1);
                     if (!ok || *abort_flag) break;
-                    tc::fence_after_sync();
-                    pv(0, j);
+                    const bool more = j + 1 < nk;
+                    if (j < nk_t[0]) {
+                        ok = mbar_wait(bar(kPFull), pc[0] & 1);
+                        // O_A is overwritten by this item's first P.V: the
+                        // previous item's epilogue must have read it
+                        if (ok && j == 0 && oe[0] > 0) ok = mbar_wait(bar(kOFree), (oe[0] - 1) & 1);
+                        if (!ok || *abort_flag) break;
+                        ++pc[0];
+                        tc::fence_after_sync();
+                        pv(0, j, gk);
+                    }
+                    if (more) {
+                        ok = mbar_wait(bar(kKFull + ((gk + 1) & 1)), ((gk + 1) >> 1) & 1);
+                        if (!ok || *abort_flag) break;
+                        tc::fence_after_sync();
+                        if (j + 1 < nk_t[0]) qk(0, gk + 1);
+                    }
+                    if (j < nk_t[1]) {
+                        ok = mbar_wait(bar(kPFull + 1), pc[1] & 1);
+                        if (ok && j == 0 && oe[1] > 0)
+                            ok = mbar_wait(bar(kOFree + 1), (oe[1] - 1) & 1);
+                        if (!ok || *abort_flag) break;
+                        ++pc[1];
+                        tc::fence_after_sync();
+                        pv(1, j, gk);
+                    }
+                    tc::commit(bar(kVEmpty + (gk & 1)));
+                    if (more) {
+                        if (j + 1 < nk_t[1]) qk(1, gk + 1);
+                        tc::commit(bar(kKEmpty + ((gk + 1) & 1)));
+                        if (j + 2 == nk) tc::commit(bar(kQEmpty));  // the item's last Q.K^T
+                    }
                 }
-                if (more) {
-                    ok = mbar_wait(bar(kKFull + ((j + 1) & 1)), ((j + 1) >> 1) & 1);
-                    if (!ok || *abort_flag) break;
-                    tc::fence_after_sync();
-                    if (j + 1 < nk_t[0]) qk(0, j + 1);
-                }
-                if (j < nk_t[1]) {
-                    ok = mbar_wait(bar(kPFull + 1), j & 1);
-                    if (!ok || *abort_flag) break;
-                    tc::fence_after_sync();
-                    pv(1, j);
-                }
-                tc::commit(bar(kVEmpty + (j & 1)));
-                if (more) {
-                    if (j + 1 < nk_t[1]) qk(1, j + 1);
-                    tc::commit(bar(kKEmpty + ((j + 1) & 1)));
-                }
+                if (nk_t[0] > 0) ++oe[0];
+                if (nk_t[1] > 0) ++oe[1];
+                kt += nk;
+                ++qn;
             }
             if (!ok) give_up(p, abort_flag);
             // nothing of ours may still be running when TMEM is freed
@@ -471,174 +592,204 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int q4 = warp & 3;            // TMEM lane quarter of this warp
         const int r = q4 * 32 + lane;       // query row of this thread
         const uint32_t trow = tmem + (static_cast<uint32_t>(q4 * 32) << 16);
-        const int g = r / p.Lt, l = l0_t[t] + (r - g * p.Lt);
-        const bool row_valid = t < ntiles && g < p.G && l < Lb;
-        const int h = kvh * p.G + g;
-        const int lim = min(p.causal ? l + S - Lb : S - 1, S - 1);
-        const int nkt = nk_t[t];
         const float c = p.scale_log2;
         // with an explicit mask the scores are taken to log2 units (and the
         // mask added) right after the load, so the rest scales by 1
         const float cs = kMask ? 1.f : c;
-        const float* const mask_row =
-            kMask && row_valid
-                ? p.mask + ((static_cast<long long>(b) * p.H_q + h) * p.L + l) * p.mask_S
-                : nullptr;
-        // the lines holding this row's visible mask entries of key tile jj go
-        // to L2 ahead of use: keys [jj * BN, min(jj * BN + BN, lim + 1)), all
-        // inside the row (lim < S <= mask_S)
-        auto prefetch_mask = [&](int jj) {
-            if (!kMask || !mask_row || jj >= nkt) return;
-            const int k0 = jj * BN;
-            if (k0 > lim) return;
-            const int k1 = min(k0 + BN, lim + 1) - 1;  // last visible key of the tile
-#pragma unroll
-            for (int e = 0; e < 4; ++e) prefetch_l2(mask_row + min(k0 + 32 * e, k1));
-            prefetch_l2(mask_row + k1);
-        };
-        prefetch_mask(0);
-        float mrow = neg_inf();
-        float2 lsum2 = make_float2(0.f, 0.f);
+        int sc = 0;               // S fills of this tile consumed (kSFull phases)
+        int pvA = 0, pvB = 0;     // P.V products of tiles A and B in earlier items (kODone phases)
         bool ok = true;
-        for (int j = 0; j < nkt; ++j) {
-            prefetch_mask(j + 1);
-            ok = warp_wait(bar(kSFull + t), j & 1);
-            if (!ok || aborted(abort_flag)) break;
-            tc::fence_after_sync();
-            float x[4][32];
+        Item it;
+        for (int k = 0; ok; ++k) {
+            ok = take_item(k, it);
+            if (!ok || !it.live) break;
+            const ItemWork w = item_work(p, it);
+            const int nkA = w.nk_t[0], nkB = w.nk_t[1];
+            const int nkt = t == 0 ? nkA : nkB;
+            const int pv_own = t == 0 ? pvA : pvB;
+            const int lim_min = t == 0 ? w.lim_min_t[0] : w.lim_min_t[1];
+            const int g = r / p.Lt, l = (t == 0 ? w.l0_t[0] : w.l0_t[1]) + (r - g * p.Lt);
+            const bool row_valid = t < w.ntiles && g < p.G && l < it.Lb;
+            const int h = it.kvh * p.G + g;
+            const int S = it.S, Lb = it.Lb;
+            const int lim = min(p.causal ? l + S - Lb : S - 1, S - 1);
+            // output row (b, h, l): [B, H_q, L, D], or [tokens, H_q, D] from token q0
+            const long long orow_idx =
+                kVarlen ? (static_cast<long long>(it.q0 + l) * p.H_q + h)
+                        : ((static_cast<long long>(it.b) * p.H_q + h) * p.L + l);
+            const float* const mask_row =
+                kMask && row_valid
+                    ? p.mask + ((static_cast<long long>(it.b) * p.H_q + h) * p.L + l) * p.mask_S
+                    : nullptr;
+            // the lines holding this row's visible mask entries of key tile jj go
+            // to L2 ahead of use: keys [jj * BN, min(jj * BN + BN, lim + 1)), all
+            // inside the row (lim < S <= mask_S)
+            auto prefetch_mask = [&](int jj) {
+                if (!kMask || !mask_row || jj >= nkt) return;
+                const int k0 = jj * BN;
+                if (k0 > lim) return;
+                const int k1 = min(k0 + BN, lim + 1) - 1;  // last visible key of the tile
 #pragma unroll
-            for (int cc = 0; cc < 4; ++cc) tc::ld32(trow + col_s(t) + cc * 32, x[cc]);
-            tc::wait_ld();
-            if constexpr (kMask) {  // s * scale * log2 e + mask * log2 e
-                // only the words holding a visible key (k0 + 4q <= lim < mask_S)
-                const int k0 = j * BN;
-#pragma unroll
-                for (int q = 0; q < 32; ++q) {
-                    float4 mv = make_float4(0.f, 0.f, 0.f, 0.f);
-                    if (mask_row && k0 + 4 * q <= lim)
-                        mv = __ldg(reinterpret_cast<const float4*>(mask_row + k0) + q);
-                    const int cc = q >> 3, e = (q & 7) * 4;
-                    x[cc][e + 0] = fmaf(x[cc][e + 0], c, mv.x * 1.4426950408889634f);
-                    x[cc][e + 1] = fmaf(x[cc][e + 1], c, mv.y * 1.4426950408889634f);
-                    x[cc][e + 2] = fmaf(x[cc][e + 2], c, mv.z * 1.4426950408889634f);
-                    x[cc][e + 3] = fmaf(x[cc][e + 3], c, mv.w * 1.4426950408889634f);
-                }
+                for (int e = 0; e < 4; ++e) prefetch_l2(mask_row + min(k0 + 32 * e, k1));
+                prefetch_l2(mask_row + k1);
+            };
+            prefetch_mask(0);
+            // the shared P buffer: the previous item's last products must be done
+            // before tile A's first P of this item lands there (tile B's first P
+            // follows tile A's first product, which follows these)
+            if (t == 0 && nkt > 0) {
+                if (pvA > 0) ok = warp_wait(bar(kODone), (pvA - 1) & 1);
+                if (ok && pvB > 0) ok = warp_wait(bar(kODone + 1), (pvB - 1) & 1);
+                if (!ok) break;
             }
-            // causal / length mask (frontier tiles only), row max of raw scores
-            const bool masking = j * BN + BN - 1 > lim_min_t[t];  // uniform over the CTA
-            if (masking) {
-                const int cmax = lim - j * BN;  // columns <= cmax are visible
-#pragma unroll
-                for (int cc = 0; cc < 4; ++cc)
-#pragma unroll
-                    for (int e = 0; e < 32; ++e)
-                        if (cc * 32 + e > cmax) x[cc][e] = neg_inf();
-            }
-            float mq[4];
-#pragma unroll
-            for (int cc = 0; cc < 4; ++cc) {
-                mq[cc] = x[cc][0];
-#pragma unroll
-                for (int e = 1; e < 31; e += 2) mq[cc] = fmax3(mq[cc], x[cc][e], x[cc][e + 1]);
-                mq[cc] = fmaxf(mq[cc], x[cc][31]);
-            }
-            float mt = fmax3(mq[0], mq[1], fmaxf(mq[2], mq[3]));
-            mt *= cs;
-            const bool grow = mt > mrow + kLazyRescaleLog2;
-            const bool any_grow = __any_sync(0xffffffffu, grow);
-            const float mn = grow ? mt : mrow;
-            const float alpha = grow ? fast_exp2(mrow - mn) : 1.f;  // 2^-inf = 0 at start
-            mrow = mn;
-            // P = 2^(s*c - m) packed to bf16 pairs in registers, before any wait
-            const float mu = (mrow == neg_inf()) ? 0.f : mrow;
-            const float2 c2 = make_float2(cs, cs), nm2 = make_float2(-mu, -mu);
-            float2 ts = make_float2(0.f, 0.f);
-            uint32_t pw[64];
-            exp_pack(x, c2, nm2, pw, ts);
-            lsum2.x = lsum2.x * alpha + ts.x;
-            lsum2.y = lsum2.y * alpha + ts.y;
-            // O is rescaled once this tile's previous P.V is done
-            if (any_grow && j > 0) {
-                ok = warp_wait(bar(kODone + t), (j - 1) & 1);
+            float mrow = neg_inf();
+            float2 lsum2 = make_float2(0.f, 0.f);
+            for (int j = 0; j < nkt; ++j) {
+                prefetch_mask(j + 1);
+                ok = warp_wait(bar(kSFull + t), (sc + j) & 1);
                 if (!ok || aborted(abort_flag)) break;
                 tc::fence_after_sync();
+                float x[4][32];
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc) tc::ld32(trow + col_s(t) + cc * 32, x[cc]);
+                tc::wait_ld();
+                if constexpr (kMask) {  // s * scale * log2 e + mask * log2 e
+                    // only the words holding a visible key (k0 + 4q <= lim < mask_S)
+                    const int k0 = j * BN;
+#pragma unroll
+                    for (int q = 0; q < 32; ++q) {
+                        float4 mv = make_float4(0.f, 0.f, 0.f, 0.f);
+                        if (mask_row && k0 + 4 * q <= lim)
+                            mv = __ldg(reinterpret_cast<const float4*>(mask_row + k0) + q);
+                        const int cc = q >> 3, e = (q & 7) * 4;
+                        x[cc][e + 0] = fmaf(x[cc][e + 0], c, mv.x * 1.4426950408889634f);
+                        x[cc][e + 1] = fmaf(x[cc][e + 1], c, mv.y * 1.4426950408889634f);
+                        x[cc][e + 2] = fmaf(x[cc][e + 2], c, mv.z * 1.4426950408889634f);
+                        x[cc][e + 3] = fmaf(x[cc][e + 3], c, mv.w * 1.4426950408889634f);
+                    }
+                }
+                // causal / length mask (frontier tiles only), row max of raw scores
+                const bool masking = j * BN + BN - 1 > lim_min;  // uniform over the CTA
+                if (masking) {
+                    const int cmax = lim - j * BN;  // columns <= cmax are visible
+#pragma unroll
+                    for (int cc = 0; cc < 4; ++cc)
+#pragma unroll
+                        for (int e = 0; e < 32; ++e)
+                            if (cc * 32 + e > cmax) x[cc][e] = neg_inf();
+                }
+                float mq[4];
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc) {
+                    mq[cc] = x[cc][0];
+#pragma unroll
+                    for (int e = 1; e < 31; e += 2) mq[cc] = fmax3(mq[cc], x[cc][e], x[cc][e + 1]);
+                    mq[cc] = fmaxf(mq[cc], x[cc][31]);
+                }
+                float mt = fmax3(mq[0], mq[1], fmaxf(mq[2], mq[3]));
+                mt *= cs;
+                const bool grow = mt > mrow + kLazyRescaleLog2;
+                const bool any_grow = __any_sync(0xffffffffu, grow);
+                const float mn = grow ? mt : mrow;
+                const float alpha = grow ? fast_exp2(mrow - mn) : 1.f;  // 2^-inf = 0 at start
+                mrow = mn;
+                // P = 2^(s*c - m) packed to bf16 pairs in registers, before any wait
+                const float mu = (mrow == neg_inf()) ? 0.f : mrow;
+                const float2 c2 = make_float2(cs, cs), nm2 = make_float2(-mu, -mu);
+                float2 ts = make_float2(0.f, 0.f);
+                uint32_t pw[64];
+                exp_pack(x, c2, nm2, pw, ts);
+                lsum2.x = lsum2.x * alpha + ts.x;
+                lsum2.y = lsum2.y * alpha + ts.y;
+                // O is rescaled once this tile's previous P.V is done
+                if (any_grow && j > 0) {
+                    ok = warp_wait(bar(kODone + t), (pv_own + j - 1) & 1);
+                    if (!ok || aborted(abort_flag)) break;
+                    tc::fence_after_sync();
+#pragma unroll 1
+                    for (int cc = 0; cc < 4; ++cc) {
+                        float o[32];
+                        tc::ld32(trow + col_o(t) + cc * 32, o);
+                        tc::wait_ld();
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) o[e] *= alpha;
+                        tc::st32(trow + col_o(t) + cc * 32, o);
+                    }
+                    tc::wait_st();
+                }
+                // the shared P buffer is free once the P.V that read it last is done:
+                // A(j) follows B(j-1), B(j) follows A(j) (or its own tile's previous
+                // P.V when the other tile has none there)
+                {
+                    int wt = -1, wj = -1;
+                    if (t == 0) {
+                        if (j - 1 >= 0 && j - 1 < nkB) wt = 1, wj = j - 1;
+                        else if (j > 0) wt = 0, wj = j - 1;
+                    } else {
+                        if (j < nkA) wt = 0, wj = j;
+                        else if (j > 0) wt = 1, wj = j - 1;
+                    }
+                    if (wt >= 0) {
+                        ok = warp_wait(bar(kODone + wt), ((wt == 0 ? pvA : pvB) + wj) & 1);
+                        if (!ok || aborted(abort_flag)) break;
+                    }
+                }
+                tc::fence_after_sync();
+                uint8_t* const prow = sbase + kOffP + r * 128;
+#pragma unroll
+                for (int q = 0; q < 16; ++q) {  // 8 keys per 16-byte chunk
+                    const uint4 wv = make_uint4(pw[4 * q], pw[4 * q + 1], pw[4 * q + 2], pw[4 * q + 3]);
+                    const int half = q >> 3, cq = q & 7;
+                    *reinterpret_cast<uint4*>(prow + half * kHalf + ((cq ^ (r & 7)) << 4)) = wv;
+                }
+                fence_proxy_async_smem();
+                tc::fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(kPFull + t));
+            }
+            if (!ok) break;
+            const float lsum = lsum2.x + lsum2.y;
+            if (nkt > 0) {
+                if (!warp_wait(bar(kODone + t), (pv_own + nkt - 1) & 1)) {
+                    ok = false;
+                    break;
+                }
+                tc::fence_after_sync();
+                const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+                uint16_t* const orow = static_cast<uint16_t*>(p.out) + orow_idx * kD;
 #pragma unroll 1
                 for (int cc = 0; cc < 4; ++cc) {
                     float o[32];
                     tc::ld32(trow + col_o(t) + cc * 32, o);
                     tc::wait_ld();
+                    if (row_valid) {
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) o[e] *= alpha;
-                    tc::st32(trow + col_o(t) + cc * 32, o);
-                }
-                tc::wait_st();
-            }
-            // the shared P buffer is free once the P.V that read it last is done:
-            // A(j) follows B(j-1), B(j) follows A(j) (or its own tile's previous
-            // P.V when the other tile has none there)
-            {
-                int wt = -1, wj = -1;
-                if (t == 0) {
-                    if (j - 1 >= 0 && j - 1 < nk_t[1]) wt = 1, wj = j - 1;
-                    else if (j > 0) wt = 0, wj = j - 1;
-                } else {
-                    if (j < nk_t[0]) wt = 0, wj = j;
-                    else if (j > 0) wt = 1, wj = j - 1;
-                }
-                if (wt >= 0) {
-                    ok = warp_wait(bar(kODone + wt), wj & 1);
-                    if (!ok || aborted(abort_flag)) break;
-                }
-            }
-            tc::fence_after_sync();
-            uint8_t* const prow = sbase + kOffP + r * 128;
-#pragma unroll
-            for (int q = 0; q < 16; ++q) {  // 8 keys per 16-byte chunk
-                const uint4 w = make_uint4(pw[4 * q], pw[4 * q + 1], pw[4 * q + 2], pw[4 * q + 3]);
-                const int half = q >> 3, cq = q & 7;
-                *reinterpret_cast<uint4*>(prow + half * kHalf + ((cq ^ (r & 7)) << 4)) = w;
-            }
-            fence_proxy_async_smem();
-            tc::fence_before_sync();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar(kPFull + t));
-        }
-        const float lsum = lsum2.x + lsum2.y;
-        if (!ok) {
-            if (lane == 0) give_up(p, abort_flag);
-        } else if (nkt > 0 && warp_wait(bar(kODone + t), (nkt - 1) & 1)) {
-            tc::fence_after_sync();
-            const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
-            uint16_t* const orow = static_cast<uint16_t*>(p.out) +
-                                   (out_rows->base + static_cast<long long>(h) * out_rows->sh +
-                                    static_cast<long long>(l) * out_rows->sl) * kD;
-#pragma unroll 1
-            for (int cc = 0; cc < 4; ++cc) {
-                float o[32];
-                tc::ld32(trow + col_o(t) + cc * 32, o);
-                tc::wait_ld();
-                if (row_valid) {
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const uint4 w = make_uint4(
-                            pack_bf16x2(o[q * 8 + 0] * inv, o[q * 8 + 1] * inv),
-                            pack_bf16x2(o[q * 8 + 2] * inv, o[q * 8 + 3] * inv),
-                            pack_bf16x2(o[q * 8 + 4] * inv, o[q * 8 + 5] * inv),
-                            pack_bf16x2(o[q * 8 + 6] * inv, o[q * 8 + 7] * inv));
-                        *reinterpret_cast<uint4*>(orow + cc * 32 + q * 8) = w;
+                        for (int q = 0; q < 4; ++q) {
+                            const uint4 wv = make_uint4(
+                                pack_bf16x2(o[q * 8 + 0] * inv, o[q * 8 + 1] * inv),
+                                pack_bf16x2(o[q * 8 + 2] * inv, o[q * 8 + 3] * inv),
+                                pack_bf16x2(o[q * 8 + 4] * inv, o[q * 8 + 5] * inv),
+                                pack_bf16x2(o[q * 8 + 6] * inv, o[q * 8 + 7] * inv));
+                            *reinterpret_cast<uint4*>(orow + cc * 32 + q * 8) = wv;
+                        }
                     }
                 }
+                // O of this tile is read: the next item's first P.V may overwrite it
+                tc::fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(kOFree + t));
             }
-        } else if (nkt > 0) {
-            if (lane == 0) give_up(p, abort_flag);
+            if (!w.valid_seq && row_valid) {
+                uint4* orow = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) + orow_idx * kD);
+                for (int q = 0; q < kD / 8; ++q) orow[q] = make_uint4(0u, 0u, 0u, 0u);
+            }
+            sc += nkt;
+            pvA += nkA;
+            pvB += nkB;
         }
-        if (!valid_seq && row_valid) {
-            uint4* orow = reinterpret_cast<uint4*>(
-                static_cast<uint16_t*>(p.out) +
-                (out_rows->base + static_cast<long long>(h) * out_rows->sh +
-                 static_cast<long long>(l) * out_rows->sl) * kD);
-            for (int q = 0; q < kD / 8; ++q) orow[q] = make_uint4(0u, 0u, 0u, 0u);
-        }
+        if (!ok && lane == 0) give_up(p, abort_flag);
+    } else {
+        // warps 2 and 3: readers of no item; they only keep the ring moving
     }
 
     // ---- tear-down: free TMEM once every role is done -----------------------
@@ -836,6 +987,7 @@ pa_status prefill_launch(const Call& c) {
     p.cu_q = c.cu_q;
     p.total_q = c.total_q;
     p.pair_prefix = nullptr;
+    p.item_counter = reinterpret_cast<int*>(static_cast<uint8_t*>(c.ws) + kTileCounterOffset);
     long long pairs = static_cast<long long>(p.nPairs) * sh.B;
     if (c.cu_q) {
         // the pairs of all sequences are at most ceil(L_b / (2 Lt)) each, so at
@@ -850,7 +1002,10 @@ pa_status prefill_launch(const Call& c) {
         if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
         if (pairs == 0) return PA_OK;
     }
-    const unsigned grid = static_cast<unsigned>(pairs * sh.H_kv);
+    // persistent: one CTA per SM (or per item, when there are fewer)
+    const long long items = pairs * sh.H_kv;
+    p.n_items = static_cast<int>(items);
+    const unsigned grid = static_cast<unsigned>(std::min<long long>(items, c.dev.sm_count));
     if (c.ev_before && cudaEventRecord(c.ev_before, c.stream) != cudaSuccess) return PA_ERR_CUDA;
     if (c.cu_q)  // (a ragged batch takes no explicit mask)
         prefill_tile_kernel<false, true><<<grid, kThreads, kSmemBytes, c.stream>>>(tq, tk, tv, p);

@@ -41,6 +41,25 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint6
         : "memory");
 }
 
+// The same with the accumulate flag fixed at compile time (1: D += A * B;
+// 0: D = A * B), so no predicate is formed at run time.
+template <int kAccumulate>
+__device__ __forceinline__ void mma_bf16_c(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                           uint32_t idesc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "n"(kAccumulate)
+        : "memory");
+}
+
+// Descriptor of the operand `off` bytes further on: the start address sits in
+// the low 14 bits as address / 16, and shared-memory addresses stay below
+// 256 KB, so adding off / 16 never carries out of the field.
+__device__ __forceinline__ uint64_t desc_advance(uint64_t desc, uint32_t off) {
+    return desc + static_cast<uint64_t>(off >> 4);
+}
+
 // Arrive once on `bar` when every tcgen05 op this thread issued so far is done.
 __device__ __forceinline__ void commit(uint32_t bar) {
     asm volatile(

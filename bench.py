@@ -337,6 +337,18 @@ def aggregate(bytes_per_step: float, steps: int, local_ms_total: float, world: i
 # ---------------------------------------------------------------------------
 # CPU oracle timing (cpu_baseline leg and --impl reference)
 # ---------------------------------------------------------------------------
+def host_us_per_call(call, n=200):
+    """Median CPU time, in microseconds, of enqueueing one call (host-side
+    argument checks, tensor-map encoding, kernel launches), measured call by
+    call without synchronising; the caller synchronises afterwards."""
+    ts = []
+    for _ in range(n):
+        t0 = time.perf_counter()
+        call()
+        ts.append(time.perf_counter() - t0)
+    return round(float(np.median(ts)) * 1e6, 2)
+
+
 def sub_batch(inp, n):
     """The first n sequences of a workload (same pool)."""
     return synth.PagedInputs(np.ascontiguousarray(inp.query[:n]), inp.key_pages,
@@ -415,7 +427,7 @@ def headline(args) -> bool:
 
 PREFILL_KEYS = ("metric", "value", "unit", "ms_per_step", "steps", "warmup", "dtype",
                 "clocks", "e2e", "gpu_launches", "roofline", "cpu_baseline", "step_ms_median",
-                "wall_s_timed_region")
+                "wall_s_timed_region", "host_us_per_call")
 
 
 def prefill_record(sub) -> dict:
@@ -524,6 +536,8 @@ def measure(args, device, world, rank):
     st, flag = B.pa_check_device_flag(ws, stream=stream)
     if flag:
         raise RuntimeError(f"device flag {flag:#x} after timed steps")
+    host_us = host_us_per_call(call)
+    torch.cuda.synchronize(device)
 
     value, t_max = aggregate(bytes_step, K, float(step_ms.sum()), world, device)
     ms_per_step = t_max / K
@@ -632,6 +646,7 @@ def measure(args, device, world, rank):
                   "with events around the dominant kernel, same timed region",
         "step_ms_median": round(float(np.median(step_ms)), 5),
         "wall_s_timed_region": round(wall, 3),
+        "host_us_per_call": host_us,
     }
     if rank == 0 and not args.no_cpu_baseline:
         unit_fn = (lambda s: algorithmic_flops(s) / 1e12) if bound == "tensor" else (
@@ -732,6 +747,8 @@ def run_mixed(args):
     _, flag = B.pa_check_device_flag(ws, stream=stream)
     if flag:
         raise RuntimeError(f"device flag {flag:#x} after timed steps")
+    host_us = host_us_per_call(call)
+    torch.cuda.synchronize(device)
     value, t_max = aggregate(bytes_step, K, float(step_ms.sum()), world, device)
     peaks, peaks_src = load_peaks()
     achieved = bytes_step / (float(step_ms.mean()) * 1e-3) / 1e9
@@ -796,6 +813,7 @@ def run_mixed(args):
                    "algorithmic_bytes_per_step": bytes_step,
                    "algorithmic_flops_per_step": flops_step},
         "clocks": clocks, "e2e": e2e, "gpu_launches": K * launches, "roofline": roofline,
+        "host_us_per_call": host_us,
     }
     if rank == 0 and not args.no_cpu_baseline:
         import oracle
@@ -895,6 +913,8 @@ def run_append(args):
     _, flag = B.pa_check_device_flag(ws, stream=stream)
     if flag:
         raise RuntimeError(f"device flag {flag:#x} after timed steps")
+    host_us = host_us_per_call(call)
+    torch.cuda.synchronize(device)
     value, t_max = aggregate(bytes_step, K, float(step_ms.sum()), world, device)
     peaks, peaks_src = load_peaks()
     achieved = bytes_step / (float(step_ms.mean()) * 1e-3) / 1e9

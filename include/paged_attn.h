@@ -97,9 +97,12 @@ typedef struct {
 /* Bytes of workspace a call with this shape needs on the current device (the
  * largest over the schedules).  The first 4 bytes are the flag word; the
  * caller must zero the workspace once before its first use (the flag is then
- * sticky across calls until cleared).  The rest holds the decode schedule's
- * per-split partial states (m, l, o[D] in fp32) and, last, the tile plan of
- * a ragged batch (B + 2 ints); it needs no initialisation.
+ * sticky across calls until cleared; the schedules' work counters in the
+ * first 256 bytes are zero again whenever a call has finished).  The rest
+ * holds the decode schedule's per-split partial states (m, l, o[D] in fp32),
+ * the tile plan of a ragged batch (B + 2 ints) and, last, the tile schedule's
+ * per-chunk partial states when it splits the keys of few, long query tiles
+ * (m, l, o[D] in fp32 per query row and chunk); it needs no initialisation.
  * Returns 0 for an invalid shape. */
 size_t pa_workspace_bytes(const pa_shape* shape);
 
@@ -263,7 +266,9 @@ pa_status pa_validate_metadata_varlen(const pa_shape* shape, const int32_t* bloc
  * or -1 for an invalid shape. */
 int pa_choose_schedule(const pa_shape* shape);
 
-/* Kernel launches one call of this shape and schedule enqueues. */
+/* Kernel launches one call of this shape and schedule enqueues on the current
+ * device (the tile schedule adds a merge kernel when it splits keys), or -1
+ * for an invalid shape or no device. */
 int pa_launch_count(const pa_shape* shape, int schedule);
 
 /* Decode schedule without a caller workspace, for callers that cannot
@@ -280,8 +285,9 @@ int pa_launch_count(const pa_shape* shape, int schedule);
  *   - Every argument is checked first, as in pa_paged_attention_sched
  *     (PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED on a device other than
  *     compute capability 10.3); a rejected call enqueues nothing.
- *   - Shapes whose decode scratch (pa_workspace_bytes) exceeds 8 MiB are
- *     rejected with PA_ERR_WORKSPACE before anything is enqueued.
+ *   - Shapes whose decode scratch (the page walk's part of
+ *     pa_workspace_bytes) exceeds 8 MiB are rejected with PA_ERR_WORKSPACE
+ *     before anything is enqueued.
  *   - Every call looks up the array's device address with the calling
  *     thread's device current (cheap once the library's device code is
  *     loaded there; still right after a cudaDeviceReset).  The first call on

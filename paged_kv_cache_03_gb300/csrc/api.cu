@@ -423,7 +423,11 @@ int pa_choose_schedule(const pa_shape* shape) {
 int pa_launch_count(const pa_shape* shape, int schedule) {
     if (check_shape(shape) != PA_OK) return -1;
     if (schedule == PA_SCHED_AUTO) schedule = choose(*shape);
-    return schedule == PA_SCHED_DECODE ? 2 : 1;
+    if (schedule == PA_SCHED_DECODE) return 2;
+    DeviceInfo dev;
+    if (current_device_info(&dev) != PA_OK) return -1;
+    // tiles (+ the merge of key chunks or of the last tile's rows)
+    return (tile_nsplit(*shape, dev.sm_count) > 1 || tile_remainder_rows(*shape) > 0) ? 2 : 1;
 }
 
 const char* pa_status_str(pa_status status) {

@@ -1459,8 +1459,12 @@ size_t varlen_plan_offset(const pa_shape& sh, int sm_count) {
     return align_up(d > kFlagBytes ? d : kFlagBytes, 256);
 }
 
+size_t tile_partials_offset(const pa_shape& sh, int sm_count) {
+    return align_up(varlen_plan_offset(sh, sm_count) + 4 * (static_cast<size_t>(sh.B) + 2), 256);
+}
+
 size_t workspace_bytes_total(const pa_shape& sh, int sm_count) {
-    return varlen_plan_offset(sh, sm_count) + 4 * (static_cast<size_t>(sh.B) + 2);
+    return tile_partials_offset(sh, sm_count) + tile_partial_bytes(sh, sm_count);
 }
 
 pa_status decode_launch(const Call& c) {

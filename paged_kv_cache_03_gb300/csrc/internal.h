@@ -85,6 +85,15 @@ pa_status decode_launch(const Call& c);
 
 // ---- prefill schedule (tcgen05 tensor cores) ------------------------------
 bool prefill_supported(const pa_shape& sh);
+// Key chunks per query-tile pair ([B, H_q, L, D] layout, no mask): more than 1
+// when the pairs alone would not fill the GPU twice; their partials follow the
+// ragged batch's plan in the workspace.
+int tile_nsplit(const pa_shape& sh, int sm_count);
+// Rows of a last query tile of at most 8 rows that the tile schedule gives to
+// the warp-level tensor cores of the last full pair's CTA (0: none).
+int tile_remainder_rows(const pa_shape& sh);
+size_t tile_partial_bytes(const pa_shape& sh, int sm_count);
+size_t tile_partials_offset(const pa_shape& sh, int sm_count);
 // 2-D TMA map over a bf16 row-major [rows, 128] matrix (the K or V pool seen
 // as rows (page * H_kv + kv_head) * page_size + slot), boxes of 64 dims x
 // box_rows rows, 128-byte swizzle.

@@ -49,7 +49,7 @@ extern "C" pa_status pa_paged_attention_decode_noalloc(
     st = pa::current_device_info(&dev);
     if (st != PA_OK) return st;
     if (dev.cc_major != 10 || dev.cc_minor != 3) return PA_ERR_UNSUPPORTED;
-    const size_t need = pa::workspace_bytes_total(*shape, dev.sm_count);
+    const size_t need = pa::decode_workspace_bytes(*shape, dev.sm_count);  // the page walk's
     if (need > pa::kNoAllocScratchBytes) return PA_ERR_WORKSPACE;  // beyond the fixed maximum
     void* scratch = nullptr;
     if (cudaGetSymbolAddress(&scratch, pa::g_noalloc_scratch) != cudaSuccess || !scratch) {

@@ -111,8 +111,24 @@ struct PrefillParams {
     const int32_t* cu_q;
     const int* pair_prefix;
     int total_q;
-    int n_items;        // work items (query-tile pairs x kv heads); a ragged batch's come from its plan
+    int n_items;        // work items (query-tile pairs x kv heads x key splits); a ragged batch's come from its plan
     int* item_counter;  // [next item to claim, CTAs done]: zero between calls
+    // key split ([B, H_q, L, D] layout only): each pair's key tiles are cut into
+    // nsplit equal chunks, one work item each; with nsplit > 1 every item writes
+    // fp32 partials (m, l per row; o[D] per row of a chunk with keys) that
+    // tile_combine_kernel merges
+    int nsplit;
+    float2* part_ml;  // [B * H_q * L][nsplit]
+    float* part_o;    // [B * H_q * L][nsplit][D]
+    // The last query tile of a sequence, when it holds at most 8 rows (nrem =
+    // G x the positions from rem_l0 on), is not a tensor-core item of its own:
+    // warps 2 and 3 of the last full pair's CTA take those rows over each
+    // staged K/V tile with warp-level MMA, 64 keys each, and write fp32
+    // partials per (key chunk, warp) for tile_combine_kernel.  0: none.
+    int nrem, rem_l0;
+    float2* rem_ml;  // [B * H_kv][nrem][nsplit * 2]
+    float* rem_o;    // [B * H_kv][nrem][nsplit * 2][D]
+    const void* q;   // the query, [B, H_q, L, D] (read by warps 2 and 3)
 };
 
 __device__ __forceinline__ float neg_inf() { return __int_as_float(0xff800000); }
@@ -192,14 +208,17 @@ __device__ __forceinline__ void exp_pack(const float (&x)[4][32], float2 c2, flo
 
 // One work item: query-tile pair mp of sequence b under kv head kvh.
 struct Item {
-    int b, kvh, mp, S, Lb, q0, nM, live;
+    int b, kvh, mp, S, Lb, q0, nM, live, c;  // c: key chunk of a split pair
 };
 
 // Work item i, heaviest pairs first (a CTA claims items from a counter, so
 // the heavy ones start early and the light ones fill the gaps at the end).
-template <bool kVarlen>
+// Full pairs go in decreasing mp (later queries see more keys under the
+// causal rule); an odd last tile, alone in its pair, does half a pair's
+// products and goes after the heavier half of the full pairs.
+template <bool kVarlen, bool kSplit>
 __device__ __forceinline__ Item decode_item(const PrefillParams& p, int i, int n_items) {
-    Item it{0, 0, 0, 0, 0, 0, 0, 0};
+    Item it{0, 0, 0, 0, 0, 0, 0, 0, 0};
     if (i >= n_items) return it;
     it.live = 1;
     if constexpr (kVarlen) {
@@ -217,9 +236,18 @@ __device__ __forceinline__ Item decode_item(const PrefillParams& p, int i, int n
         it.nM = (it.Lb + p.Lt - 1) / p.Lt;
         it.mp = (it.nM + 1) / 2 - 1 - (ip - __ldg(p.pair_prefix + lo));  // heavy pairs first
     } else {
+        const int ns = kSplit ? p.nsplit : 1;
+        const int pi = i / ns;  // the chunks of a pair are consecutive items
+        it.c = i - pi * ns;
         const int per_m = p.H_kv * p.B;
-        it.mp = p.nPairs - 1 - i / per_m;
-        const int rest = i % per_m;
+        const int q = pi / per_m;  // rank of the pair in the claim order
+        const int nfull = p.nM / 2, ins = nfull - nfull / 2;
+        if ((p.nM & 1) && q == ins) {
+            it.mp = nfull;  // the odd last tile
+        } else {
+            it.mp = nfull - 1 - ((p.nM & 1) && q > ins ? q - 1 : q);
+        }
+        const int rest = pi % per_m;
         it.b = rest / p.H_kv;
         it.kvh = rest % p.H_kv;
         it.Lb = p.L;
@@ -234,9 +262,13 @@ __device__ __forceinline__ Item decode_item(const PrefillParams& p, int i, int n
 // the first query position of each tile and the last key its first row sees.
 struct ItemWork {
     int nk_t[2], lim_min_t[2], l0_t[2], nk, ntiles;
+    // this item's key tiles: j0 .. j0 + nkc - 1, of which tile t takes the
+    // first nkc_t[t] (all of them without a key split)
+    int j0, nkc_t[2], nkc;
     bool valid_seq;
 };
 
+template <bool kSplit>
 __device__ __forceinline__ ItemWork item_work(const PrefillParams& p, const Item& it) {
     ItemWork w;
     w.valid_seq = it.S >= 1 && static_cast<long long>(it.S) <= p.max_S &&
@@ -252,13 +284,25 @@ __device__ __forceinline__ ItemWork item_work(const PrefillParams& p, const Item
         w.nk_t[t] = exists ? lim_max / BN + 1 : 0;
     }
     w.nk = max(w.nk_t[0], w.nk_t[1]);
+    // the last full pair also stages every key the remainder rows see
+    if (kSplit && p.nrem > 0 && it.mp == p.nPairs - 1 && w.valid_seq)
+        w.nk = max(w.nk, (it.S - 1) / BN + 1);
     w.ntiles = (2 * it.mp + 1 < it.nM) ? 2 : 1;
+    const int ns = kSplit ? p.nsplit : 1;
+    w.j0 = kSplit ? it.c * w.nk / ns : 0;
+    const int j1 = kSplit ? (it.c + 1) * w.nk / ns : w.nk;
+#pragma unroll
+    for (int t = 0; t < 2; ++t) w.nkc_t[t] = max(0, min(j1, w.nk_t[t]) - w.j0);
+    // (every tile of the chunk is staged: the last full pair's remainder rows
+    // may see a key tile past both of its query tiles' frontiers)
+    w.nkc = max(0, j1 - w.j0);
     return w;
 }
 
 // kMask: an explicit additive mask is read; kVarlen: a ragged batch (queries
-// packed by token, per-sequence query counts).  Separate instantiations, so
-// the plain kernel carries none of their code or registers.
+// packed by token, per-sequence query counts); kSplit: the keys of each pair
+// are cut into p.nsplit chunks that write fp32 partials.  Separate
+// instantiations, so the plain kernel carries none of their code or registers.
 //
 // Persistent: one CTA per SM claims work items (query-tile pairs) from a
 // counter in the workspace until none are left, so one item's set-up, query
@@ -266,7 +310,7 @@ __device__ __forceinline__ ItemWork item_work(const PrefillParams& p, const Item
 // epilogue instead of each CTA paying them alone.  The producer publishes
 // each item through a 2-slot ring in shared memory; every role runs the
 // item's steps with its own running counts of the barriers' phases.
-template <bool kMask, bool kVarlen>
+template <bool kMask, bool kVarlen, bool kSplit>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tile_kernel(const __grid_constant__ CUtensorMap tm_q,
                         const __grid_constant__ CUtensorMap tm_k,
@@ -290,15 +334,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(bar(kQEmpty), 1);
         for (int s = 0; s < 2; ++s) {
             mbar_init(bar(kKFull + s), 1);
-            mbar_init(bar(kKEmpty + s), 1);
+            mbar_init(bar(kKEmpty + s), (kSplit && p.nrem > 0) ? 3 : 1);  // + warps 2, 3
             mbar_init(bar(kSFull + s), 1);
             mbar_init(bar(kPFull + s), 4);
             mbar_init(bar(kODone + s), 1);
             mbar_init(bar(kOFree + s), 4);
             mbar_init(bar(kVFull + s), 1);
-            mbar_init(bar(kVEmpty + s), 1);
+            mbar_init(bar(kVEmpty + s), (kSplit && p.nrem > 0) ? 3 : 1);
             mbar_init(bar(kItemFull + s), 1);
-            mbar_init(bar(kItemEmpty + s), 9);  // the MMA thread + 8 softmax warps
+            // the MMA thread + 8 softmax warps (+ warps 2 and 3 for remainder rows)
+            mbar_init(bar(kItemEmpty + s), (kSplit && p.nrem > 0) ? 11 : 9);
         }
         mbar_init(bar(kMmaDone), 1);
         mbar_init(bar(kVTail), 1);
@@ -329,7 +374,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // kItemEmpty.
     auto read_item = [&](int k) {
         const int4 a = item_slot[2 * (k & 1)], c = item_slot[2 * (k & 1) + 1];
-        return Item{a.x, a.y, a.z, a.w, c.x, c.y, c.z, c.w};
+        return Item{a.x, a.y, a.z, a.w, c.x, c.y, c.z, c.w & 1, c.w >> 1};
     };
     auto take_item = [&](int k, Item& it) -> bool {  // a whole warp
         if (!warp_wait(bar(kItemFull + (k & 1)), (k >> 1) & 1)) return false;
@@ -359,23 +404,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         int kdone = 0, vdone = 0;  // K and V tiles issued in all
         bool ok = true;
         for (int k = 0; ok; ++k) {
-            const Item it = decode_item<kVarlen>(p, idx, n_items);
+            const Item it = decode_item<kVarlen, kSplit>(p, idx, n_items);
             const int next = it.live ? claim() : idx;  // the next item's claim goes out early
-            const ItemWork w = item_work(p, it);
+            const ItemWork w = item_work<kSplit>(p, it);
             if (k >= 2 && !warp_wait(bar(kItemEmpty + (k & 1)), ((k >> 1) - 1) & 1)) {
                 if (lane == 0) give_up(p, abort_flag);
                 break;
             }
             if (lane == 0) {
                 item_slot[2 * (k & 1)] = make_int4(it.b, it.kvh, it.mp, it.S);
-                item_slot[2 * (k & 1) + 1] = make_int4(it.Lb, it.q0, it.nM, it.live);
+                item_slot[2 * (k & 1) + 1] = make_int4(it.Lb, it.q0, it.nM, it.live | (it.c << 1));
                 mbar_arrive(bar(kItemFull + (k & 1)));
             }
             __syncwarp();
             if (!it.live) break;
             idx = next;
             if (!w.valid_seq && lane == 0) atomicOr(p.flag, PA_FLAG_BAD_CONTEXT);
-            if (w.nk == 0) continue;
+            if (w.nkc == 0) continue;
             // the query tiles, once the previous item's products have read theirs
             if (qn > 0 && !warp_wait(bar(kQEmpty), (qn - 1) & 1)) {
                 if (lane == 0) give_up(p, abort_flag);
@@ -406,9 +451,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int tail_tile = (it.S % p.box_rows != 0) ? (it.S - 1) / BN : -1;
             int rows_cur[4], rows_next[4] = {-1, -1, -1, -1};
             uint32_t bytes_cur, bytes_next = 0;
-            tile_boxes(p, it.b, it.kvh, it.S, 0, lane, rows_cur, bytes_cur);
-            for (int j = 0; j < w.nk; ++j) {
-                const int gk = kt + j, s = gk & 1;
+            tile_boxes(p, it.b, it.kvh, it.S, w.j0, lane, rows_cur, bytes_cur);
+            for (int jj = 0; jj < w.nkc; ++jj) {
+                const int j = w.j0 + jj;  // key tile
+                const int gk = kt + jj, s = gk & 1;
                 if (gk >= 2 && !warp_wait(bar(kKEmpty + s), ((gk >> 1) - 1) & 1)) {
                     if (lane == 0) give_up(p, abort_flag);
                     ok = false;
@@ -435,7 +481,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 issue_boxes(&tm_v, base + kOffV + s * kTile, rows_cur, lane, p.box_rows, vbar,
                             pol_kv);
                 // rows of the next tile, looked up before waiting for a free slot
-                if (j + 1 < w.nk) tile_boxes(p, it.b, it.kvh, it.S, j + 1, lane, rows_next, bytes_next);
+                if (jj + 1 < w.nkc) tile_boxes(p, it.b, it.kvh, it.S, j + 1, lane, rows_next, bytes_next);
                 if (vtail) {  // the item's last tile: nothing of this item waits behind it
                     if (!warp_wait(bar(kVTail), vtails & 1)) {
                         if (lane == 0) give_up(p, abort_flag);
@@ -461,7 +507,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int q = 0; q < 4; ++q) rows_cur[q] = rows_next[q];
                 bytes_cur = bytes_next;
             }
-            kt += w.nk;
+            kt += w.nkc;
         }
         // let every copy into this CTA's shared memory land before leaving
         if (qn > 0 && !mbar_wait(bar(kQFull), (qn - 1) & 1)) give_up(p, abort_flag);
@@ -527,10 +573,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 it = read_item(k);
                 mbar_arrive(bar(kItemEmpty + (k & 1)));
                 if (!it.live) break;
-                const ItemWork w = item_work(p, it);
-                if (w.nk == 0) continue;
-                const int* nk_t = w.nk_t;
-                const int nk = w.nk;
+                const ItemWork w = item_work<kSplit>(p, it);
+                if (w.nkc == 0) continue;
+                const int* nk_t = w.nkc_t;  // this item's tiles (j counts from its first)
+                const int nk = w.nkc;
                 ok = mbar_wait(bar(kQFull), qn & 1) && mbar_wait(bar(kKFull + (kt & 1)), (kt >> 1) & 1);
                 if (!ok || *abort_flag) break;
                 tc::fence_after_sync();
@@ -603,8 +649,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int k = 0; ok; ++k) {
             ok = take_item(k, it);
             if (!ok || !it.live) break;
-            const ItemWork w = item_work(p, it);
-            const int nkA = w.nk_t[0], nkB = w.nk_t[1];
+            const ItemWork w = item_work<kSplit>(p, it);
+            const int nkA = w.nkc_t[0], nkB = w.nkc_t[1];
             const int nkt = t == 0 ? nkA : nkB;
             const int pv_own = t == 0 ? pvA : pvB;
             const int lim_min = t == 0 ? w.lim_min_t[0] : w.lim_min_t[1];
@@ -624,7 +670,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // the lines holding this row's visible mask entries of key tile jj go
             // to L2 ahead of use: keys [jj * BN, min(jj * BN + BN, lim + 1)), all
             // inside the row (lim < S <= mask_S)
-            auto prefetch_mask = [&](int jj) {
+            auto prefetch_mask = [&](int jj) {  // (no key split with a mask: j0 = 0)
                 if (!kMask || !mask_row || jj >= nkt) return;
                 const int k0 = jj * BN;
                 if (k0 > lim) return;
@@ -644,7 +690,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             float mrow = neg_inf();
             float2 lsum2 = make_float2(0.f, 0.f);
-            for (int j = 0; j < nkt; ++j) {
+            for (int j = 0; j < nkt; ++j) {  // j: this item's tile count, jt the key tile
+                const int jt = w.j0 + j;
                 prefetch_mask(j + 1);
                 ok = warp_wait(bar(kSFull + t), (sc + j) & 1);
                 if (!ok || aborted(abort_flag)) break;
@@ -655,7 +702,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc::wait_ld();
                 if constexpr (kMask) {  // s * scale * log2 e + mask * log2 e
                     // only the words holding a visible key (k0 + 4q <= lim < mask_S)
-                    const int k0 = j * BN;
+                    const int k0 = jt * BN;
 #pragma unroll
                     for (int q = 0; q < 32; ++q) {
                         float4 mv = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -669,9 +716,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
                 // causal / length mask (frontier tiles only), row max of raw scores
-                const bool masking = j * BN + BN - 1 > lim_min;  // uniform over the CTA
+                const bool masking = jt * BN + BN - 1 > lim_min;  // uniform over the CTA
                 if (masking) {
-                    const int cmax = lim - j * BN;  // columns <= cmax are visible
+                    const int cmax = lim - jt * BN;  // columns <= cmax are visible
 #pragma unroll
                     for (int cc = 0; cc < 4; ++cc)
 #pragma unroll
@@ -749,6 +796,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (!ok) break;
             const float lsum = lsum2.x + lsum2.y;
+            // a split pair: this chunk's (m, l) of every row, o of rows with keys
+            constexpr bool split = kSplit;
+            const long long prow = kSplit ? orow_idx * p.nsplit + it.c : 0;
+            if (split && row_valid) p.part_ml[prow] = make_float2(nkt > 0 ? mrow : neg_inf(), lsum);
             if (nkt > 0) {
                 if (!warp_wait(bar(kODone + t), (pv_own + nkt - 1) & 1)) {
                     ok = false;
@@ -762,7 +813,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     float o[32];
                     tc::ld32(trow + col_o(t) + cc * 32, o);
                     tc::wait_ld();
-                    if (row_valid) {
+                    if (split) {
+                        if (row_valid) {
+                            float4* const po = reinterpret_cast<float4*>(p.part_o + prow * kD + cc * 32);
+#pragma unroll
+                            for (int q = 0; q < 8; ++q)
+                                po[q] = make_float4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+                        }
+                    } else if (row_valid) {
 #pragma unroll
                         for (int q = 0; q < 4; ++q) {
                             const uint4 wv = make_uint4(
@@ -779,7 +837,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(kOFree + t));
             }
-            if (!w.valid_seq && row_valid) {
+            if (!w.valid_seq && row_valid && !split) {
                 uint4* orow = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) + orow_idx * kD);
                 for (int q = 0; q < kD / 8; ++q) orow[q] = make_uint4(0u, 0u, 0u, 0u);
             }
@@ -788,8 +846,161 @@ __global__ void __launch_bounds__(kThreads, 1)
             pvB += nkB;
         }
         if (!ok && lane == 0) give_up(p, abort_flag);
+    } else if (kSplit && (warp == 2 || warp == 3)) {
+        // ====================== remainder rows (warps 2, 3) =====================
+        // S^T = K Q^T and O^T += V^T P^T with mma m16n8k16 (16 keys x 8 rows):
+        // lane 4g + t holds keys g and g + 8 of rows 2t and 2t + 1, and O^T of
+        // dims 16 i + g and 16 i + g + 8 of the same rows (rows past nrem are
+        // zero).  P is rounded to bf16 and the row sums add the rounded weights.
+        if (p.nrem > 0) {
+            const int wr = warp - 2;          // keys 64 wr .. 64 wr + 63 of every tile
+            const int g = lane >> 2, t4 = lane & 3;
+            const int Lrem = p.L - p.rem_l0;
+            const float c = p.scale_log2;
+            int kt = 0;
+            bool ok = true;
+            Item it;
+            for (int k = 0; ok; ++k) {
+                ok = take_item(k, it);
+                if (!ok || !it.live) break;
+                const ItemWork w = item_work<true>(p, it);
+                const bool rem = it.mp == p.nPairs - 1;
+                uint32_t qf[8][2];
+                float oacc[8][4];
+                float m_r[2] = {neg_inf(), neg_inf()}, l_r[2] = {0.f, 0.f};
+                int lim_r[2] = {-1, -1};  // last key each of rows 2t, 2t + 1 sees
+                if (rem) {
+                    const bool qok = g < p.nrem && w.valid_seq;
+                    const int gq = g / Lrem, lq = p.rem_l0 + (g - gq * Lrem);
+                    const uint16_t* const qrow =
+                        static_cast<const uint16_t*>(p.q) +
+                        ((static_cast<long long>(it.b) * p.H_q + it.kvh * p.G + gq) * p.L + lq) * kD;
+#pragma unroll
+                    for (int ks = 0; ks < 8; ++ks) {
+                        qf[ks][0] = qok ? __ldg(reinterpret_cast<const unsigned int*>(qrow + ks * 16 + 2 * t4)) : 0u;
+                        qf[ks][1] = qok ? __ldg(reinterpret_cast<const unsigned int*>(qrow + ks * 16 + 8 + 2 * t4)) : 0u;
+                    }
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const int rr = 2 * t4 + e;
+                        const int lr = p.rem_l0 + rr % Lrem;
+                        if (rr < p.nrem && w.valid_seq)
+                            lim_r[e] = min(p.causal ? lr + it.S - p.L : it.S - 1, it.S - 1);
+                    }
+#pragma unroll
+                    for (int mt = 0; mt < 8; ++mt) oacc[mt][0] = oacc[mt][1] = oacc[mt][2] = oacc[mt][3] = 0.f;
+                }
+                for (int jj = 0; jj < w.nkc; ++jj) {
+                    const int j = w.j0 + jj, gk = kt + jj, s = gk & 1;
+                    ok = warp_wait(bar(kKFull + s), (gk >> 1) & 1) &&
+                         warp_wait(bar(kVFull + s), (gk >> 1) & 1);
+                    if (!ok || aborted(abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    if (rem) {
+                        const uint32_t kb = base + kOffK + s * kTile, vb = base + kOffV + s * kTile;
+#pragma unroll 1
+                        for (int grp = 0; grp < 4; ++grp) {
+                            const int kw0 = 64 * wr + 16 * grp;  // first key of the group in the tile
+                            if (j * BN + kw0 >= it.S) break;     // (uniform over the warp)
+                            float sacc[4] = {0.f, 0.f, 0.f, 0.f};
+                            {
+                                const int r = kw0 + (lane & 7) + ((lane >> 3) & 1) * 8;
+#pragma unroll
+                                for (int ks = 0; ks < 8; ++ks) {
+                                    const int cq = ks * 2 + (lane >> 4);
+                                    uint32_t a[4];
+                                    ldmatrix_x4(a, kb + (cq >> 3) * kHalf + r * 128 + (((cq & 7) ^ (r & 7)) << 4));
+                                    mma_16816(sacc, a, qf[ks][0], qf[ks][1]);
+                                }
+                            }
+                            float x[4];
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const int key = j * BN + kw0 + g + (e >> 1) * 8;
+                                x[e] = key <= lim_r[e & 1] ? sacc[e] * c : neg_inf();
+                            }
+                            float mt0 = fmaxf(x[0], x[2]), mt1 = fmaxf(x[1], x[3]);
+#pragma unroll
+                            for (int o = 4; o < 32; o <<= 1) {
+                                mt0 = fmaxf(mt0, __shfl_xor_sync(0xffffffffu, mt0, o));
+                                mt1 = fmaxf(mt1, __shfl_xor_sync(0xffffffffu, mt1, o));
+                            }
+                            const bool gr0 = mt0 > m_r[0] + kLazyRescaleLog2;
+                            const bool gr1 = mt1 > m_r[1] + kLazyRescaleLog2;
+                            if (__any_sync(0xffffffffu, gr0 || gr1)) {
+                                const float a0 = gr0 ? fast_exp2(m_r[0] - mt0) : 1.f;
+                                const float a1 = gr1 ? fast_exp2(m_r[1] - mt1) : 1.f;
+                                if (gr0) m_r[0] = mt0;
+                                if (gr1) m_r[1] = mt1;
+                                l_r[0] *= a0;
+                                l_r[1] *= a1;
+#pragma unroll
+                                for (int mt = 0; mt < 8; ++mt) {
+                                    oacc[mt][0] *= a0;
+                                    oacc[mt][1] *= a1;
+                                    oacc[mt][2] *= a0;
+                                    oacc[mt][3] *= a1;
+                                }
+                            }
+                            const float mu0 = m_r[0] == neg_inf() ? 0.f : m_r[0];
+                            const float mu1 = m_r[1] == neg_inf() ? 0.f : m_r[1];
+                            const uint32_t X0 = pack_bf16x2(fast_exp2(x[0] - mu0), fast_exp2(x[1] - mu1));
+                            const uint32_t X1 = pack_bf16x2(fast_exp2(x[2] - mu0), fast_exp2(x[3] - mu1));
+                            {
+                                const float2 f0 = bf16x2_to_float2(X0), f1 = bf16x2_to_float2(X1);
+                                l_r[0] += f0.x + f1.x;
+                                l_r[1] += f0.y + f1.y;
+                            }
+                            const uint32_t pb0 = movmatrix_trans(X0), pb1 = movmatrix_trans(X1);
+                            {
+                                const int r = kw0 + (lane & 7) + (lane >> 4) * 8;
+#pragma unroll
+                                for (int mt = 0; mt < 8; ++mt) {
+                                    const int cq = mt * 2 + ((lane >> 3) & 1);
+                                    uint32_t a[4];
+                                    ldmatrix_x4_trans(a, vb + (cq >> 3) * kHalf + r * 128 + (((cq & 7) ^ (r & 7)) << 4));
+                                    mma_16816(oacc[mt], a, pb0, pb1);
+                                }
+                            }
+                        }
+                    }
+                    __syncwarp();
+                    if (lane == 0) {
+                        mbar_arrive(bar(kKEmpty + s));
+                        mbar_arrive(bar(kVEmpty + s));
+                    }
+                }
+                if (!ok) break;
+                kt += w.nkc;
+                if (rem) {  // this warp's partial of the chunk: (m, l) per row, o^T
+#pragma unroll
+                    for (int o = 4; o < 32; o <<= 1) {
+                        l_r[0] += __shfl_xor_sync(0xffffffffu, l_r[0], o);
+                        l_r[1] += __shfl_xor_sync(0xffffffffu, l_r[1], o);
+                    }
+                    const int nslot = p.nsplit * 2, slot = it.c * 2 + wr;
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const int rr = 2 * t4 + e;
+                        if (rr >= p.nrem) continue;
+                        const long long pr =
+                            (static_cast<long long>(it.b * p.H_kv + it.kvh) * p.nrem + rr) * nslot + slot;
+                        if (g == 0) p.rem_ml[pr] = make_float2(l_r[e] > 0.f ? m_r[e] : neg_inf(), l_r[e]);
+                        float* const po = p.rem_o + pr * kD;
+#pragma unroll
+                        for (int mt = 0; mt < 8; ++mt) {
+                            po[16 * mt + g] = oacc[mt][e];
+                            po[16 * mt + g + 8] = oacc[mt][2 + e];
+                        }
+                    }
+                }
+            }
+            if (!ok && lane == 0) give_up(p, abort_flag);
+        }
     } else {
-        // warps 2 and 3: readers of no item; they only keep the ring moving
+        // warps 2 and 3 (other instances): readers of no item
     }
 
     // ---- tear-down: free TMEM once every role is done -----------------------
@@ -799,6 +1010,55 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::fence_after_sync();
         tc::tmem_dealloc(tmem, kTmemCols);
     }
+}
+
+// Merges the key chunks of split pairs: one warp per output row (b, h, l) of
+// the [B, H_q, L, D] layout, four dims per lane.  Chunks that saw no key of a
+// row (m = -inf) weigh nothing; a row with none (a sequence whose context
+// breaks the contract) is written as zeros.
+__global__ void __launch_bounds__(128) tile_combine_kernel(const PrefillParams p) {
+    pdl_wait_primary();
+    const long long rows = static_cast<long long>(p.B) * p.H_q * p.L;
+    const long long row = static_cast<long long>(blockIdx.x) * 4 + (threadIdx.x >> 5);
+    if (row >= rows) return;
+    const int lane = threadIdx.x & 31;
+    int ns = p.nsplit;
+    const float2* ml = p.part_ml + row * ns;
+    const float* po = p.part_o + row * ns * kD;
+    if (p.nrem > 0) {  // a remainder row: its partials per (chunk, warp)
+        const int l = static_cast<int>(row % p.L);
+        if (l >= p.rem_l0) {
+            const long long bh = row / p.L;
+            const int h = static_cast<int>(bh % p.H_q), b = static_cast<int>(bh / p.H_q);
+            const int kvh = h / p.G, rr = (h - kvh * p.G) * (p.L - p.rem_l0) + (l - p.rem_l0);
+            ns = 2 * p.nsplit;
+            const long long pr = (static_cast<long long>(b * p.H_kv + kvh) * p.nrem + rr) * ns;
+            ml = p.rem_ml + pr;
+            po = p.rem_o + pr * kD;
+        }
+    }
+    float M = neg_inf();
+    for (int c = lane; c < ns; c += 32) M = fmaxf(M, ml[c].x);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    float den = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (M != neg_inf()) {
+        for (int c = 0; c < ns; ++c) {
+            const float2 v = ml[c];
+            if (v.x == neg_inf()) continue;
+            const float a = fast_exp2(v.x - M);
+            den += a * v.y;
+            const float4 o = *reinterpret_cast<const float4*>(po + c * kD + 4 * lane);
+            acc.x += a * o.x;
+            acc.y += a * o.y;
+            acc.z += a * o.z;
+            acc.w += a * o.w;
+        }
+    }
+    const float inv = den > 0.f ? 1.f / den : 0.f;
+    *reinterpret_cast<uint2*>(static_cast<uint16_t*>(p.out) + row * kD + 4 * lane) =
+        make_uint2(pack_bf16x2(acc.x * inv, acc.y * inv), pack_bf16x2(acc.z * inv, acc.w * inv));
 }
 
 // Ragged batch: pair_prefix[b] = query-tile pairs of the sequences before b
@@ -918,6 +1178,40 @@ int gcd_int(int a, int b) {
 
 }  // namespace
 
+// Rows of the last query tile handled by warps 2 and 3 of the last full pair
+// ([B, H_q, L, D] layout, no mask): G x its positions when the tile is alone
+// in its pair and holds at most 8 rows, else 0.
+int tile_remainder_rows(const pa_shape& sh) {
+    if (!prefill_supported(sh)) return 0;
+    const int G = sh.H_q / sh.H_kv, Lt = BM / G;
+    const int nM = (sh.L + Lt - 1) / Lt;
+    if (nM < 3 || nM % 2 == 0) return 0;
+    const int rows = G * (sh.L - (nM - 1) * Lt);
+    return rows <= 8 ? rows : 0;
+}
+
+int tile_nsplit(const pa_shape& sh, int sm_count) {
+    if (!prefill_supported(sh) || sm_count < 1) return 1;
+    const int G = sh.H_q / sh.H_kv, Lt = BM / G;
+    const long long nM = (sh.L + Lt - 1) / Lt;
+    const long long items = (tile_remainder_rows(sh) > 0 ? nM / 2 : (nM + 1) / 2) * sh.B * sh.H_kv;
+    if (items >= 2ll * sm_count) return 1;  // enough pairs to fill the GPU twice
+    // a few chunks of at least two key tiles each on the longest context
+    const long long cap_tiles = (static_cast<long long>(sh.max_pages_per_seq) * sh.page_size + BN - 1) / BN;
+    long long ns = (2ll * sm_count + items - 1) / items;
+    ns = std::min(ns, std::min(cap_tiles / 2, 16ll));
+    return ns > 1 ? static_cast<int>(ns) : 1;
+}
+
+size_t tile_partial_bytes(const pa_shape& sh, int sm_count) {
+    const long long ns = tile_nsplit(sh, sm_count);
+    const int nrem = tile_remainder_rows(sh);
+    if (ns <= 1 && nrem == 0) return 0;
+    const size_t rows = static_cast<size_t>(sh.B) * sh.H_q * sh.L * ns;
+    const size_t rrows = static_cast<size_t>(sh.B) * sh.H_kv * nrem * ns * 2;
+    return align_up(rows * 8, 256) + rows * kD * 4 + align_up(rrows * 8, 256) + rrows * kD * 4;
+}
+
 bool prefill_supported(const pa_shape& sh) {
     if (sh.dtype != PA_BF16 || sh.D != kD) return false;
     const int G = sh.H_q / sh.H_kv;
@@ -950,13 +1244,16 @@ pa_status prefill_launch(const Call& c) {
 
     static int attr_done[64] = {0};
     if (c.dev.device >= 0 && c.dev.device < 64 && !attr_done[c.dev.device]) {
-        if (cudaFuncSetAttribute(prefill_tile_kernel<false, false>,
+        if (cudaFuncSetAttribute(prefill_tile_kernel<false, false, false>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  kSmemBytes) != cudaSuccess ||
-            cudaFuncSetAttribute(prefill_tile_kernel<true, false>,
+            cudaFuncSetAttribute(prefill_tile_kernel<false, false, true>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  kSmemBytes) != cudaSuccess ||
-            cudaFuncSetAttribute(prefill_tile_kernel<false, true>,
+            cudaFuncSetAttribute(prefill_tile_kernel<true, false, false>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kSmemBytes) != cudaSuccess ||
+            cudaFuncSetAttribute(prefill_tile_kernel<false, true, false>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  kSmemBytes) != cudaSuccess)
             return PA_ERR_CUDA;
@@ -988,6 +1285,35 @@ pa_status prefill_launch(const Call& c) {
     p.total_q = c.total_q;
     p.pair_prefix = nullptr;
     p.item_counter = reinterpret_cast<int*>(static_cast<uint8_t*>(c.ws) + kTileCounterOffset);
+    p.nsplit = (c.cu_q || c.mask) ? 1 : tile_nsplit(sh, c.dev.sm_count);
+    p.nrem = (c.cu_q || c.mask) ? 0 : tile_remainder_rows(sh);
+    p.rem_l0 = 0;
+    p.q = c.q;
+    p.part_ml = nullptr;
+    p.part_o = nullptr;
+    p.rem_ml = nullptr;
+    p.rem_o = nullptr;
+    if (p.nrem > 0) {  // the last tile's rows go to warps 2 and 3 of the last full pair
+        p.rem_l0 = (p.nM - 1) * Lt;
+        p.nM -= 1;
+        p.nPairs = p.nM / 2;
+    }
+    const bool split = p.nsplit > 1 || p.nrem > 0;  // partials and the merge kernel
+    if (split) {
+        uint8_t* const ws = static_cast<uint8_t*>(c.ws) + tile_partials_offset(sh, c.dev.sm_count);
+        if (c.ws_bytes < tile_partials_offset(sh, c.dev.sm_count) + tile_partial_bytes(sh, c.dev.sm_count))
+            return PA_ERR_WORKSPACE;
+        const size_t rows = static_cast<size_t>(sh.B) * sh.H_q * sh.L * p.nsplit;
+        const size_t rrows = static_cast<size_t>(sh.B) * sh.H_kv * p.nrem * p.nsplit * 2;
+        size_t off = 0;
+        p.part_ml = reinterpret_cast<float2*>(ws + off);
+        off += align_up(rows * 8, 256);
+        p.part_o = reinterpret_cast<float*>(ws + off);
+        off += rows * kD * 4;
+        p.rem_ml = reinterpret_cast<float2*>(ws + off);
+        off += align_up(rrows * 8, 256);
+        p.rem_o = reinterpret_cast<float*>(ws + off);
+    }
     long long pairs = static_cast<long long>(p.nPairs) * sh.B;
     if (c.cu_q) {
         // the pairs of all sequences are at most ceil(L_b / (2 Lt)) each, so at
@@ -1003,18 +1329,33 @@ pa_status prefill_launch(const Call& c) {
         if (pairs == 0) return PA_OK;
     }
     // persistent: one CTA per SM (or per item, when there are fewer)
-    const long long items = pairs * sh.H_kv;
+    const long long items = pairs * sh.H_kv * p.nsplit;
     p.n_items = static_cast<int>(items);
     const unsigned grid = static_cast<unsigned>(std::min<long long>(items, c.dev.sm_count));
     if (c.ev_before && cudaEventRecord(c.ev_before, c.stream) != cudaSuccess) return PA_ERR_CUDA;
     if (c.cu_q)  // (a ragged batch takes no explicit mask)
-        prefill_tile_kernel<false, true><<<grid, kThreads, kSmemBytes, c.stream>>>(tq, tk, tv, p);
+        prefill_tile_kernel<false, true, false><<<grid, kThreads, kSmemBytes, c.stream>>>(tq, tk, tv, p);
     else if (c.mask)
-        prefill_tile_kernel<true, false><<<grid, kThreads, kSmemBytes, c.stream>>>(tq, tk, tv, p);
+        prefill_tile_kernel<true, false, false><<<grid, kThreads, kSmemBytes, c.stream>>>(tq, tk, tv, p);
+    else if (split)
+        prefill_tile_kernel<false, false, true><<<grid, kThreads, kSmemBytes, c.stream>>>(tq, tk, tv, p);
     else
-        prefill_tile_kernel<false, false><<<grid, kThreads, kSmemBytes, c.stream>>>(tq, tk, tv, p);
+        prefill_tile_kernel<false, false, false><<<grid, kThreads, kSmemBytes, c.stream>>>(tq, tk, tv, p);
     if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
     if (c.ev_after && cudaEventRecord(c.ev_after, c.stream) != cudaSuccess) return PA_ERR_CUDA;
+    if (split) {  // merge the key chunks (may launch while the tiles finish)
+        const long long rows = static_cast<long long>(sh.B) * sh.H_q * sh.L;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(static_cast<unsigned>((rows + 3) / 4));
+        cfg.blockDim = dim3(128);
+        cfg.stream = c.stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (cudaLaunchKernelEx(&cfg, tile_combine_kernel, p) != cudaSuccess) return PA_ERR_CUDA;
+    }
     return PA_OK;
 }
 

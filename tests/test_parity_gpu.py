@@ -396,6 +396,38 @@ def test_long_prefill_8192(oracle_lib):
     gu.assert_parity(got, gu.oracle_rows(oracle_lib, inp, rows), "bf16", "prefill 8192")
 
 
+# ---- the tile schedule's key split and last-tile rows -----------------------------
+SPLIT_CASES = [
+    # (name, kwargs): few query-tile pairs (keys split into chunks), and a last
+    # query tile of at most 8 rows taken by the last full pair's CTA
+    ("L65_G4_remainder4", dict(B=3, H_q=16, H_kv=4, L=65, page_size=64,
+                               context_lens=[65, 700, 2000])),
+    ("L66_G4_remainder8", dict(B=2, H_q=8, H_kv=2, L=66, page_size=128,
+                               context_lens=[66, 1500])),
+    ("L33_G8_remainder8", dict(B=2, H_q=16, H_kv=2, L=33, page_size=32,
+                               context_lens=[40, 900])),
+    ("L257_G1_remainder1", dict(B=1, H_q=2, H_kv=2, L=257, page_size=64, context_lens=[600])),
+    ("L65_many_pairs_no_split", dict(B=40, H_q=32, H_kv=8, L=65, page_size=128,
+                                     ctx_range=(65, 400))),
+    ("L200_split_only", dict(B=1, H_q=8, H_kv=2, L=200, page_size=16, context_lens=[3000])),
+    # contexts of 128 k + 1 keys: only the last tile's rows see the final key tile
+    ("L65_last_key_tile_remainder_only", dict(B=3, H_q=32, H_kv=8, L=65, page_size=128,
+                                              context_lens=[129, 257, 1025])),
+]
+
+
+@pytest.mark.parametrize("name,kw", SPLIT_CASES, ids=[c[0] for c in SPLIT_CASES])
+@pytest.mark.parametrize("causal", [True, False])
+def test_tile_key_split_and_last_tile_rows(oracle_lib, name, kw, causal):
+    """Shapes on which the tile schedule splits each pair's keys into chunks
+    merged by the combine kernel, and/or gives the rows of a short last query
+    tile to the warp-level tensor cores of the last full pair: every element
+    against the oracle, on the automatic choice and the forced tiles."""
+    inp = synth.generate(D=128, seed=sum(map(ord, name)) + 31, causal=causal, name=name, **kw)
+    for sched in (B.PA_SCHED_AUTO, B.PA_SCHED_PREFILL):
+        check(oracle_lib, inp, sched, what=f"{name} causal={causal} sched {sched}")
+
+
 # ---- mask=None with more queries than keys ---------------------------------------
 NONCAUSAL_LONG_L = [
     # (name, kwargs): L > context_len for some or all sequences, causal off

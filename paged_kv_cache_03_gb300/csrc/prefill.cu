@@ -25,15 +25,20 @@
 //     and one thread issues tcgen05.mma in the order PV_A(j), S_A(j+1),
 //     PV_B(j), S_B(j+1): while one softmax warpgroup works on its tile the
 //     tensor core runs the other tile's products.  S = Q.K^T uses K-major
-//     operands; O += P.V reads V MN-major from its natural [key][dim] layout.
+//     operands; O += P.V takes P from TMEM and reads V MN-major from its
+//     natural [key][dim] layout.  S_t(j+1) overwrites the columns that hold
+//     P_t(j); it is issued after P.V_t(j), and one thread's MMAs execute in
+//     issue order.
 //   * Warps 4-7 (tile A) and 8-11 (tile B) run the softmax, one TMEM lane
 //     (query row) per thread: S row from TMEM, causal/length mask, row max of
 //     the raw scores, running max moved only when it grows by more than 2^8
 //     (then O is rescaled in TMEM), p = 2^(s*scale*log2 e - m) with one packed
-//     FMA and one exp2 per score, P rounded to bf16 into swizzled shared
-//     memory for the P.V MMA (one buffer, written by A and B in turn), running
-//     sum in fp32; at the end O/l -> bf16 -> global.  Whole K/V tiles past a
-//     tile's last causal frontier are skipped.
+//     FMA and one exp2 per score, P rounded to bf16 and stored back into
+//     Tensor Memory over the first 64 columns of the tile's S, where the P.V
+//     MMA reads it as its A operand (so P crosses no shared memory and the
+//     two tiles never wait for each other's products), running sum in fp32;
+//     at the end O/l -> bf16 -> global.  Whole K/V tiles past a tile's last
+//     causal frontier are skipped.
 //   * Boxes are copied whole, so a sequence's last K/V tile can carry page
 //     rows past its context (unused slots, any contents).  Their scores are
 //     masked to -inf.  Their V rows would still meet a weight of exactly 0,
@@ -70,8 +75,7 @@ constexpr int kTile = 2 * kHalf;  // 128 rows x 128 bf16
 constexpr int kOffQ = 0;                    // tile t at kOffQ + t * kTile
 constexpr int kOffK = kOffQ + 2 * kTile;    // slot s at kOffK + s * kTile
 constexpr int kOffV = kOffK + 2 * kTile;    // slot s at kOffV + s * kTile
-constexpr int kOffP = kOffV + 2 * kTile;    // one P buffer, used by A and B in turn
-constexpr int kOffBar = kOffP + kTile;
+constexpr int kOffBar = kOffV + 2 * kTile;
 enum Bar {
     kQFull = 0,
     kKFull = 1,   // + slot
@@ -535,7 +539,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t dQ1 = tc::smem_desc_sw128(base + kOffQ + kTile, 16, 1024);
             const uint64_t dK0 = tc::smem_desc_sw128(base + kOffK, 16, 1024);
             const uint64_t dK1 = tc::smem_desc_sw128(base + kOffK + kTile, 16, 1024);
-            const uint64_t dP = tc::smem_desc_sw128(base + kOffP, 16, 1024);
             const uint64_t dV0 = tc::smem_desc_sw128(base + kOffV, kHalf, 1024);
             const uint64_t dV1 = tc::smem_desc_sw128(base + kOffV + kTile, kHalf, 1024);
             auto qk = [&](int t, int gk) {
@@ -549,17 +552,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tc::commit(bar(kSFull + t));
             };
+            // P is read from Tensor Memory, where the softmax left it over
+            // the first 64 columns of the tile's S (8 columns per 16 keys).
+            // The next Q.K^T into those columns is issued after this product,
+            // and the tensor core runs one thread's MMAs in issue order.
             auto pv = [&](int t, int j, int gk) {
                 const uint64_t dv = (gk & 1) ? dV1 : dV0;
-                const uint32_t d = tmem + col_o(t);
-                if (j > 0) tc::mma_bf16_c<1>(d, dP, dv, idO);
-                else tc::mma_bf16_c<0>(d, dP, dv, idO);
+                const uint32_t d = tmem + col_o(t), a = tmem + col_s(t);
+                if (j > 0) tc::mma_bf16_ts_c<1>(d, a, dv, idO);
+                else tc::mma_bf16_ts_c<0>(d, a, dv, idO);
 #pragma unroll
-                for (int kk = 1; kk < BN / 16; ++kk) {
-                    const uint32_t poff = (kk >> 2) * kHalf + (kk & 3) * 32;
-                    tc::mma_bf16_c<1>(d, tc::desc_advance(dP, poff),
-                                      tc::desc_advance(dv, kk * 16 * 128), idO);
-                }
+                for (int kk = 1; kk < BN / 16; ++kk)
+                    tc::mma_bf16_ts_c<1>(d, a + kk * 8, tc::desc_advance(dv, kk * 16 * 128), idO);
                 tc::commit(bar(kODone + t));
             };
             int kt = 0, qn = 0;
@@ -680,14 +684,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 prefetch_l2(mask_row + k1);
             };
             prefetch_mask(0);
-            // the shared P buffer: the previous item's last products must be done
-            // before tile A's first P of this item lands there (tile B's first P
-            // follows tile A's first product, which follows these)
-            if (t == 0 && nkt > 0) {
-                if (pvA > 0) ok = warp_wait(bar(kODone), (pvA - 1) & 1);
-                if (ok && pvB > 0) ok = warp_wait(bar(kODone + 1), (pvB - 1) & 1);
-                if (!ok) break;
-            }
             float mrow = neg_inf();
             float2 lsum2 = make_float2(0.f, 0.f);
             for (int j = 0; j < nkt; ++j) {  // j: this item's tile count, jt the key tile
@@ -764,32 +760,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     tc::wait_st();
                 }
-                // the shared P buffer is free once the P.V that read it last is done:
-                // A(j) follows B(j-1), B(j) follows A(j) (or its own tile's previous
-                // P.V when the other tile has none there)
-                {
-                    int wt = -1, wj = -1;
-                    if (t == 0) {
-                        if (j - 1 >= 0 && j - 1 < nkB) wt = 1, wj = j - 1;
-                        else if (j > 0) wt = 0, wj = j - 1;
-                    } else {
-                        if (j < nkA) wt = 0, wj = j;
-                        else if (j > 0) wt = 1, wj = j - 1;
-                    }
-                    if (wt >= 0) {
-                        ok = warp_wait(bar(kODone + wt), ((wt == 0 ? pvA : pvB) + wj) & 1);
-                        if (!ok || aborted(abort_flag)) break;
-                    }
-                }
-                tc::fence_after_sync();
-                uint8_t* const prow = sbase + kOffP + r * 128;
-#pragma unroll
-                for (int q = 0; q < 16; ++q) {  // 8 keys per 16-byte chunk
-                    const uint4 wv = make_uint4(pw[4 * q], pw[4 * q + 1], pw[4 * q + 2], pw[4 * q + 3]);
-                    const int half = q >> 3, cq = q & 7;
-                    *reinterpret_cast<uint4*>(prow + half * kHalf + ((cq ^ (r & 7)) << 4)) = wv;
-                }
-                fence_proxy_async_smem();
+                // P over the first 64 columns of this tile's S (read above)
+                tc::st32(trow + col_s(t), *reinterpret_cast<const uint32_t(*)[32]>(pw));
+                tc::st32(trow + col_s(t) + 32, *reinterpret_cast<const uint32_t(*)[32]>(pw + 32));
+                tc::wait_st();
                 tc::fence_before_sync();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(kPFull + t));
@@ -807,18 +781,30 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tc::fence_after_sync();
                 const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+                // 32-byte stores where the output allows them (each is one
+                // whole sector of the row: half as many store requests)
+                const bool out32 = (reinterpret_cast<uintptr_t>(p.out) & 31u) == 0;
                 uint16_t* const orow = static_cast<uint16_t*>(p.out) + orow_idx * kD;
 #pragma unroll 1
                 for (int cc = 0; cc < 4; ++cc) {
                     float o[32];
                     tc::ld32(trow + col_o(t) + cc * 32, o);
                     tc::wait_ld();
-                    if (split) {
+                    if (split) {  // fp32 partial rows start on 512-byte boundaries
                         if (row_valid) {
-                            float4* const po = reinterpret_cast<float4*>(p.part_o + prow * kD + cc * 32);
+                            float* const po = p.part_o + prow * kD + cc * 32;
 #pragma unroll
-                            for (int q = 0; q < 8; ++q)
-                                po[q] = make_float4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+                            for (int q = 0; q < 4; ++q)
+                                st_global_v8(po + 8 * q, *reinterpret_cast<const uint32_t(*)[8]>(o + 8 * q));
+                        }
+                    } else if (row_valid && out32) {
+#pragma unroll
+                        for (int q = 0; q < 2; ++q) {
+                            uint32_t w8[8];
+#pragma unroll
+                            for (int e = 0; e < 8; ++e)
+                                w8[e] = pack_bf16x2(o[q * 16 + 2 * e] * inv, o[q * 16 + 2 * e + 1] * inv);
+                            st_global_v8(orow + cc * 32 + q * 16, w8);
                         }
                     } else if (row_valid) {
 #pragma unroll

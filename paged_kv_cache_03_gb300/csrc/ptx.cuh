@@ -151,6 +151,13 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return r;
 }
 
+// 256-bit global store (sm_100 and later); ptr must be 32-byte aligned.
+__device__ __forceinline__ void st_global_v8(void* ptr, const uint32_t (&w)[8]) {
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(ptr), "r"(w[0]),
+                 "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+                 : "memory");
+}
+
 // ---- warp-level tensor-core MMA (m16n8k16, bf16 in, fp32 accumulate) ------
 // Fragment layouts (lane = 4 * g + t): A (16 x 16, row-major) regs {a0..a3} =
 // rows {g, g + 8, g, g + 8} x cols {2t, 2t, 2t + 8, 2t + 8} (+1 in the high

@@ -53,6 +53,19 @@ __device__ __forceinline__ void mma_bf16_c(uint32_t d_tmem, uint64_t a_desc, uin
         : "memory");
 }
 
+// D[tmem] (+)= A[tmem] * B[smem], kind::f16, accumulate flag fixed at compile
+// time.  A (M x 16, K-major) is read from Tensor Memory: lane = row, two bf16
+// per 32-bit column, the lower K index in the low half.
+template <int kAccumulate>
+__device__ __forceinline__ void mma_bf16_ts_c(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                              uint32_t idesc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "n"(kAccumulate)
+        : "memory");
+}
+
 // Descriptor of the operand `off` bytes further on: the start address sits in
 // the low 14 bits as address / 16, and shared-memory addresses stay below
 // 256 KB, so adding off / 16 never carries out of the field.
@@ -109,8 +122,7 @@ __device__ __forceinline__ void ld32(uint32_t taddr, float (&v)[32]) {
           "=r"(r[31])
         : "r"(taddr));
 }
-__device__ __forceinline__ void st32(uint32_t taddr, const float (&v)[32]) {
-    const uint32_t* r = reinterpret_cast<const uint32_t*>(v);
+__device__ __forceinline__ void st32(uint32_t taddr, const uint32_t (&r)[32]) {
     asm volatile(
         "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
         "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
@@ -121,6 +133,9 @@ __device__ __forceinline__ void st32(uint32_t taddr, const float (&v)[32]) {
         "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
         "r"(r[29]), "r"(r[30]), "r"(r[31])
         : "memory");
+}
+__device__ __forceinline__ void st32(uint32_t taddr, const float (&v)[32]) {
+    st32(taddr, *reinterpret_cast<const uint32_t(*)[32]>(v));
 }
 __device__ __forceinline__ void wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }

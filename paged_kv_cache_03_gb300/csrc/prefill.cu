@@ -885,70 +885,86 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                     if (rem) {
+                        // the warp's 64 keys as 4 groups of 16, interleaved so
+                        // that 4 independent accumulation chains are in flight
                         const uint32_t kb = base + kOffK + s * kTile, vb = base + kOffV + s * kTile;
-#pragma unroll 1
-                        for (int grp = 0; grp < 4; ++grp) {
-                            const int kw0 = 64 * wr + 16 * grp;  // first key of the group in the tile
-                            if (j * BN + kw0 >= it.S) break;     // (uniform over the warp)
-                            float sacc[4] = {0.f, 0.f, 0.f, 0.f};
-                            {
-                                const int r = kw0 + (lane & 7) + ((lane >> 3) & 1) * 8;
+                        const int kw0 = 64 * wr;  // first key of the warp in the tile
+                        float sacc[4][4];
 #pragma unroll
-                                for (int ks = 0; ks < 8; ++ks) {
-                                    const int cq = ks * 2 + (lane >> 4);
-                                    uint32_t a[4];
-                                    ldmatrix_x4(a, kb + (cq >> 3) * kHalf + r * 128 + (((cq & 7) ^ (r & 7)) << 4));
-                                    mma_16816(sacc, a, qf[ks][0], qf[ks][1]);
+                        for (int grp = 0; grp < 4; ++grp)
+                            sacc[grp][0] = sacc[grp][1] = sacc[grp][2] = sacc[grp][3] = 0.f;
+                        {
+                            const int r0 = kw0 + (lane & 7) + ((lane >> 3) & 1) * 8;
+#pragma unroll
+                            for (int ks = 0; ks < 8; ++ks) {
+                                const int cq = ks * 2 + (lane >> 4);
+                                uint32_t a[4][4];
+#pragma unroll
+                                for (int grp = 0; grp < 4; ++grp) {
+                                    const int r = r0 + 16 * grp;
+                                    ldmatrix_x4(a[grp], kb + (cq >> 3) * kHalf + r * 128 + (((cq & 7) ^ (r & 7)) << 4));
                                 }
+#pragma unroll
+                                for (int grp = 0; grp < 4; ++grp) mma_16816(sacc[grp], a[grp], qf[ks][0], qf[ks][1]);
                             }
-                            float x[4];
+                        }
+                        // scores in log2 units, masked past each row's last key;
+                        // one max over the 64 keys per row
+                        float mt0 = neg_inf(), mt1 = neg_inf();
+#pragma unroll
+                        for (int grp = 0; grp < 4; ++grp)
 #pragma unroll
                             for (int e = 0; e < 4; ++e) {
-                                const int key = j * BN + kw0 + g + (e >> 1) * 8;
-                                x[e] = key <= lim_r[e & 1] ? sacc[e] * c : neg_inf();
+                                const int key = j * BN + kw0 + 16 * grp + g + (e >> 1) * 8;
+                                sacc[grp][e] = key <= lim_r[e & 1] ? sacc[grp][e] * c : neg_inf();
+                                if (e & 1) mt1 = fmaxf(mt1, sacc[grp][e]);
+                                else mt0 = fmaxf(mt0, sacc[grp][e]);
                             }
-                            float mt0 = fmaxf(x[0], x[2]), mt1 = fmaxf(x[1], x[3]);
 #pragma unroll
-                            for (int o = 4; o < 32; o <<= 1) {
-                                mt0 = fmaxf(mt0, __shfl_xor_sync(0xffffffffu, mt0, o));
-                                mt1 = fmaxf(mt1, __shfl_xor_sync(0xffffffffu, mt1, o));
-                            }
-                            const bool gr0 = mt0 > m_r[0] + kLazyRescaleLog2;
-                            const bool gr1 = mt1 > m_r[1] + kLazyRescaleLog2;
-                            if (__any_sync(0xffffffffu, gr0 || gr1)) {
-                                const float a0 = gr0 ? fast_exp2(m_r[0] - mt0) : 1.f;
-                                const float a1 = gr1 ? fast_exp2(m_r[1] - mt1) : 1.f;
-                                if (gr0) m_r[0] = mt0;
-                                if (gr1) m_r[1] = mt1;
-                                l_r[0] *= a0;
-                                l_r[1] *= a1;
+                        for (int o = 4; o < 32; o <<= 1) {
+                            mt0 = fmaxf(mt0, __shfl_xor_sync(0xffffffffu, mt0, o));
+                            mt1 = fmaxf(mt1, __shfl_xor_sync(0xffffffffu, mt1, o));
+                        }
+                        const bool gr0 = mt0 > m_r[0] + kLazyRescaleLog2;
+                        const bool gr1 = mt1 > m_r[1] + kLazyRescaleLog2;
+                        if (__any_sync(0xffffffffu, gr0 || gr1)) {
+                            const float a0 = gr0 ? fast_exp2(m_r[0] - mt0) : 1.f;
+                            const float a1 = gr1 ? fast_exp2(m_r[1] - mt1) : 1.f;
+                            if (gr0) m_r[0] = mt0;
+                            if (gr1) m_r[1] = mt1;
+                            l_r[0] *= a0;
+                            l_r[1] *= a1;
 #pragma unroll
-                                for (int mt = 0; mt < 8; ++mt) {
-                                    oacc[mt][0] *= a0;
-                                    oacc[mt][1] *= a1;
-                                    oacc[mt][2] *= a0;
-                                    oacc[mt][3] *= a1;
-                                }
+                            for (int mt = 0; mt < 8; ++mt) {
+                                oacc[mt][0] *= a0;
+                                oacc[mt][1] *= a1;
+                                oacc[mt][2] *= a0;
+                                oacc[mt][3] *= a1;
                             }
-                            const float mu0 = m_r[0] == neg_inf() ? 0.f : m_r[0];
-                            const float mu1 = m_r[1] == neg_inf() ? 0.f : m_r[1];
-                            const uint32_t X0 = pack_bf16x2(fast_exp2(x[0] - mu0), fast_exp2(x[1] - mu1));
-                            const uint32_t X1 = pack_bf16x2(fast_exp2(x[2] - mu0), fast_exp2(x[3] - mu1));
-                            {
-                                const float2 f0 = bf16x2_to_float2(X0), f1 = bf16x2_to_float2(X1);
-                                l_r[0] += f0.x + f1.x;
-                                l_r[1] += f0.y + f1.y;
-                            }
-                            const uint32_t pb0 = movmatrix_trans(X0), pb1 = movmatrix_trans(X1);
-                            {
-                                const int r = kw0 + (lane & 7) + (lane >> 4) * 8;
+                        }
+                        const float mu0 = m_r[0] == neg_inf() ? 0.f : m_r[0];
+                        const float mu1 = m_r[1] == neg_inf() ? 0.f : m_r[1];
+                        uint32_t pb[4][2];  // P^T fragments (B operand) per group
 #pragma unroll
-                                for (int mt = 0; mt < 8; ++mt) {
-                                    const int cq = mt * 2 + ((lane >> 3) & 1);
-                                    uint32_t a[4];
-                                    ldmatrix_x4_trans(a, vb + (cq >> 3) * kHalf + r * 128 + (((cq & 7) ^ (r & 7)) << 4));
-                                    mma_16816(oacc[mt], a, pb0, pb1);
-                                }
+                        for (int grp = 0; grp < 4; ++grp) {
+                            const uint32_t X0 = pack_bf16x2(fast_exp2(sacc[grp][0] - mu0), fast_exp2(sacc[grp][1] - mu1));
+                            const uint32_t X1 = pack_bf16x2(fast_exp2(sacc[grp][2] - mu0), fast_exp2(sacc[grp][3] - mu1));
+                            const float2 f0 = bf16x2_to_float2(X0), f1 = bf16x2_to_float2(X1);
+                            l_r[0] += f0.x + f1.x;
+                            l_r[1] += f0.y + f1.y;
+                            pb[grp][0] = movmatrix_trans(X0);
+                            pb[grp][1] = movmatrix_trans(X1);
+                        }
+                        // O^T += V^T P^T: consecutive products go to different dims
+#pragma unroll
+                        for (int grp = 0; grp < 4; ++grp) {
+                            const int r = kw0 + 16 * grp + (lane & 7) + (lane >> 4) * 8;
+#pragma unroll
+                            for (int mt = 0; mt < 8; ++mt) {
+                                const int cq = mt * 2 + ((lane >> 3) & 1);
+                                uint32_t a[4];
+                                ldmatrix_x4_trans(a, vb + (cq >> 3) * kHalf + r * 128 + (((cq & 7) ^ (r & 7)) << 4));
+                                mma_16816(oacc[mt], a, pb[grp][0], pb[grp][1]);
                             }
                         }
                     }

@@ -75,7 +75,11 @@ constexpr int kTile = 2 * kHalf;  // 128 rows x 128 bf16
 constexpr int kOffQ = 0;                    // tile t at kOffQ + t * kTile
 constexpr int kOffK = kOffQ + 2 * kTile;    // slot s at kOffK + s * kTile
 constexpr int kOffV = kOffK + 2 * kTile;    // slot s at kOffV + s * kTile
-constexpr int kOffBar = kOffV + 2 * kTile;
+// Output staging for the tiled stores of the epilogue: 16 rows x 256 bytes
+// per warp (two 64-dim halves, 128-byte swizzled), tile t at + t * 16 KB.
+constexpr int kOffStage = kOffV + 2 * kTile;
+constexpr int kStageRows = 16;
+constexpr int kOffBar = kOffStage + 2 * 4 * kStageRows * 256;
 enum Bar {
     kQFull = 0,
     kKFull = 1,   // + slot
@@ -318,7 +322,8 @@ template <bool kMask, bool kVarlen, bool kSplit>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tile_kernel(const __grid_constant__ CUtensorMap tm_q,
                         const __grid_constant__ CUtensorMap tm_k,
-                        const __grid_constant__ CUtensorMap tm_v, const PrefillParams p) {
+                        const __grid_constant__ CUtensorMap tm_v,
+                        const __grid_constant__ CUtensorMap tm_o, const PrefillParams p) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -781,40 +786,76 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tc::fence_after_sync();
                 const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
-                // 32-byte stores where the output allows them (each is one
-                // whole sector of the row: half as many store requests)
-                const bool out32 = (reinterpret_cast<uintptr_t>(p.out) & 31u) == 0;
-                uint16_t* const orow = static_cast<uint16_t*>(p.out) + orow_idx * kD;
+                if constexpr (split) {
+                    // fp32 partial rows (512-byte aligned), 256-bit stores
 #pragma unroll 1
-                for (int cc = 0; cc < 4; ++cc) {
-                    float o[32];
-                    tc::ld32(trow + col_o(t) + cc * 32, o);
-                    tc::wait_ld();
-                    if (split) {  // fp32 partial rows start on 512-byte boundaries
+                    for (int cc = 0; cc < 4; ++cc) {
+                        float o[32];
+                        tc::ld32(trow + col_o(t) + cc * 32, o);
+                        tc::wait_ld();
                         if (row_valid) {
                             float* const po = p.part_o + prow * kD + cc * 32;
 #pragma unroll
                             for (int q = 0; q < 4; ++q)
                                 st_global_v8(po + 8 * q, *reinterpret_cast<const uint32_t(*)[8]>(o + 8 * q));
                         }
-                    } else if (row_valid && out32) {
-#pragma unroll
-                        for (int q = 0; q < 2; ++q) {
-                            uint32_t w8[8];
-#pragma unroll
-                            for (int e = 0; e < 8; ++e)
-                                w8[e] = pack_bf16x2(o[q * 16 + 2 * e] * inv, o[q * 16 + 2 * e + 1] * inv);
-                            st_global_v8(orow + cc * 32 + q * 16, w8);
+                    }
+                } else {
+                    // O/l as bf16: each warp's rows go out 16 at a time through
+                    // its staging slice and one tiled store per 64-dim half
+                    // (rows of one head, consecutive positions, all valid);
+                    // other rows are stored directly
+                    const uint32_t stage = base + kOffStage + (t * 4 + q4) * (kStageRows * 256);
+                    uint16_t* const orow = static_cast<uint16_t*>(p.out) + orow_idx * kD;
+#pragma unroll 1
+                    for (int rd = 0; rd < 2; ++rd) {
+                        const bool mine = (lane >> 4) == rd;
+                        // (a ragged batch's short chunks gained nothing from it: measured)
+                        const bool tiled = !kVarlen && p.Lt % kStageRows == 0 &&
+                                           __all_sync(0xffffffffu, !mine || row_valid);
+                        if (tiled) {
+                            if (lane == 0) tc::bulk_wait_read();  // the slice's last stores
+                            __syncwarp();
                         }
-                    } else if (row_valid) {
+                        const int rr = lane & 15;
+#pragma unroll 1
+                        for (int cc = 0; cc < 4; ++cc) {
+                            float o[32];
+                            tc::ld32(trow + col_o(t) + cc * 32, o);
+                            tc::wait_ld();
+                            if (!mine || !row_valid) continue;
 #pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            const uint4 wv = make_uint4(
-                                pack_bf16x2(o[q * 8 + 0] * inv, o[q * 8 + 1] * inv),
-                                pack_bf16x2(o[q * 8 + 2] * inv, o[q * 8 + 3] * inv),
-                                pack_bf16x2(o[q * 8 + 4] * inv, o[q * 8 + 5] * inv),
-                                pack_bf16x2(o[q * 8 + 6] * inv, o[q * 8 + 7] * inv));
-                            *reinterpret_cast<uint4*>(orow + cc * 32 + q * 8) = wv;
+                            for (int q = 0; q < 4; ++q) {
+                                const int e = q * 8;
+                                const uint4 wv = make_uint4(pack_bf16x2(o[e + 0] * inv, o[e + 1] * inv),
+                                                            pack_bf16x2(o[e + 2] * inv, o[e + 3] * inv),
+                                                            pack_bf16x2(o[e + 4] * inv, o[e + 5] * inv),
+                                                            pack_bf16x2(o[e + 6] * inv, o[e + 7] * inv));
+                                if (tiled) {
+                                    const int qq = cc * 4 + q;  // 16-byte chunk of the row
+                                    const uint32_t a = stage + (qq >> 3) * (kStageRows * 128) + rr * 128 +
+                                                       (((qq & 7) ^ (rr & 7)) << 4);
+                                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a),
+                                                 "r"(wv.x), "r"(wv.y), "r"(wv.z), "r"(wv.w)
+                                                 : "memory");
+                                } else {
+                                    *reinterpret_cast<uint4*>(orow + cc * 32 + e) = wv;
+                                }
+                            }
+                        }
+                        if (tiled) {
+                            fence_proxy_async_smem();
+                            __syncwarp();
+                            const int src = 16 * rd;  // the round's first row
+                            {
+                                const int row0 = static_cast<int>(
+                                    __shfl_sync(0xffffffffu, static_cast<unsigned long long>(orow_idx), src));
+                                if (lane == 0) {
+                                    tc::tma_store_2d(&tm_o, stage, 0, row0);
+                                    tc::tma_store_2d(&tm_o, stage + kStageRows * 128, 64, row0);
+                                    tc::bulk_commit();
+                                }
+                            }
                         }
                     }
                 }
@@ -832,6 +873,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             pvB += nkB;
         }
         if (!ok && lane == 0) give_up(p, abort_flag);
+        if (lane == 0) tc::bulk_wait_all();  // the output stores have landed
     } else if (kSplit && (warp == 2 || warp == 3)) {
         // ====================== remainder rows (warps 2, 3) =====================
         // S^T = K Q^T and O^T += V^T P^T with mma m16n8k16 (16 keys x 8 rows):
@@ -1236,11 +1278,15 @@ pa_status prefill_launch(const Call& c) {
     const int G = sh.H_q / sh.H_kv;
     const int Lt = BM / G;
     const int box_rows = gcd_int(sh.page_size, BN);
-    CUtensorMap tq, tk, tv;
+    CUtensorMap tq, tk, tv, to;
     const long long pool_rows = static_cast<long long>(sh.num_pages) * sh.H_kv * sh.page_size;
     const bool q_ok = c.cu_q ? make_map_tokens(&tq, c.q, sh.H_q, c.total_q, Lt)
                              : make_map(&tq, c.q, static_cast<long long>(sh.B) * sh.H_q * sh.L, Lt);
-    if (!q_ok || !make_map(&tk, c.kp, pool_rows, box_rows) ||
+    // the output in boxes of 16 rows, for the epilogue's tiled stores (the
+    // ragged batch's instance stores rows directly and never reads it)
+    const bool o_ok = c.cu_q ? (to = tq, true)
+                             : make_map(&to, c.out, static_cast<long long>(sh.B) * sh.H_q * sh.L, kStageRows);
+    if (!q_ok || !o_ok || !make_map(&tk, c.kp, pool_rows, box_rows) ||
         !make_map(&tv, c.vp, pool_rows, box_rows))
         return PA_ERR_CUDA;
 
@@ -1336,13 +1382,13 @@ pa_status prefill_launch(const Call& c) {
     const unsigned grid = static_cast<unsigned>(std::min<long long>(items, c.dev.sm_count));
     if (c.ev_before && cudaEventRecord(c.ev_before, c.stream) != cudaSuccess) return PA_ERR_CUDA;
     if (c.cu_q)  // (a ragged batch takes no explicit mask)
-        prefill_tile_kernel<false, true, false><<<grid, kThreads, kSmemBytes, c.stream>>>(tq, tk, tv, p);
+        prefill_tile_kernel<false, true, false><<<grid, kThreads, kSmemBytes, c.stream>>>(tq, tk, tv, to, p);
     else if (c.mask)
-        prefill_tile_kernel<true, false, false><<<grid, kThreads, kSmemBytes, c.stream>>>(tq, tk, tv, p);
+        prefill_tile_kernel<true, false, false><<<grid, kThreads, kSmemBytes, c.stream>>>(tq, tk, tv, to, p);
     else if (split)
-        prefill_tile_kernel<false, false, true><<<grid, kThreads, kSmemBytes, c.stream>>>(tq, tk, tv, p);
+        prefill_tile_kernel<false, false, true><<<grid, kThreads, kSmemBytes, c.stream>>>(tq, tk, tv, to, p);
     else
-        prefill_tile_kernel<false, false, false><<<grid, kThreads, kSmemBytes, c.stream>>>(tq, tk, tv, p);
+        prefill_tile_kernel<false, false, false><<<grid, kThreads, kSmemBytes, c.stream>>>(tq, tk, tv, to, p);
     if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
     if (c.ev_after && cudaEventRecord(c.ev_after, c.stream) != cudaSuccess) return PA_ERR_CUDA;
     if (split) {  // merge the key chunks (may launch while the tiles finish)

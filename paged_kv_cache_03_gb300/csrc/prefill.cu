@@ -80,6 +80,23 @@ constexpr int kOffV = kOffK + 2 * kTile;    // slot s at kOffV + s * kTile
 constexpr int kOffStage = kOffV + 2 * kTile;
 constexpr int kStageRows = 16;
 constexpr int kOffBar = kOffStage + 2 * 4 * kStageRows * 256;
+// With an explicit mask the kernel keeps one K slot and stages the mask in
+// two 32 KB slots instead: the second K slot and the output staging (whose
+// rows that instance stores directly).  A slot holds 64 keys x 128 rows of
+// fp32 as two 32-key column blocks of 16 KB, each G boxes of Lt rows x 128
+// bytes, 128-byte swizzled.
+constexpr int kOffMask0 = kOffK + kTile;
+constexpr int kOffMask1 = kOffStage;
+constexpr int kMaskHalf = 64;  // keys per mask slot
+// K/V ring positions: with a mask K has one slot, else two
+template <bool kMask>
+struct KRing {
+    static constexpr int kSlots = kMask ? 1 : 2;
+    __device__ static int slot(int g) { return kMask ? 0 : (g & 1); }
+    __device__ static uint32_t full_parity(int g) { return kMask ? (g & 1) : ((g >> 1) & 1); }
+    // the wait for the slot to be free before tile g is loaded into it
+    __device__ static uint32_t empty_parity(int g) { return kMask ? ((g - 1) & 1) : (((g >> 1) - 1) & 1); }
+};
 enum Bar {
     kQFull = 0,
     kKFull = 1,   // + slot
@@ -95,7 +112,12 @@ enum Bar {
     kOFree = 18,      // + tile: the item's epilogue has read O
     kItemFull = 20,   // + slot: a work item is published
     kItemEmpty = 22,  // + slot: every role has read it
-    kNumBars = 24     // (even: what follows stays 16-byte aligned)
+    // A slot's fills alternate between the query tiles, so each tile waits on
+    // a full barrier of its own: it then waits for that barrier's phases in
+    // order, never for one two phases ahead of the barrier.
+    kMaskFull = 24,   // + 2 * tile + slot: the tile's mask half-tile is staged
+    kMaskEmpty = 28,  // + slot: the half-tile in the slot has been read
+    kNumBars = 30     // (even: what follows stays 16-byte aligned)
 };
 constexpr int kOffItems = kOffBar + kNumBars * 8;  // 2 slots x 32 bytes
 constexpr int kOffTmemSlot = kOffItems + 64;
@@ -307,6 +329,12 @@ __device__ __forceinline__ ItemWork item_work(const PrefillParams& p, const Item
     return w;
 }
 
+// The last key any row of the query tile starting at position l0 sees.
+__device__ __forceinline__ int tile_last_key(const PrefillParams& p, const Item& it, int l0) {
+    const int l_last = min(l0 + p.Lt, it.Lb) - 1;
+    return min(p.causal ? l_last + it.S - it.Lb : it.S - 1, it.S - 1);
+}
+
 // kMask: an explicit additive mask is read; kVarlen: a ragged batch (queries
 // packed by token, per-sequence query counts); kSplit: the keys of each pair
 // are cut into p.nsplit chunks that write fp32 partials.  Separate
@@ -323,7 +351,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefill_tile_kernel(const __grid_constant__ CUtensorMap tm_q,
                         const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_v,
-                        const __grid_constant__ CUtensorMap tm_o, const PrefillParams p) {
+                        const __grid_constant__ CUtensorMap tm_o,
+                        const __grid_constant__ CUtensorMap tm_m, const PrefillParams p) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -351,8 +380,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(bar(kVFull + s), 1);
             mbar_init(bar(kVEmpty + s), (kSplit && p.nrem > 0) ? 3 : 1);
             mbar_init(bar(kItemFull + s), 1);
-            // the MMA thread + 8 softmax warps (+ warps 2 and 3 for remainder rows)
-            mbar_init(bar(kItemEmpty + s), (kSplit && p.nrem > 0) ? 11 : 9);
+            // the MMA thread + 8 softmax warps (+ warps 2 and 3 for remainder
+            // rows, + warp 2 that stages the mask)
+            mbar_init(bar(kItemEmpty + s), (kSplit && p.nrem > 0) ? 11 : kMask ? 10 : 9);
+            mbar_init(bar(kMaskFull + s), 1);
+            mbar_init(bar(kMaskFull + 2 + s), 1);
+            mbar_init(bar(kMaskEmpty + s), 4);
         }
         mbar_init(bar(kMmaDone), 1);
         mbar_init(bar(kVTail), 1);
@@ -385,6 +418,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int4 a = item_slot[2 * (k & 1)], c = item_slot[2 * (k & 1) + 1];
         return Item{a.x, a.y, a.z, a.w, c.x, c.y, c.z, c.w & 1, c.w >> 1};
     };
+    using KR = KRing<kMask>;
     auto take_item = [&](int k, Item& it) -> bool {  // a whole warp
         if (!warp_wait(bar(kItemFull + (k & 1)), (k >> 1) & 1)) return false;
         it = read_item(k);
@@ -463,8 +497,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             tile_boxes(p, it.b, it.kvh, it.S, w.j0, lane, rows_cur, bytes_cur);
             for (int jj = 0; jj < w.nkc; ++jj) {
                 const int j = w.j0 + jj;  // key tile
-                const int gk = kt + jj, s = gk & 1;
-                if (gk >= 2 && !warp_wait(bar(kKEmpty + s), ((gk >> 1) - 1) & 1)) {
+                const int gk = kt + jj, s = gk & 1, ks = KR::slot(gk);
+                if (gk >= KR::kSlots && !warp_wait(bar(kKEmpty + ks), KR::empty_parity(gk))) {
                     if (lane == 0) give_up(p, abort_flag);
                     ok = false;
                     break;
@@ -473,10 +507,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ok = false;
                     break;
                 }
-                if (lane == 0) mbar_arrive_expect_tx(bar(kKFull + s), bytes_cur);
+                if (lane == 0) mbar_arrive_expect_tx(bar(kKFull + ks), bytes_cur);
                 __syncwarp();
-                issue_boxes(&tm_k, base + kOffK + s * kTile, rows_cur, lane, p.box_rows,
-                            bar(kKFull + s), pol_kv);
+                issue_boxes(&tm_k, base + kOffK + ks * kTile, rows_cur, lane, p.box_rows,
+                            bar(kKFull + ks), pol_kv);
                 kdone = gk + 1;
                 if (gk >= 2 && !warp_wait(bar(kVEmpty + s), ((gk >> 1) - 1) & 1)) {
                     if (lane == 0) give_up(p, abort_flag);
@@ -520,8 +554,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // let every copy into this CTA's shared memory land before leaving
         if (qn > 0 && !mbar_wait(bar(kQFull), (qn - 1) & 1)) give_up(p, abort_flag);
-        for (int g = max(0, kdone - 2); g < kdone; ++g)
-            if (!mbar_wait(bar(kKFull + (g & 1)), (g >> 1) & 1)) give_up(p, abort_flag);
+        for (int g = max(0, kdone - KR::kSlots); g < kdone; ++g)
+            if (!mbar_wait(bar(kKFull + KR::slot(g)), KR::full_parity(g))) give_up(p, abort_flag);
         for (int g = max(0, vdone - 2); g < vdone; ++g)
             if (!mbar_wait(bar(kVFull + (g & 1)), (g >> 1) & 1)) give_up(p, abort_flag);
         // the last CTA to stop claiming resets the counters for the next call
@@ -547,7 +581,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t dV0 = tc::smem_desc_sw128(base + kOffV, kHalf, 1024);
             const uint64_t dV1 = tc::smem_desc_sw128(base + kOffV + kTile, kHalf, 1024);
             auto qk = [&](int t, int gk) {
-                const uint64_t dq = t ? dQ1 : dQ0, dk = (gk & 1) ? dK1 : dK0;
+                const uint64_t dq = t ? dQ1 : dQ0, dk = KR::slot(gk) ? dK1 : dK0;
                 const uint32_t d = tmem + col_s(t);
                 tc::mma_bf16_c<0>(d, dq, dk, idS);
 #pragma unroll
@@ -586,12 +620,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (w.nkc == 0) continue;
                 const int* nk_t = w.nkc_t;  // this item's tiles (j counts from its first)
                 const int nk = w.nkc;
-                ok = mbar_wait(bar(kQFull), qn & 1) && mbar_wait(bar(kKFull + (kt & 1)), (kt >> 1) & 1);
+                ok = mbar_wait(bar(kQFull), qn & 1) && mbar_wait(bar(kKFull + KR::slot(kt)), KR::full_parity(kt));
                 if (!ok || *abort_flag) break;
                 tc::fence_after_sync();
                 if (nk_t[0] > 0) qk(0, kt);
                 if (nk_t[1] > 0) qk(1, kt);
-                tc::commit(bar(kKEmpty + (kt & 1)));
+                tc::commit(bar(kKEmpty + KR::slot(kt)));
                 if (nk == 1) tc::commit(bar(kQEmpty));  // all of the item's Q.K^T issued
                 for (int j = 0; ok && j < nk; ++j) {
                     const int gk = kt + j;
@@ -609,7 +643,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         pv(0, j, gk);
                     }
                     if (more) {
-                        ok = mbar_wait(bar(kKFull + ((gk + 1) & 1)), ((gk + 1) >> 1) & 1);
+                        ok = mbar_wait(bar(kKFull + KR::slot(gk + 1)), KR::full_parity(gk + 1));
                         if (!ok || *abort_flag) break;
                         tc::fence_after_sync();
                         if (j + 1 < nk_t[0]) qk(0, gk + 1);
@@ -626,7 +660,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tc::commit(bar(kVEmpty + (gk & 1)));
                     if (more) {
                         if (j + 1 < nk_t[1]) qk(1, gk + 1);
-                        tc::commit(bar(kKEmpty + ((gk + 1) & 1)));
+                        tc::commit(bar(kKEmpty + KR::slot(gk + 1)));
                         if (j + 2 == nk) tc::commit(bar(kQEmpty));  // the item's last Q.K^T
                     }
                 }
@@ -653,6 +687,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float cs = kMask ? 1.f : c;
         int sc = 0;               // S fills of this tile consumed (kSFull phases)
         int pvA = 0, pvB = 0;     // P.V products of tiles A and B in earlier items (kODone phases)
+        int mask_steps = 0;       // this tile's mask key tiles in earlier items
         bool ok = true;
         Item it;
         for (int k = 0; ok; ++k) {
@@ -672,28 +707,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             const long long orow_idx =
                 kVarlen ? (static_cast<long long>(it.q0 + l) * p.H_q + h)
                         : ((static_cast<long long>(it.b) * p.H_q + h) * p.L + l);
-            const float* const mask_row =
-                kMask && row_valid
-                    ? p.mask + ((static_cast<long long>(it.b) * p.H_q + h) * p.L + l) * p.mask_S
-                    : nullptr;
-            // the lines holding this row's visible mask entries of key tile jj go
-            // to L2 ahead of use: keys [jj * BN, min(jj * BN + BN, lim + 1)), all
-            // inside the row (lim < S <= mask_S)
-            auto prefetch_mask = [&](int jj) {  // (no key split with a mask: j0 = 0)
-                if (!kMask || !mask_row || jj >= nkt) return;
-                const int k0 = jj * BN;
-                if (k0 > lim) return;
-                const int k1 = min(k0 + BN, lim + 1) - 1;  // last visible key of the tile
-#pragma unroll
-                for (int e = 0; e < 4; ++e) prefetch_l2(mask_row + min(k0 + 32 * e, k1));
-                prefetch_l2(mask_row + k1);
-            };
-            prefetch_mask(0);
+            // the last key any row of this tile sees: mask columns past it are
+            // not staged (no key split with a mask: j0 = 0)
+            const int lim_tile = tile_last_key(p, it, t == 0 ? w.l0_t[0] : w.l0_t[1]);
             float mrow = neg_inf();
             float2 lsum2 = make_float2(0.f, 0.f);
             for (int j = 0; j < nkt; ++j) {  // j: this item's tile count, jt the key tile
                 const int jt = w.j0 + j;
-                prefetch_mask(j + 1);
                 ok = warp_wait(bar(kSFull + t), (sc + j) & 1);
                 if (!ok || aborted(abort_flag)) break;
                 tc::fence_after_sync();
@@ -702,19 +722,35 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int cc = 0; cc < 4; ++cc) tc::ld32(trow + col_s(t) + cc * 32, x[cc]);
                 tc::wait_ld();
                 if constexpr (kMask) {  // s * scale * log2 e + mask * log2 e
-                    // only the words holding a visible key (k0 + 4q <= lim < mask_S)
-                    const int k0 = jt * BN;
+                    // the tile's mask, two staged halves of 64 keys (half h in
+                    // slot h), the tile's (mask_steps + j)-th fill of each slot
 #pragma unroll
-                    for (int q = 0; q < 32; ++q) {
-                        float4 mv = make_float4(0.f, 0.f, 0.f, 0.f);
-                        if (mask_row && k0 + 4 * q <= lim)
-                            mv = __ldg(reinterpret_cast<const float4*>(mask_row + k0) + q);
-                        const int cc = q >> 3, e = (q & 7) * 4;
-                        x[cc][e + 0] = fmaf(x[cc][e + 0], c, mv.x * 1.4426950408889634f);
-                        x[cc][e + 1] = fmaf(x[cc][e + 1], c, mv.y * 1.4426950408889634f);
-                        x[cc][e + 2] = fmaf(x[cc][e + 2], c, mv.z * 1.4426950408889634f);
-                        x[cc][e + 3] = fmaf(x[cc][e + 3], c, mv.w * 1.4426950408889634f);
+                    for (int hh = 0; hh < 2; ++hh) {
+                        const int ms = hh;
+                        ok = warp_wait(bar(kMaskFull + 2 * t + ms), (mask_steps + j) & 1);
+                        if (!ok) break;
+                        const uint32_t sb = base + (ms ? kOffMask1 : kOffMask0);
+#pragma unroll
+                        for (int cb = 0; cb < 2; ++cb) {
+                            const int cc = 2 * hh + cb;
+                            if (jt * BN + 32 * cc > lim_tile) continue;  // not staged: masked below
+#pragma unroll
+                            for (int q = 0; q < 8; ++q) {
+                                float4 mv;
+                                asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                                             : "=f"(mv.x), "=f"(mv.y), "=f"(mv.z), "=f"(mv.w)
+                                             : "r"(sb + cb * (BM * 128) + r * 128 + ((q ^ (r & 7)) << 4)));
+                                const int e = 4 * q;
+                                x[cc][e + 0] = fmaf(x[cc][e + 0], c, mv.x * 1.4426950408889634f);
+                                x[cc][e + 1] = fmaf(x[cc][e + 1], c, mv.y * 1.4426950408889634f);
+                                x[cc][e + 2] = fmaf(x[cc][e + 2], c, mv.z * 1.4426950408889634f);
+                                x[cc][e + 3] = fmaf(x[cc][e + 3], c, mv.w * 1.4426950408889634f);
+                            }
+                        }
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(bar(kMaskEmpty + ms));
                     }
+                    if (!ok) break;
                 }
                 // causal / length mask (frontier tiles only), row max of raw scores
                 const bool masking = jt * BN + BN - 1 > lim_min;  // uniform over the CTA
@@ -811,7 +847,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int rd = 0; rd < 2; ++rd) {
                         const bool mine = (lane >> 4) == rd;
                         // (a ragged batch's short chunks gained nothing from it: measured)
-                        const bool tiled = !kVarlen && p.Lt % kStageRows == 0 &&
+                        const bool tiled = !kVarlen && !kMask && p.Lt % kStageRows == 0 &&
                                            __all_sync(0xffffffffu, !mine || row_valid);
                         if (tiled) {
                             if (lane == 0) tc::bulk_wait_read();  // the slice's last stores
@@ -871,9 +907,73 @@ __global__ void __launch_bounds__(kThreads, 1)
             sc += nkt;
             pvA += nkA;
             pvB += nkB;
+            mask_steps += nkt;
         }
         if (!ok && lane == 0) give_up(p, abort_flag);
         if (lane == 0) tc::bulk_wait_all();  // the output stores have landed
+    } else if (kMask && warp == 2) {
+        // ====================== mask stager (warp 2, with a mask) ===================
+        // Per key tile and query tile (A, then B), two half-tiles of 64 keys
+        // into the two mask slots in turn: per 32-key column block with a
+        // visible key, G boxes (one per head) of Lt rows.  The next key
+        // tile's boxes are prefetched into L2 meanwhile.
+        const uint64_t pol_m = l2_policy_evict_first();
+        if (lane == 0) tc::prefetch_tensormap(&tm_m);
+        int n = 0;               // half-tiles staged
+        int fills[2] = {0, 0};   // key tiles staged per query tile
+        bool ok = true;
+        Item it;
+        auto row_of = [&](const ItemWork& w, int t, int g) {
+            return ((it.b * p.H_q) + it.kvh * p.G + g) * p.L + w.l0_t[t];
+        };
+        for (int k = 0; ok; ++k) {
+            ok = take_item(k, it);
+            if (!ok || !it.live) break;
+            const ItemWork w = item_work<kSplit>(p, it);
+            const int lim_t[2] = {tile_last_key(p, it, w.l0_t[0]), tile_last_key(p, it, w.l0_t[1])};
+            for (int j = 0; ok && j < w.nkc; ++j) {
+                for (int t = 0; t < 2 && ok; ++t) {
+                    if (j >= w.nkc_t[t]) continue;
+                    const int k0 = (w.j0 + j) * BN;
+                    if (lane == 0 && j + 1 < w.nkc_t[t])  // the next key tile, into L2
+                        for (int cb = 0; cb < 4; ++cb)
+                            if (k0 + BN + 32 * cb <= lim_t[t])
+                                for (int g = 0; g < p.G; ++g)
+                                    tc::tma_prefetch_2d(&tm_m, k0 + BN + 32 * cb, row_of(w, t, g));
+                    for (int hh = 0; hh < 2; ++hh) {
+                        const int ms = n & 1;  // (= hh: every key tile stages two halves)
+                        if (n >= 2 && !warp_wait(bar(kMaskEmpty + ms), ((n >> 1) - 1) & 1)) {
+                            ok = false;
+                            break;
+                        }
+                        if (aborted(abort_flag)) {
+                            ok = false;
+                            break;
+                        }
+                        int nb = 0;  // column blocks with a visible key
+                        for (int cb = 0; cb < 2; ++cb) nb += (k0 + kMaskHalf * hh + 32 * cb <= lim_t[t]);
+                        if (lane == 0) {
+                            const uint32_t sb = base + (ms ? kOffMask1 : kOffMask0);
+                            const uint32_t full = bar(kMaskFull + 2 * t + ms);
+                            mbar_arrive_expect_tx(full, static_cast<uint32_t>(nb * BM * 128));
+                            for (int cb = 0; cb < nb; ++cb)
+                                for (int g = 0; g < p.G; ++g)
+                                    tc::tma_load_2d(sb + cb * (BM * 128) + g * p.Lt * 128, &tm_m,
+                                                    k0 + kMaskHalf * hh + 32 * cb, row_of(w, t, g),
+                                                    full, pol_m);
+                        }
+                        __syncwarp();
+                        ++n;
+                    }
+                    if (ok) ++fills[t];
+                }
+            }
+        }
+        if (!ok && lane == 0) give_up(p, abort_flag);
+        // let the staged copies land before leaving
+        for (int t = 0; t < 2; ++t)
+            for (int hh = 0; hh < 2 && fills[t] > 0; ++hh)
+                if (!mbar_wait(bar(kMaskFull + 2 * t + hh), (fills[t] - 1) & 1)) give_up(p, abort_flag);
     } else if (kSplit && (warp == 2 || warp == 3)) {
         // ====================== remainder rows (warps 2, 3) =====================
         // S^T = K Q^T and O^T += V^T P^T with mma m16n8k16 (16 keys x 8 rows):
@@ -1211,6 +1311,20 @@ bool make_map_tokens(CUtensorMap* map, const void* ptr, int H_q, long long token
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// fp32 mask map: rows x cols (cols a multiple of 4), boxes of 32 columns x
+// box_rows rows, 128-byte swizzle; columns past cols read as zero.
+bool make_map_mask(CUtensorMap* map, const float* ptr, long long rows, long long cols, int box_rows) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 4};
+    cuuint32_t box[2] = {32u, static_cast<cuuint32_t>(box_rows)};
+    cuuint32_t estr[2] = {1u, 1u};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(ptr), dims, strides, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 int gcd_int(int a, int b) {
     while (b) {
         const int t = a % b;
@@ -1278,7 +1392,7 @@ pa_status prefill_launch(const Call& c) {
     const int G = sh.H_q / sh.H_kv;
     const int Lt = BM / G;
     const int box_rows = gcd_int(sh.page_size, BN);
-    CUtensorMap tq, tk, tv, to;
+    CUtensorMap tq, tk, tv, to, tm;
     const long long pool_rows = static_cast<long long>(sh.num_pages) * sh.H_kv * sh.page_size;
     const bool q_ok = c.cu_q ? make_map_tokens(&tq, c.q, sh.H_q, c.total_q, Lt)
                              : make_map(&tq, c.q, static_cast<long long>(sh.B) * sh.H_q * sh.L, Lt);
@@ -1288,6 +1402,11 @@ pa_status prefill_launch(const Call& c) {
                              : make_map(&to, c.out, static_cast<long long>(sh.B) * sh.H_q * sh.L, kStageRows);
     if (!q_ok || !o_ok || !make_map(&tk, c.kp, pool_rows, box_rows) ||
         !make_map(&tv, c.vp, pool_rows, box_rows))
+        return PA_ERR_CUDA;
+    // the explicit mask [B * H_q * L rows, mask_S columns] fp32, in boxes of
+    // 32 columns x Lt rows (one head's rows of a query tile)
+    tm = to;
+    if (c.mask && !make_map_mask(&tm, c.mask, static_cast<long long>(sh.B) * sh.H_q * sh.L, c.mask_S, Lt))
         return PA_ERR_CUDA;
 
     static int attr_done[64] = {0};
@@ -1382,13 +1501,13 @@ pa_status prefill_launch(const Call& c) {
     const unsigned grid = static_cast<unsigned>(std::min<long long>(items, c.dev.sm_count));
     if (c.ev_before && cudaEventRecord(c.ev_before, c.stream) != cudaSuccess) return PA_ERR_CUDA;
     if (c.cu_q)  // (a ragged batch takes no explicit mask)
-        prefill_tile_kernel<false, true, false><<<grid, kThreads, kSmemBytes, c.stream>>>(tq, tk, tv, to, p);
+        prefill_tile_kernel<false, true, false><<<grid, kThreads, kSmemBytes, c.stream>>>(tq, tk, tv, to, tm, p);
     else if (c.mask)
-        prefill_tile_kernel<true, false, false><<<grid, kThreads, kSmemBytes, c.stream>>>(tq, tk, tv, to, p);
+        prefill_tile_kernel<true, false, false><<<grid, kThreads, kSmemBytes, c.stream>>>(tq, tk, tv, to, tm, p);
     else if (split)
-        prefill_tile_kernel<false, false, true><<<grid, kThreads, kSmemBytes, c.stream>>>(tq, tk, tv, to, p);
+        prefill_tile_kernel<false, false, true><<<grid, kThreads, kSmemBytes, c.stream>>>(tq, tk, tv, to, tm, p);
     else
-        prefill_tile_kernel<false, false, false><<<grid, kThreads, kSmemBytes, c.stream>>>(tq, tk, tv, to, p);
+        prefill_tile_kernel<false, false, false><<<grid, kThreads, kSmemBytes, c.stream>>>(tq, tk, tv, to, tm, p);
     if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
     if (c.ev_after && cudaEventRecord(c.ev_after, c.stream) != cudaSuccess) return PA_ERR_CUDA;
     if (split) {  // merge the key chunks (may launch while the tiles finish)

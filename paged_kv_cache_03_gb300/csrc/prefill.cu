@@ -915,8 +915,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ====================== mask stager (warp 2, with a mask) ===================
         // Per key tile and query tile (A, then B), two half-tiles of 64 keys
         // into the two mask slots in turn: per 32-key column block with a
-        // visible key, G boxes (one per head) of Lt rows.  The next key
-        // tile's boxes are prefetched into L2 meanwhile.
+        // visible key, G boxes (one per head) of Lt rows.  (Prefetching the
+        // next key tile's boxes into L2 as well, with TMA or per-thread
+        // prefetches, made the masked prefill 7-60% slower: measured.)
         const uint64_t pol_m = l2_policy_evict_first();
         if (lane == 0) tc::prefetch_tensormap(&tm_m);
         int n = 0;               // half-tiles staged
@@ -935,11 +936,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int t = 0; t < 2 && ok; ++t) {
                     if (j >= w.nkc_t[t]) continue;
                     const int k0 = (w.j0 + j) * BN;
-                    if (lane == 0 && j + 1 < w.nkc_t[t])  // the next key tile, into L2
-                        for (int cb = 0; cb < 4; ++cb)
-                            if (k0 + BN + 32 * cb <= lim_t[t])
-                                for (int g = 0; g < p.G; ++g)
-                                    tc::tma_prefetch_2d(&tm_m, k0 + BN + 32 * cb, row_of(w, t, g));
                     for (int hh = 0; hh < 2; ++hh) {
                         const int ms = n & 1;  // (= hh: every key tile stages two halves)
                         if (n >= 2 && !warp_wait(bar(kMaskEmpty + ms), ((n >> 1) - 1) & 1)) {

@@ -80,22 +80,24 @@ constexpr int kOffV = kOffK + 2 * kTile;    // slot s at kOffV + s * kTile
 constexpr int kOffStage = kOffV + 2 * kTile;
 constexpr int kStageRows = 16;
 constexpr int kOffBar = kOffStage + 2 * 4 * kStageRows * 256;
-// With an explicit mask the kernel keeps one K slot and stages the mask in
-// two 32 KB slots instead: the second K slot and the output staging (whose
-// rows that instance stores directly).  A slot holds 64 keys x 128 rows of
-// fp32 as two 32-key column blocks of 16 KB, each G boxes of Lt rows x 128
-// bytes, 128-byte swizzled.
-constexpr int kOffMask0 = kOffK + kTile;
-constexpr int kOffMask1 = kOffStage;
+// With an explicit mask the kernel keeps one K slot and one V slot and
+// stages the mask in three 32 KB slots instead: the second K slot, the
+// second V slot and the output staging (whose rows that instance stores
+// directly).  A slot holds 64 keys x 128 rows of fp32 as two 32-key column
+// blocks of 16 KB, each G boxes of Lt rows x 128 bytes, 128-byte swizzled.
+constexpr int kMaskSlots = 3;
+__host__ __device__ constexpr int mask_off(int s) {
+    return s == 0 ? kOffK + kTile : s == 1 ? kOffV + kTile : kOffStage;
+}
 constexpr int kMaskHalf = 64;  // keys per mask slot
-// K/V ring positions: with a mask K has one slot, else two
-template <bool kMask>
+// K/V ring positions: with a mask one slot, else two
+template <bool kOne>
 struct KRing {
-    static constexpr int kSlots = kMask ? 1 : 2;
-    __device__ static int slot(int g) { return kMask ? 0 : (g & 1); }
-    __device__ static uint32_t full_parity(int g) { return kMask ? (g & 1) : ((g >> 1) & 1); }
+    static constexpr int kSlots = kOne ? 1 : 2;
+    __device__ static int slot(int g) { return kOne ? 0 : (g & 1); }
+    __device__ static uint32_t full_parity(int g) { return kOne ? (g & 1) : ((g >> 1) & 1); }
     // the wait for the slot to be free before tile g is loaded into it
-    __device__ static uint32_t empty_parity(int g) { return kMask ? ((g - 1) & 1) : (((g >> 1) - 1) & 1); }
+    __device__ static uint32_t empty_parity(int g) { return kOne ? ((g - 1) & 1) : (((g >> 1) - 1) & 1); }
 };
 enum Bar {
     kQFull = 0,
@@ -113,11 +115,11 @@ enum Bar {
     kItemFull = 20,   // + slot: a work item is published
     kItemEmpty = 22,  // + slot: every role has read it
     // A slot's fills alternate between the query tiles, so each tile waits on
-    // a full barrier of its own: it then waits for that barrier's phases in
-    // order, never for one two phases ahead of the barrier.
-    kMaskFull = 24,   // + 2 * tile + slot: the tile's mask half-tile is staged
-    kMaskEmpty = 28,  // + slot: the half-tile in the slot has been read
-    kNumBars = 30     // (even: what follows stays 16-byte aligned)
+    // full barriers of its own: it then waits for their phases in order,
+    // never for one two phases ahead of the barrier.
+    kMaskFull = 24,   // + 3 * tile + slot: the tile's mask half-tile is staged
+    kMaskEmpty = 30,  // + slot: the half-tile in the slot has been read
+    kNumBars = 34     // (even: what follows stays 16-byte aligned)
 };
 constexpr int kOffItems = kOffBar + kNumBars * 8;  // 2 slots x 32 bytes
 constexpr int kOffTmemSlot = kOffItems + 64;
@@ -383,9 +385,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             // the MMA thread + 8 softmax warps (+ warps 2 and 3 for remainder
             // rows, + warp 2 that stages the mask)
             mbar_init(bar(kItemEmpty + s), (kSplit && p.nrem > 0) ? 11 : kMask ? 10 : 9);
-            mbar_init(bar(kMaskFull + s), 1);
-            mbar_init(bar(kMaskFull + 2 + s), 1);
-            mbar_init(bar(kMaskEmpty + s), 4);
+            if (kMask) {
+                for (int t = 0; t < 2; ++t) mbar_init(bar(kMaskFull + 3 * t + s), 1);
+                mbar_init(bar(kMaskEmpty + s), 4);
+            }
+        }
+        if (kMask) {  // the third mask slot
+            for (int t = 0; t < 2; ++t) mbar_init(bar(kMaskFull + 3 * t + 2), 1);
+            mbar_init(bar(kMaskEmpty + 2), 4);
         }
         mbar_init(bar(kMmaDone), 1);
         mbar_init(bar(kVTail), 1);
@@ -419,6 +426,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         return Item{a.x, a.y, a.z, a.w, c.x, c.y, c.z, c.w & 1, c.w >> 1};
     };
     using KR = KRing<kMask>;
+    using VR = KRing<kMask>;
     auto take_item = [&](int k, Item& it) -> bool {  // a whole warp
         if (!warp_wait(bar(kItemFull + (k & 1)), (k >> 1) & 1)) return false;
         it = read_item(k);
@@ -512,16 +520,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 issue_boxes(&tm_k, base + kOffK + ks * kTile, rows_cur, lane, p.box_rows,
                             bar(kKFull + ks), pol_kv);
                 kdone = gk + 1;
-                if (gk >= 2 && !warp_wait(bar(kVEmpty + s), ((gk >> 1) - 1) & 1)) {
+                const int vs = VR::slot(gk);
+                if (gk >= VR::kSlots && !warp_wait(bar(kVEmpty + vs), VR::empty_parity(gk))) {
                     if (lane == 0) give_up(p, abort_flag);
                     ok = false;
                     break;
                 }
                 const bool vtail = j == tail_tile;
-                const uint32_t vbar = vtail ? bar(kVTail) : bar(kVFull + s);
+                const uint32_t vbar = vtail ? bar(kVTail) : bar(kVFull + vs);
                 if (lane == 0) mbar_arrive_expect_tx(vbar, bytes_cur);
                 __syncwarp();
-                issue_boxes(&tm_v, base + kOffV + s * kTile, rows_cur, lane, p.box_rows, vbar,
+                issue_boxes(&tm_v, base + kOffV + vs * kTile, rows_cur, lane, p.box_rows, vbar,
                             pol_kv);
                 // rows of the next tile, looked up before waiting for a free slot
                 if (jj + 1 < w.nkc) tile_boxes(p, it.b, it.kvh, it.S, j + 1, lane, rows_next, bytes_next);
@@ -534,7 +543,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ++vtails;
                     for (int r = it.S - j * BN + lane; r < BN; r += 32) {
                         uint4* const vrow =
-                            reinterpret_cast<uint4*>(sbase + kOffV + s * kTile + r * 128);
+                            reinterpret_cast<uint4*>(sbase + kOffV + vs * kTile + r * 128);
 #pragma unroll
                         for (int q = 0; q < 8; ++q) {
                             vrow[q] = make_uint4(0u, 0u, 0u, 0u);
@@ -543,7 +552,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     fence_proxy_async_smem();  // the MMA reads them through the async proxy
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(bar(kVFull + s));
+                    if (lane == 0) mbar_arrive(bar(kVFull + vs));
                 }
                 vdone = gk + 1;
 #pragma unroll
@@ -556,8 +565,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (qn > 0 && !mbar_wait(bar(kQFull), (qn - 1) & 1)) give_up(p, abort_flag);
         for (int g = max(0, kdone - KR::kSlots); g < kdone; ++g)
             if (!mbar_wait(bar(kKFull + KR::slot(g)), KR::full_parity(g))) give_up(p, abort_flag);
-        for (int g = max(0, vdone - 2); g < vdone; ++g)
-            if (!mbar_wait(bar(kVFull + (g & 1)), (g >> 1) & 1)) give_up(p, abort_flag);
+        for (int g = max(0, vdone - VR::kSlots); g < vdone; ++g)
+            if (!mbar_wait(bar(kVFull + VR::slot(g)), VR::full_parity(g))) give_up(p, abort_flag);
         // the last CTA to stop claiming resets the counters for the next call
         if (lane == 0) {
             __threadfence();
@@ -596,7 +605,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // The next Q.K^T into those columns is issued after this product,
             // and the tensor core runs one thread's MMAs in issue order.
             auto pv = [&](int t, int j, int gk) {
-                const uint64_t dv = (gk & 1) ? dV1 : dV0;
+                const uint64_t dv = VR::slot(gk) ? dV1 : dV0;
                 const uint32_t d = tmem + col_o(t), a = tmem + col_s(t);
                 if (j > 0) tc::mma_bf16_ts_c<1>(d, a, dv, idO);
                 else tc::mma_bf16_ts_c<0>(d, a, dv, idO);
@@ -629,7 +638,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (nk == 1) tc::commit(bar(kQEmpty));  // all of the item's Q.K^T issued
                 for (int j = 0; ok && j < nk; ++j) {
                     const int gk = kt + j;
-                    ok = mbar_wait(bar(kVFull + (gk & 1)), (gk >> 1) & 1);
+                    ok = mbar_wait(bar(kVFull + VR::slot(gk)), VR::full_parity(gk));
                     if (!ok || *abort_flag) break;
                     const bool more = j + 1 < nk;
                     if (j < nk_t[0]) {
@@ -657,7 +666,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tc::fence_after_sync();
                         pv(1, j, gk);
                     }
-                    tc::commit(bar(kVEmpty + (gk & 1)));
+                    tc::commit(bar(kVEmpty + VR::slot(gk)));
                     if (more) {
                         if (j + 1 < nk_t[1]) qk(1, gk + 1);
                         tc::commit(bar(kKEmpty + KR::slot(gk + 1)));
@@ -687,7 +696,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float cs = kMask ? 1.f : c;
         int sc = 0;               // S fills of this tile consumed (kSFull phases)
         int pvA = 0, pvB = 0;     // P.V products of tiles A and B in earlier items (kODone phases)
-        int mask_steps = 0;       // this tile's mask key tiles in earlier items
+        int mask_ts = 0;          // mask (query tile, key tile) steps staged for earlier items
+        int mf0 = 0, mf1 = 0, mf2 = 0;  // this tile's mask fills consumed per slot
         bool ok = true;
         Item it;
         for (int k = 0; ok; ++k) {
@@ -722,14 +732,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int cc = 0; cc < 4; ++cc) tc::ld32(trow + col_s(t) + cc * 32, x[cc]);
                 tc::wait_ld();
                 if constexpr (kMask) {  // s * scale * log2 e + mask * log2 e
-                    // the tile's mask, two staged halves of 64 keys (half h in
-                    // slot h), the tile's (mask_steps + j)-th fill of each slot
+                    // the tile's mask, two staged halves of 64 keys; the stager
+                    // fills the slots in turn, per key tile tile A's halves,
+                    // then tile B's
+                    const int n0 = 2 * (mask_ts + min(j, nkA) + min(j, nkB) + (t == 1 && j < nkA ? 1 : 0));
 #pragma unroll
                     for (int hh = 0; hh < 2; ++hh) {
-                        const int ms = hh;
-                        ok = warp_wait(bar(kMaskFull + 2 * t + ms), (mask_steps + j) & 1);
+                        const int ms = (n0 + hh) % kMaskSlots;
+                        const int f = ms == 0 ? mf0 : ms == 1 ? mf1 : mf2;  // this tile's fills of the slot so far
+                        ok = warp_wait(bar(kMaskFull + 3 * t + ms), f & 1);
                         if (!ok) break;
-                        const uint32_t sb = base + (ms ? kOffMask1 : kOffMask0);
+                        if (ms == 0) ++mf0;
+                        else if (ms == 1) ++mf1;
+                        else ++mf2;
+                        const uint32_t sb = base + mask_off(ms);
 #pragma unroll
                         for (int cb = 0; cb < 2; ++cb) {
                             const int cc = 2 * hh + cb;
@@ -907,7 +923,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             sc += nkt;
             pvA += nkA;
             pvB += nkB;
-            mask_steps += nkt;
+            mask_ts += nkA + nkB;
         }
         if (!ok && lane == 0) give_up(p, abort_flag);
         if (lane == 0) tc::bulk_wait_all();  // the output stores have landed
@@ -920,8 +936,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // prefetches, made the masked prefill 7-60% slower: measured.)
         const uint64_t pol_m = l2_policy_evict_first();
         if (lane == 0) tc::prefetch_tensormap(&tm_m);
-        int n = 0;               // half-tiles staged
-        int fills[2] = {0, 0};   // key tiles staged per query tile
+        int n = 0;                     // half-tiles staged
+        int fills[2][kMaskSlots] = {};  // per query tile and slot
         bool ok = true;
         Item it;
         auto row_of = [&](const ItemWork& w, int t, int g) {
@@ -937,8 +953,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (j >= w.nkc_t[t]) continue;
                     const int k0 = (w.j0 + j) * BN;
                     for (int hh = 0; hh < 2; ++hh) {
-                        const int ms = n & 1;  // (= hh: every key tile stages two halves)
-                        if (n >= 2 && !warp_wait(bar(kMaskEmpty + ms), ((n >> 1) - 1) & 1)) {
+                        const int ms = n % kMaskSlots;
+                        if (n >= kMaskSlots &&
+                            !warp_wait(bar(kMaskEmpty + ms), ((n / kMaskSlots) - 1) & 1)) {
                             ok = false;
                             break;
                         }
@@ -949,8 +966,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         int nb = 0;  // column blocks with a visible key
                         for (int cb = 0; cb < 2; ++cb) nb += (k0 + kMaskHalf * hh + 32 * cb <= lim_t[t]);
                         if (lane == 0) {
-                            const uint32_t sb = base + (ms ? kOffMask1 : kOffMask0);
-                            const uint32_t full = bar(kMaskFull + 2 * t + ms);
+                            const uint32_t sb = base + mask_off(ms);
+                            const uint32_t full = bar(kMaskFull + 3 * t + ms);
                             mbar_arrive_expect_tx(full, static_cast<uint32_t>(nb * BM * 128));
                             for (int cb = 0; cb < nb; ++cb)
                                 for (int g = 0; g < p.G; ++g)
@@ -959,17 +976,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                     full, pol_m);
                         }
                         __syncwarp();
+                        ++fills[t][ms];
                         ++n;
                     }
-                    if (ok) ++fills[t];
                 }
             }
         }
         if (!ok && lane == 0) give_up(p, abort_flag);
         // let the staged copies land before leaving
         for (int t = 0; t < 2; ++t)
-            for (int hh = 0; hh < 2 && fills[t] > 0; ++hh)
-                if (!mbar_wait(bar(kMaskFull + 2 * t + hh), (fills[t] - 1) & 1)) give_up(p, abort_flag);
+            for (int ms = 0; ms < kMaskSlots; ++ms)
+                if (fills[t][ms] > 0 && !mbar_wait(bar(kMaskFull + 3 * t + ms), (fills[t][ms] - 1) & 1))
+                    give_up(p, abort_flag);
     } else if (kSplit && (warp == 2 || warp == 3)) {
         // ====================== remainder rows (warps 2, 3) =====================
         // S^T = K Q^T and O^T += V^T P^T with mma m16n8k16 (16 keys x 8 rows):

@@ -86,8 +86,8 @@ pa_status decode_launch(const Call& c);
 // ---- prefill schedule (tcgen05 tensor cores) ------------------------------
 bool prefill_supported(const pa_shape& sh);
 // Key chunks per query-tile pair ([B, H_q, L, D] layout, no mask): more than 1
-// when the pairs alone would not fill the GPU twice; their partials follow the
-// ragged batch's plan in the workspace.
+// when at least two chunks per pair still give every item an SM of its own;
+// their partials follow the ragged batch's plan in the workspace.
 int tile_nsplit(const pa_shape& sh, int sm_count);
 // Rows of a last query tile of at most 8 rows that the tile schedule gives to
 // the warp-level tensor cores of the last full pair's CTA (0: none).

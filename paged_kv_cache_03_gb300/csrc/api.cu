@@ -73,19 +73,21 @@ bool scale_ok(float scale) { return scale >= 0.f && scale <= FLT_MAX; }
 int choose(const pa_shape& s) {
     if (s.dtype != PA_BF16 || !prefill_supported(s)) return PA_SCHED_DECODE;
     const long long rows = static_cast<long long>(s.H_q / s.H_kv) * s.L;
-    // Measured crossover (operator sweep over G in {1, 4}, L in 1..128,
-    // contexts 64..32768, B in {1, 4, 8, 64, 256}): with more than 4 query
-    // rows per kv head the tensor-core tiles win at almost every context
-    // length (1.3x at 8 rows, 2-10x beyond); with at most 4 rows the page walk
-    // on CUDA cores wins, except on calls so small that the tile schedule's
-    // lower fixed cost decides: B * H_kv * context capacity up to 64K token
-    // rows and a capacity of at most 1024 keys (beyond it one tile CTA per
-    // (sequence, kv head) walks too many key tiles in turn: at B = 1 and 4096
-    // keys the tiles take 62 us, the page walk 37 us).
+    // Measured crossover (operator sweep, G = 4, L in {1, 2, 4}, contexts 256
+    // to 16384, B in {1, 8, 64}, H_kv = 8): with more than 4 query rows per kv
+    // head the tensor-core tiles win everywhere (1.5x at 8 rows and B = 8 over
+    // 16384 keys, 2-3x beyond); with at most 4 rows the page walk wins over a
+    // real batch, except (1) on calls so small that the tile schedule's lower
+    // fixed cost decides: B * H_kv * context capacity up to 64K token rows and
+    // a capacity of at most 1024 keys, and (2) when there are at most 8
+    // (sequence, kv head) pairs: the tiles then cut each pair's keys into up
+    // to 16 chunks on SMs of their own (B = 1 over 16384 keys: tiles 33 us,
+    // page walk 42 us; B = 8 over 4096 keys: tiles 44 us, page walk 41 us).
     if (rows > kMixedDecodeRows) return PA_SCHED_PREFILL;
     const long long cap = static_cast<long long>(s.max_pages_per_seq) * s.page_size;
     const long long work = static_cast<long long>(s.B) * s.H_kv * cap;
-    return work <= 65536 && cap <= 1024 ? PA_SCHED_PREFILL : PA_SCHED_DECODE;
+    if (work <= 65536 && cap <= 1024) return PA_SCHED_PREFILL;
+    return static_cast<long long>(s.B) * s.H_kv <= 8 ? PA_SCHED_PREFILL : PA_SCHED_DECODE;
 }
 
 }  // namespace

@@ -117,12 +117,17 @@ def test_schedule_rule():
     assert B.pa_choose_schedule(good_shape(L=2048, **decode_cfg)) == B.PA_SCHED_PREFILL
     # a tiny call: the tile schedule's lower fixed cost wins even for one row
     assert B.pa_choose_schedule(good_shape(L=1)) == B.PA_SCHED_PREFILL
-    # ... but not over long contexts: one tile CTA per (sequence, kv head) then
-    # walks too many key tiles (B = 1, 4096 keys: tiles 62 us, page walk 37 us)
-    one_long = dict(B=1, H_q=32, H_kv=8, num_pages=64, page_size=128)
+    # at most 8 (sequence, kv head) pairs: the tiles split each pair's keys over
+    # SMs of their own, at any context (B = 1, 16384 keys: tiles 33 us, page walk 42 us)
+    one_long = dict(B=1, H_q=32, H_kv=8, num_pages=256, page_size=128)
     assert B.pa_choose_schedule(good_shape(L=1, max_pages_per_seq=8, **one_long)) == \
         B.PA_SCHED_PREFILL
-    assert B.pa_choose_schedule(good_shape(L=1, max_pages_per_seq=32, **one_long)) == \
+    assert B.pa_choose_schedule(good_shape(L=1, max_pages_per_seq=128, **one_long)) == \
+        B.PA_SCHED_PREFILL
+    # ... but over a batch of 8 sequences and long contexts the page walk
+    # (B = 8, 4096 keys: tiles 44 us, page walk 41 us)
+    eight_long = dict(B=8, H_q=32, H_kv=8, num_pages=256, page_size=128)
+    assert B.pa_choose_schedule(good_shape(L=1, max_pages_per_seq=32, **eight_long)) == \
         B.PA_SCHED_DECODE
     # fp32 and shapes the tiles do not take (page size not a multiple of 8)
     assert B.pa_choose_schedule(good_shape(L=2048, dtype=B.PA_F32)) == B.PA_SCHED_DECODE

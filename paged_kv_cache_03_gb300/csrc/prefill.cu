@@ -1034,18 +1034,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 for (int jj = 0; jj < w.nkc; ++jj) {
                     const int j = w.j0 + jj, gk = kt + jj, s = gk & 1;
-                    ok = warp_wait(bar(kKFull + s), (gk >> 1) & 1) &&
-                         warp_wait(bar(kVFull + s), (gk >> 1) & 1);
+                    // S^T as soon as K lands; K is released before P.V waits for V
+                    ok = warp_wait(bar(kKFull + s), (gk >> 1) & 1);
                     if (!ok || aborted(abort_flag)) {
                         ok = false;
                         break;
                     }
+                    const uint32_t kb = base + kOffK + s * kTile, vb = base + kOffV + s * kTile;
+                    const int kw0 = 64 * wr;  // first key of the warp in the tile
+                    float sacc[4][4];
                     if (rem) {
                         // the warp's 64 keys as 4 groups of 16, interleaved so
                         // that 4 independent accumulation chains are in flight
-                        const uint32_t kb = base + kOffK + s * kTile, vb = base + kOffV + s * kTile;
-                        const int kw0 = 64 * wr;  // first key of the warp in the tile
-                        float sacc[4][4];
 #pragma unroll
                         for (int grp = 0; grp < 4; ++grp)
                             sacc[grp][0] = sacc[grp][1] = sacc[grp][2] = sacc[grp][3] = 0.f;
@@ -1064,6 +1064,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 for (int grp = 0; grp < 4; ++grp) mma_16816(sacc[grp], a[grp], qf[ks][0], qf[ks][1]);
                             }
                         }
+                    }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar(kKEmpty + s));
+                    ok = warp_wait(bar(kVFull + s), (gk >> 1) & 1);
+                    if (!ok || aborted(abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    if (rem) {
                         // scores in log2 units, masked past each row's last key;
                         // one max over the 64 keys per row
                         float mt0 = neg_inf(), mt1 = neg_inf();
@@ -1125,10 +1134,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                     }
                     __syncwarp();
-                    if (lane == 0) {
-                        mbar_arrive(bar(kKEmpty + s));
-                        mbar_arrive(bar(kVEmpty + s));
-                    }
+                    if (lane == 0) mbar_arrive(bar(kVEmpty + s));
                 }
                 if (!ok) break;
                 kt += w.nkc;

@@ -96,6 +96,21 @@ def test_masked_workloads_auto(oracle_lib, name):
     gu.assert_parity(got, ref, "bf16", f"{name} masked auto")
 
 
+@pytest.mark.parametrize("G,L", [(1, 130), (2, 90), (8, 50), (16, 30)])
+def test_masked_tiles_every_group_size(oracle_lib, G, L):
+    """The tile schedule's mask stager stages one box per head of Lt = 128 / G
+    rows: every GQA group size it takes, causal, every element."""
+    H_kv = 2 if G <= 8 else 1
+    inp = synth.generate(B=2, H_q=G * H_kv, H_kv=H_kv, L=L, D=128, page_size=32,
+                         context_lens=[L, 400], seed=100 + G, name=f"mask-G{G}")
+    mask = synth.additive_mask(inp.B * inp.H_q, inp.L, _s_mask(inp, 4), 110 + G)
+    got = gu.out_to_f64(run_masked(inp, mask, B.PA_SCHED_PREFILL))
+    ref = oracle_lib.paged_attention(inp.query, inp.key_pages, inp.value_pages,
+                                     inp.block_table, inp.context_lens, inp.scale, True,
+                                     mask=mask)
+    gu.assert_parity(got, ref, "bf16", f"mask G={G} tiles")
+
+
 @pytest.mark.parametrize("sched", ["decode", "prefill"])
 def test_fully_masked_row_outputs_zero(oracle_lib, sched):
     inp = _small_cases()[1]

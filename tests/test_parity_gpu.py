@@ -428,6 +428,28 @@ def test_tile_key_split_and_last_tile_rows(oracle_lib, name, kw, causal):
         check(oracle_lib, inp, sched, what=f"{name} causal={causal} sched {sched}")
 
 
+# ---- every GQA group size the tiles take ---------------------------------------
+GROUP_CASES = [
+    # (name, kwargs): G = H_q / H_kv from 1 to 16, so a query tile holds 128, 64,
+    # 32, 16 or 8 positions; the epilogue's tiled stores take rounds of 16 rows of
+    # one head (G <= 8) or fall back to direct stores (G = 16), and tiles past
+    # the last query rows take the direct path too
+    ("G1_Lt128", dict(B=1, H_q=4, H_kv=4, L=300, page_size=128, context_lens=[1000])),
+    ("G2_Lt64", dict(B=2, H_q=8, H_kv=4, L=150, page_size=64, context_lens=[150, 700])),
+    ("G8_Lt16", dict(B=2, H_q=16, H_kv=2, L=100, page_size=32, context_lens=[100, 300])),
+    ("G16_Lt8", dict(B=2, H_q=16, H_kv=1, L=40, page_size=16, context_lens=[40, 200])),
+]
+
+
+@pytest.mark.parametrize("name,kw", GROUP_CASES, ids=[c[0] for c in GROUP_CASES])
+@pytest.mark.parametrize("causal", [True, False])
+def test_tile_schedule_every_group_size(oracle_lib, name, kw, causal):
+    """The tile schedule forced on each GQA group size it takes, causal and
+    not: every element against the oracle."""
+    inp = synth.generate(D=128, seed=sum(map(ord, name)) + 53, causal=causal, name=name, **kw)
+    check(oracle_lib, inp, B.PA_SCHED_PREFILL, what=f"{name} causal={causal}")
+
+
 # ---- mask=None with more queries than keys ---------------------------------------
 NONCAUSAL_LONG_L = [
     # (name, kwargs): L > context_len for some or all sequences, causal off

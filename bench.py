@@ -46,6 +46,7 @@ from __future__ import annotations
 
 import argparse
 import hashlib
+import re
 import json
 import math
 import os
@@ -202,12 +203,20 @@ KERNEL_SOURCES = {
 }
 
 
+def _code_only(text: str) -> str:
+    """The source without comments and blank lines (so that a comment edit
+    does not retire the recorded counters)."""
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    lines = (re.sub(r"//.*", "", ln).rstrip() for ln in text.splitlines())
+    return "\n".join(ln for ln in lines if ln.strip())
+
+
 def kernel_source_digest(kernel: str) -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "paged_kv_cache_03_gb300", "csrc")
     for fn in sorted(KERNEL_SOURCES[kernel]):
-        with open(os.path.join(csrc, fn), "rb") as f:
-            h.update(fn.encode() + b"\0" + f.read())
+        with open(os.path.join(csrc, fn), encoding="utf-8") as f:
+            h.update(fn.encode() + b"\0" + _code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 

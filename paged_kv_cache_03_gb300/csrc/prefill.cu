@@ -39,6 +39,15 @@
 //     two tiles never wait for each other's products), running sum in fp32;
 //     at the end O/l -> bf16 -> global.  Whole K/V tiles past a tile's last
 //     causal frontier are skipped.
+//   * Epilogue: each warp's output rows go out 16 at a time through a 4 KB
+//     shared-memory slice and tiled TMA stores (one head's consecutive
+//     positions); other rows are stored directly.
+//   * Few, long query tiles: each pair's keys are cut into chunks (one wave
+//     of items), each writing fp32 partials that tile_combine_kernel merges;
+//     a last query tile of at most 8 rows rides on warps 2 and 3 of the last
+//     full pair's CTA (warp-level MMA).
+//   * With an explicit mask, warp 2 stages the mask tiles into shared memory
+//     with TMA, a slot ring of three (the instance keeps one K and one V slot).
 //   * Boxes are copied whole, so a sequence's last K/V tile can carry page
 //     rows past its context (unused slots, any contents).  Their scores are
 //     masked to -inf.  Their V rows would still meet a weight of exactly 0,

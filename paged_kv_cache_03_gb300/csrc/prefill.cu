@@ -939,7 +939,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (kMask && warp == 2) {
         // ====================== mask stager (warp 2, with a mask) ===================
         // Per key tile and query tile (A, then B), two half-tiles of 64 keys
-        // into the two mask slots in turn: per 32-key column block with a
+        // into the three mask slots in turn: per 32-key column block with a
         // visible key, G boxes (one per head) of Lt rows.  (Prefetching the
         // next key tile's boxes into L2 as well, with TMA or per-thread
         // prefetches, made the masked prefill 7-60% slower: measured.)

@@ -1210,23 +1210,53 @@ __global__ void __launch_bounds__(128) tile_combine_kernel(const PrefillParams p
             po = p.rem_o + pr * kD;
         }
     }
-    float M = neg_inf();
-    for (int c = lane; c < ns; c += 32) M = fmaxf(M, ml[c].x);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
     float den = 0.f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (M != neg_inf()) {
-        for (int c = 0; c < ns; ++c) {
-            const float2 v = ml[c];
-            if (v.x == neg_inf()) continue;
-            const float a = fast_exp2(v.x - M);
-            den += a * v.y;
-            const float4 o = *reinterpret_cast<const float4*>(po + c * kD + 4 * lane);
-            acc.x += a * o.x;
-            acc.y += a * o.y;
-            acc.z += a * o.z;
-            acc.w += a * o.w;
+    constexpr int kFew = 8;
+    if (ns <= kFew) {
+        // few chunks: every load goes out before the first use
+        float2 v[kFew];
+        float4 o[kFew];
+#pragma unroll
+        for (int c = 0; c < kFew; ++c)
+            if (c < ns) {
+                v[c] = ml[c];
+                o[c] = *reinterpret_cast<const float4*>(po + c * kD + 4 * lane);
+            }
+        float M = neg_inf();
+#pragma unroll
+        for (int c = 0; c < kFew; ++c)
+            if (c < ns) M = fmaxf(M, v[c].x);
+        if (M != neg_inf()) {
+#pragma unroll
+            for (int c = 0; c < kFew; ++c) {
+                // (a chunk without keys wrote no o row: skipped, not weighted by 0)
+                if (c >= ns || v[c].x == neg_inf()) continue;
+                const float a = fast_exp2(v[c].x - M);
+                den += a * v[c].y;
+                acc.x += a * o[c].x;
+                acc.y += a * o[c].y;
+                acc.z += a * o[c].z;
+                acc.w += a * o[c].w;
+            }
+        }
+    } else {
+        float M = neg_inf();
+        for (int c = lane; c < ns; c += 32) M = fmaxf(M, ml[c].x);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+        if (M != neg_inf()) {
+            for (int c = 0; c < ns; ++c) {
+                const float2 v = ml[c];
+                if (v.x == neg_inf()) continue;
+                const float a = fast_exp2(v.x - M);
+                den += a * v.y;
+                const float4 o = *reinterpret_cast<const float4*>(po + c * kD + 4 * lane);
+                acc.x += a * o.x;
+                acc.y += a * o.y;
+                acc.z += a * o.z;
+                acc.w += a * o.w;
+            }
         }
     }
     const float inv = den > 0.f ? 1.f / den : 0.f;

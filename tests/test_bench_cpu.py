@@ -113,3 +113,19 @@ def test_headline_rule():
     for k, v in (("workload", "prefill"), ("mask", True), ("schedule", "decode"),
                  ("no_causal", True), ("op", "append")):
         assert not bench.headline(argparse.Namespace(**{**base, k: v}))
+
+
+def test_recorded_traffic_follows_the_code_not_the_comments():
+    """The digest that keeps profiles/traffic.json tied to the kernels it was
+    measured on ignores comments and blank lines, and nothing else."""
+    src = "int f(int x) {\n    return x + 1;  // one more\n}\n"
+    assert bench._code_only(src) == bench._code_only(
+        "/* a new header\n   comment */\nint f(int x) {\n\n    return x + 1;\n}  // end\n")
+    assert bench._code_only(src) != bench._code_only(src.replace("x + 1", "x + 2"))
+    # a recorded entry whose digest no longer matches is not reported
+    with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+        recorded = json.load(f)
+    key = next(iter(recorded))
+    kernel, workload = key.split("@")
+    stale = recorded[key]["source_digest"] != bench.kernel_source_digest(kernel)
+    assert (bench.recorded_traffic(kernel, workload) is None) == stale

@@ -73,21 +73,24 @@ bool scale_ok(float scale) { return scale >= 0.f && scale <= FLT_MAX; }
 int choose(const pa_shape& s) {
     if (s.dtype != PA_BF16 || !prefill_supported(s)) return PA_SCHED_DECODE;
     const long long rows = static_cast<long long>(s.H_q / s.H_kv) * s.L;
-    // Measured crossover (operator sweep, G = 4, L in {1, 2, 4}, contexts 256
-    // to 16384, B in {1, 8, 64}, H_kv = 8): with more than 4 query rows per kv
-    // head the tensor-core tiles win everywhere (1.5x at 8 rows and B = 8 over
-    // 16384 keys, 2-3x beyond); with at most 4 rows the page walk wins over a
-    // real batch, except (1) on calls so small that the tile schedule's lower
-    // fixed cost decides: B * H_kv * context capacity up to 64K token rows and
-    // a capacity of at most 1024 keys, and (2) when there are at most 8
-    // (sequence, kv head) pairs: the tiles then cut each pair's keys into up
-    // to 16 chunks on SMs of their own (B = 1 over 16384 keys: tiles 33 us,
-    // page walk 42 us; B = 8 over 4096 keys: tiles 44 us, page walk 41 us).
+    // Measured crossover (operator sweep, G in {1, 4}, L in {1, 2, 4},
+    // contexts 256 to 16384, B in {1, 2, 4, 8, 64}, H_kv = 8): with more than
+    // 4 query rows per kv head the tensor-core tiles win everywhere (1.5x at 8
+    // rows and B = 8 over 16384 keys, 2-3x beyond).  With at most 4 rows the
+    // page walk wins over a real batch; the tiles, which cut the keys of few
+    // (sequence, kv head) pairs into chunks on SMs of their own, win (1) on
+    // calls so small that their lower fixed cost decides: B * H_kv * context
+    // capacity up to 64K token rows and a capacity of at most 1024 keys,
+    // (2) with at most 8 pairs at any context (B = 1 over 16384 keys: 29-33
+    // against 41-42 us), (3) with at most 32 pairs over at most 4096 keys
+    // (B = 4: 27 against 31-32 us; over 16384 keys the page walk, 60 against
+    // 69 us; B = 8 over 4096 keys: page walk 41 against 44 us).
     if (rows > kMixedDecodeRows) return PA_SCHED_PREFILL;
     const long long cap = static_cast<long long>(s.max_pages_per_seq) * s.page_size;
-    const long long work = static_cast<long long>(s.B) * s.H_kv * cap;
-    if (work <= 65536 && cap <= 1024) return PA_SCHED_PREFILL;
-    return static_cast<long long>(s.B) * s.H_kv <= 8 ? PA_SCHED_PREFILL : PA_SCHED_DECODE;
+    const long long pairs = static_cast<long long>(s.B) * s.H_kv;
+    if (pairs * cap <= 65536 && cap <= 1024) return PA_SCHED_PREFILL;
+    if (pairs <= 8 || (pairs <= 32 && cap <= 4096)) return PA_SCHED_PREFILL;
+    return PA_SCHED_DECODE;
 }
 
 }  // namespace

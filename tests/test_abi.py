@@ -124,8 +124,14 @@ def test_schedule_rule():
         B.PA_SCHED_PREFILL
     assert B.pa_choose_schedule(good_shape(L=1, max_pages_per_seq=128, **one_long)) == \
         B.PA_SCHED_PREFILL
-    # ... but over a batch of 8 sequences and long contexts the page walk
-    # (B = 8, 4096 keys: tiles 44 us, page walk 41 us)
+    # up to 32 pairs over at most 4096 keys: the tiles (B = 4, 4096 keys: 27 us
+    # against the page walk's 31 us), beyond that the page walk (B = 4, 16384
+    # keys: 69 against 60 us; B = 8, 4096 keys: 44 against 41 us)
+    four = dict(B=4, H_q=32, H_kv=8, num_pages=1024, page_size=128)
+    assert B.pa_choose_schedule(good_shape(L=1, max_pages_per_seq=32, **four)) == \
+        B.PA_SCHED_PREFILL
+    assert B.pa_choose_schedule(good_shape(L=1, max_pages_per_seq=128, **four)) == \
+        B.PA_SCHED_DECODE
     eight_long = dict(B=8, H_q=32, H_kv=8, num_pages=256, page_size=128)
     assert B.pa_choose_schedule(good_shape(L=1, max_pages_per_seq=32, **eight_long)) == \
         B.PA_SCHED_DECODE
